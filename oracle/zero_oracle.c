@@ -1,0 +1,358 @@
+/*
+ * zero_oracle.c - CPU oracle for the ZeRO-1/2 mixed-precision AdamW step.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE (see zero_oracle.h for who may load
+ * it, the passages each function follows and the readings R1-R9).
+ *
+ * Build: gcc -std=c11 -O2 -ffp-contract=off -fno-fast-math -fPIC -shared
+ * (-ffp-contract=off keeps every float * and + separately rounded, which is
+ * reading R2; without -ffast-math gcc never reassociates float arithmetic).
+ *
+ * Parity pins (tests/test_oracle_pins.py, tests/test_oracle_collectives.py):
+ *   oracle_bf16_rne        values fixed by the bf16 format (exact halfway
+ *                          cases, Inf, NaN, overflow), and torch's bf16 cast
+ *   oracle_make_scalars    closed forms at t=1 and t=2
+ *   oracle_adamw_elem      hand-worked 3-element 2-step example; closed form
+ *                          at step 1 with m=v=0; torch.optim.AdamW within
+ *                          1e-6 over 20 steps; zero-gradient invariants
+ *   oracle_avg_grad        identical micro-batches average exactly to the
+ *                          gradient; exact small-integer sums against a
+ *                          brute-force any-order sum
+ *   oracle_dp_step(_mt)    the above, plus thread-count invariance
+ *   oracle_zero_step       bit-identical to oracle_dp_step (the pages' ZeRO
+ *                          == DP result), pad elements untouched
+ *   oracle_reduce_scatter_sum  the worked 4-rank example 6/10/14/18
+ *   oracle_ring_allreduce  the 4-card demo 10*[0..7] and send volume
+ *                          2(p-1)/p
+ *   oracle_zero_bytes      the pages' exercises (7B/8 ranks, 7.5B/64 ranks,
+ *                          p=8 per-card units)
+ *   oracle_shard_len       hand-computed layouts (uneven 100,000,007 / 7)
+ */
+#define _POSIX_C_SOURCE 200809L
+#include "zero_oracle.h"
+
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- bf16 -- */
+
+static uint32_t f2u(float x) { uint32_t u; memcpy(&u, &x, 4); return u; }
+static float u2f(uint32_t u) { float x; memcpy(&x, &u, 4); return x; }
+
+/* Round a binary32 to the nearest bf16, ties to even (reading R7).  A bf16
+ * is the high 16 bits of a binary32, so rounding is: add half of the dropped
+ * range, plus one more when the kept part is odd (ties to even), then drop
+ * the low 16 bits.  A carry out of the fraction correctly bumps the exponent,
+ * and a carry out of the largest finite value gives Inf. */
+uint16_t oracle_bf16_rne(float x)
+{
+    uint32_t u = f2u(x);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0)
+        return (uint16_t)0x7FC0u;                     /* any NaN -> 0x7FC0 */
+    uint32_t kept_lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + kept_lsb;
+    return (uint16_t)(u >> 16);
+}
+
+float oracle_bf16_to_float(uint16_t h) { return u2f((uint32_t)h << 16); }
+
+/* ------------------------------------------------------------- scalars -- */
+
+void oracle_make_scalars(const oracle_hparams* hp, int64_t step, int32_t R,
+                         int32_t M, oracle_scalars* out)
+{
+    double t = (double)step;
+    double b1 = (double)hp->beta1, b2 = (double)hp->beta2;
+    double lr = (double)hp->lr, wd = (double)hp->weight_decay;
+    double bc1 = 1.0 - pow(b1, t);          /* bias correction of m */
+    double bc2 = 1.0 - pow(b2, t);          /* bias correction of v */
+    out->step_size = (float)(lr / bc1);
+    out->bc2_sqrt = (float)sqrt(bc2);
+    out->decay = (float)(1.0 - lr * wd);
+    out->beta1 = hp->beta1;
+    out->beta2 = hp->beta2;
+    out->one_minus_beta1 = (float)(1.0 - b1);
+    out->one_minus_beta2 = (float)(1.0 - b2);
+    out->eps = hp->eps;
+    out->denom_rm = (float)((double)R * (double)M);
+}
+
+/* ------------------------------------------------------- AdamW element -- */
+
+/* torch.optim.AdamW's algorithm for one element (reading R1), each float
+ * operation rounded on its own (reading R2):
+ *   w  <- w * (1 - lr*wd)                 decoupled weight decay
+ *   m  <- beta1*m + (1-beta1)*g           first moment
+ *   v  <- beta2*v + ((1-beta2)*g)*g       second moment
+ *   den = sqrt(v) / sqrt(1-beta2^t) + eps
+ *   w  <- w - (lr/(1-beta1^t)) * (m / den)                                 */
+void oracle_adamw_elem(const oracle_scalars* s, float g, float* w, float* m,
+                       float* v)
+{
+    float wd = *w * s->decay;
+    float a = s->beta1 * *m;
+    float b = s->one_minus_beta1 * g;
+    float m1 = a + b;
+    float c = s->beta2 * *v;
+    float d = s->one_minus_beta2 * g;
+    float e = d * g;
+    float v1 = c + e;
+    float root = sqrtf(v1);
+    float q = root / s->bc2_sqrt;
+    float den = q + s->eps;
+    float ratio = m1 / den;
+    float upd = s->step_size * ratio;
+    *w = wd - upd;
+    *m = m1;
+    *v = v1;
+}
+
+/* ----------------------------------------------------- gradient average -- */
+
+float oracle_avg_grad(const uint16_t* const* G, int32_t R, int32_t M,
+                      int64_t i, float denom_rm)
+{
+    float acc = 0.0f;
+    for (int32_t r = 0; r < R; ++r) {
+        /* local gradient accumulation of rank r, micro-batches in order */
+        float local = oracle_bf16_to_float(G[(int64_t)r * M + 0][i]);
+        for (int32_t j = 1; j < M; ++j)
+            local = local + oracle_bf16_to_float(G[(int64_t)r * M + j][i]);
+        /* ranks folded in ascending order */
+        acc = (r == 0) ? local : acc + local;
+    }
+    return acc / denom_rm;
+}
+
+/* -------------------------------------------------------------- DP step -- */
+
+static int check_args(int64_t n, int32_t R, int32_t M, const void* G,
+                      const void* W, const void* m, const void* v,
+                      const void* P, const void* hp, int64_t step)
+{
+    if (n < 0 || R < 1 || M < 1 || step < 1) return -1;
+    if (!hp) return -1;
+    if (n > 0 && (!G || !W || !m || !v || !P)) return -1;
+    return 0;
+}
+
+int oracle_dp_step(int64_t n, int32_t R, int32_t M,
+                   const uint16_t* const* G, float* W, float* m, float* v,
+                   uint16_t* const* P, const oracle_hparams* hp, int64_t step)
+{
+    if (check_args(n, R, M, G, W, m, v, P, hp, step)) return -1;
+    oracle_scalars s;
+    oracle_make_scalars(hp, step, R, M, &s);
+    for (int64_t i = 0; i < n; ++i) {
+        /* all-reduce: every rank sees the same averaged gradient */
+        float g = oracle_avg_grad(G, R, M, i, s.denom_rm);
+        oracle_adamw_elem(&s, g, &W[i], &m[i], &v[i]);
+        uint16_t p = oracle_bf16_rne(W[i]);
+        for (int32_t r = 0; r < R; ++r) P[r][i] = p;
+    }
+    return 0;
+}
+
+typedef struct {
+    int64_t lo, hi;
+    int32_t R, M;
+    const uint16_t* const* G;
+    float *W, *m, *v;
+    uint16_t* const* P;
+    const oracle_hparams* hp;
+    int64_t step;
+    int rc;
+} mt_job;
+
+static void* mt_run(void* arg)
+{
+    mt_job* jb = (mt_job*)arg;
+    int32_t RM = jb->R * jb->M;
+    const uint16_t** g = (const uint16_t**)malloc(sizeof(void*) * (size_t)RM);
+    uint16_t** p = (uint16_t**)malloc(sizeof(void*) * (size_t)jb->R);
+    if (!g || !p) { free(g); free(p); jb->rc = -2; return NULL; }
+    for (int32_t k = 0; k < RM; ++k) g[k] = jb->G[k] + jb->lo;
+    for (int32_t r = 0; r < jb->R; ++r) p[r] = jb->P[r] + jb->lo;
+    jb->rc = oracle_dp_step(jb->hi - jb->lo, jb->R, jb->M,
+                            (const uint16_t* const*)g, jb->W + jb->lo,
+                            jb->m + jb->lo, jb->v + jb->lo,
+                            (uint16_t* const*)p, jb->hp, jb->step);
+    free(g);
+    free(p);
+    return NULL;
+}
+
+int oracle_dp_step_mt(int64_t n, int32_t R, int32_t M,
+                      const uint16_t* const* G, float* W, float* m, float* v,
+                      uint16_t* const* P, const oracle_hparams* hp,
+                      int64_t step, int32_t nthreads)
+{
+    if (check_args(n, R, M, G, W, m, v, P, hp, step)) return -1;
+    if (nthreads <= 1 || n < nthreads)
+        return oracle_dp_step(n, R, M, G, W, m, v, P, hp, step);
+    mt_job* jobs = (mt_job*)calloc((size_t)nthreads, sizeof(mt_job));
+    pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+    char* started = (char*)calloc((size_t)nthreads, 1);
+    if (!jobs || !th || !started) { free(jobs); free(th); free(started); return -2; }
+    for (int32_t k = 0; k < nthreads; ++k) {
+        mt_job* jb = &jobs[k];
+        jb->lo = n * k / nthreads;
+        jb->hi = n * (k + 1) / nthreads;
+        jb->R = R; jb->M = M; jb->G = G; jb->W = W; jb->m = m; jb->v = v;
+        jb->P = P; jb->hp = hp; jb->step = step; jb->rc = 0;
+        if (pthread_create(&th[k], NULL, mt_run, jb) == 0)
+            started[k] = 1;
+        else
+            mt_run(jb);                  /* run this range on this thread */
+    }
+    int rc = 0;
+    for (int32_t k = 0; k < nthreads; ++k) {
+        if (started[k]) pthread_join(th[k], NULL);
+        if (jobs[k].rc) rc = jobs[k].rc;
+    }
+    free(jobs);
+    free(th);
+    free(started);
+    return rc;
+}
+
+/* ------------------------------------------------------------ ZeRO step -- */
+
+int64_t oracle_shard_len(int64_t n, int32_t R, int32_t align)
+{
+    if (n < 0 || R < 1 || align < 1) return -1;
+    int64_t per = (n + R - 1) / R;                       /* ceil(n / R) */
+    return (per + align - 1) / align * align;            /* roundup     */
+}
+
+int oracle_zero_step(int64_t n, int32_t R, int32_t M, int64_t S,
+                     const uint16_t* const* G, float* W, float* m, float* v,
+                     uint16_t* const* P, const oracle_hparams* hp,
+                     int64_t step)
+{
+    if (check_args(n, R, M, G, W, m, v, P, hp, step)) return -1;
+    if (S < 0 || S * R < n) return -1;
+    oracle_scalars s;
+    oracle_make_scalars(hp, step, R, M, &s);
+    int32_t RM = R * M;
+    int rc = 0;
+    for (int32_t r = 0; r < R && rc == 0; ++r) {        /* card r */
+        int64_t lo = (int64_t)r * S;
+        int64_t len = n - lo < S ? n - lo : S;
+        if (len <= 0) continue;                          /* empty shard  */
+        /* 1. reduce-scatter: card r receives chunk r of every rank's
+         *    micro-batch gradients (explicit copies, as in the pages' CPU
+         *    walkthrough where each card is a separate list element). */
+        uint16_t* recv = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)RM * (size_t)len);
+        const uint16_t** recv_ptr = (const uint16_t**)malloc(sizeof(void*) * (size_t)RM);
+        float* gshard = (float*)malloc(sizeof(float) * (size_t)len);
+        uint16_t* pshard = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)len);
+        if (!recv || !recv_ptr || !gshard || !pshard) {
+            rc = -2;
+        } else {
+            for (int32_t k = 0; k < RM; ++k) {
+                memcpy(recv + (int64_t)k * len, G[k] + lo, sizeof(uint16_t) * (size_t)len);
+                recv_ptr[k] = recv + (int64_t)k * len;
+            }
+            for (int64_t k = 0; k < len; ++k)
+                gshard[k] = oracle_avg_grad((const uint16_t* const*)recv_ptr, R, M, k,
+                                            s.denom_rm);
+            /* 2. card r updates only its own slice of the fp32 state. */
+            for (int64_t k = 0; k < len; ++k) {
+                oracle_adamw_elem(&s, gshard[k], &W[lo + k], &m[lo + k], &v[lo + k]);
+                pshard[k] = oracle_bf16_rne(W[lo + k]);
+            }
+            /* 3. all-gather: the bf16 shard is copied into every replica. */
+            for (int32_t q = 0; q < R; ++q)
+                memcpy(P[q] + lo, pshard, sizeof(uint16_t) * (size_t)len);
+        }
+        free(recv);
+        free(recv_ptr);
+        free(gshard);
+        free(pshard);
+    }
+    return rc;
+}
+
+int oracle_reduce_scatter_sum(int64_t n, int32_t R, int64_t S,
+                              const float* const* in, float* const* out)
+{
+    if (n < 0 || R < 1 || S < 0 || S * R < n || !in || !out) return -1;
+    for (int32_t r = 0; r < R; ++r) {
+        int64_t lo = (int64_t)r * S;
+        int64_t len = n - lo < S ? n - lo : S;
+        for (int64_t k = 0; k < len; ++k) {
+            float acc = in[0][lo + k];
+            for (int32_t q = 1; q < R; ++q) acc = acc + in[q][lo + k];
+            out[r][k] = acc;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------ ring demo -- */
+
+int oracle_ring_allreduce(float* const* cards, int32_t p, int64_t n,
+                          int64_t* sent)
+{
+    if (p < 1 || n < 0 || !cards || !sent) return -1;
+    for (int32_t k = 0; k < p; ++k) sent[k] = 0;
+    if (p == 1 || n == 0) return 0;
+    int64_t csz = (n + p - 1) / p;                       /* chunk length */
+    float* msg = (float*)malloc(sizeof(float) * (size_t)csz * (size_t)p);
+    if (!msg) return -2;
+#define CH_LO(c) ((int64_t)(c) * csz < n ? (int64_t)(c) * csz : n)
+#define CH_HI(c) ((int64_t)((c) + 1) * csz < n ? (int64_t)((c) + 1) * csz : n)
+    /* reduce-scatter half: in step s card k sends chunk (k - s) mod p to
+     * card k+1, which adds it to its own copy of that chunk.  All cards send
+     * at once, so the messages are staged first. */
+    for (int32_t s = 0; s < p - 1; ++s) {
+        for (int32_t k = 0; k < p; ++k) {
+            int32_t c = ((k - s) % p + p) % p;
+            int64_t lo = CH_LO(c), hi = CH_HI(c);
+            memcpy(msg + (int64_t)k * csz, cards[k] + lo, sizeof(float) * (size_t)(hi - lo));
+            sent[k] += hi - lo;
+        }
+        for (int32_t k = 0; k < p; ++k) {
+            int32_t dst = (k + 1) % p;
+            int32_t c = ((k - s) % p + p) % p;
+            int64_t lo = CH_LO(c), hi = CH_HI(c);
+            for (int64_t e = lo; e < hi; ++e)
+                cards[dst][e] = cards[dst][e] + msg[(int64_t)k * csz + (e - lo)];
+        }
+    }
+    /* now card k holds the full sum of chunk (k + 1) mod p.  All-gather half:
+     * in step s card k passes chunk (k + 1 - s) mod p on; the receiver
+     * overwrites its copy. */
+    for (int32_t s = 0; s < p - 1; ++s) {
+        for (int32_t k = 0; k < p; ++k) {
+            int32_t c = ((k + 1 - s) % p + p) % p;
+            int64_t lo = CH_LO(c), hi = CH_HI(c);
+            memcpy(msg + (int64_t)k * csz, cards[k] + lo, sizeof(float) * (size_t)(hi - lo));
+            sent[k] += hi - lo;
+        }
+        for (int32_t k = 0; k < p; ++k) {
+            int32_t dst = (k + 1) % p;
+            int32_t c = ((k + 1 - s) % p + p) % p;
+            int64_t lo = CH_LO(c), hi = CH_HI(c);
+            memcpy(cards[dst] + lo, msg + (int64_t)k * csz, sizeof(float) * (size_t)(hi - lo));
+        }
+    }
+#undef CH_LO
+#undef CH_HI
+    free(msg);
+    return 0;
+}
+
+/* ----------------------------------------------------------- accounting -- */
+
+void oracle_zero_bytes(double N, int32_t P, double bp, double bg, double bo,
+                       double out[4])
+{
+    out[0] = N * (bp + bg + bo);
+    out[1] = N * (bp + bg) + N * bo / P;
+    out[2] = N * bp + N * (bg + bo) / P;
+    out[3] = N * (bp + bg + bo) / P;
+}

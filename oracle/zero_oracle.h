@@ -1,0 +1,165 @@
+/*
+ * zero_oracle.h - CPU oracle for the ZeRO-1/2 mixed-precision AdamW step.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  This is the plain, slow, single
+ * threaded definition that the CUDA path is checked against.  Only the test
+ * suite, __graft_entry__.smoke() and the cpu_baseline / reference leg of
+ * bench.py may load it.  The product library (zero_optimizer_step_rs_gb300)
+ * neither links nor calls it, and the two share no source: the seeded input
+ * generator in zgen/ is the only module both sides use, and it holds none of
+ * the step's arithmetic.
+ *
+ * What it computes (sources are the five lecture pages on distributed
+ * training this project is built from):
+ *   - gradient accumulation g = (1/M) sum_j grad_j
+ *       [CS25 V6 Lecture 4 notes, "single-GPU baseline and gradient
+ *        accumulation", accumulation equation; LLM infra 06, section 7.2]
+ *   - data-parallel averaging g = (1/P) sum_r g_r, identical update per rank
+ *       [CS25 V6 Lecture 4 notes, "replicate the model, split the batch",
+ *        DP equation; CS324 Lecture 9 notes, section 3.1]
+ *   - reduce-scatter / all-gather, AllReduce = ReduceScatter + AllGather
+ *       [CS336 Lecture 7 book, sections 2.3 and 4.3; LLM infra 06, 2.0]
+ *   - ZeRO-1/2: each rank updates only its shard of the fp32 master weights
+ *     and Adam moments, then all-gathers the new parameters; bit-identical to
+ *     plain DP because AdamW is elementwise
+ *       [CS324 Lecture 9 notes, section 3.4; CS25 V6 Lecture 4 notes,
+ *        "ZeRO-1" and "ZeRO-2"; CS336 Lecture 7 summary, Q2]
+ *   - 16 bytes/param mixed-precision state: bf16 param 2 + bf16 grad 2 +
+ *     fp32 master 4 + m 4 + v 4
+ *       [CS324 Lecture 9 notes, section 2.1; CS336 Lecture 7 summary, Q3]
+ *   - ring all-reduce demo and its per-card send volume 2(p-1)/p
+ *       [CS324 Lecture 9 notes, section 3.2]
+ *   - per-device model-state formulas M_DP, M_Z1, M_Z2 (and Z3)
+ *       [CS25 V6 Lecture 4 notes, "ZeRO-1" and "ZeRO-2" memory equations;
+ *        CS324 Lecture 9 notes, exercises 1 and 7]
+ *
+ * Readings where the pages leave a step open (every one is listed in the
+ * repository's design notes):
+ *   R1 AdamW is torch.optim.AdamW's documented algorithm (decoupled decay
+ *      w*(1-lr*wd) first, then m/v EMA, bias correction, eps added after
+ *      the bias-corrected square root).
+ *   R2 every float operation is rounded to nearest-even on its own; no fused
+ *      multiply-add; the exact sequence is the one in oracle_adamw_elem().
+ *   R3 each rank first sums its M micro-batch gradients (j ascending), then
+ *      the rank sums are added in ascending rank order; each sum starts from
+ *      its first term (no +0.0 seed).
+ *   R4 one IEEE division of the fp32 sum by (float)(R*M) after summation.
+ *   R5 weight decay applies to every element.
+ *   R6 shard length S = roundup(ceil(N/R), ALIGN); owner(i) = i / S; state
+ *      arrays hold R*S floats with shard r at r*S; pad elements are never
+ *      read or written; replicas hold exactly N elements.
+ *   R7 bf16 cast: round to nearest, ties to even; +-Inf kept; overflow to
+ *      +-Inf; every NaN becomes the one quiet NaN 0x7FC0 (IEEE 754 fixes
+ *      neither the sign nor the payload of a NaN an operation produces).
+ *   R8 non-finite gradients propagate IEEE-wise (no skip).
+ *   R9 ZeRO-1 and ZeRO-2 compute the same numbers; the stage changes only
+ *      which buffers stay resident (the byte accounting).
+ */
+#ifndef ZERO_ORACLE_H
+#define ZERO_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* AdamW hyper-parameters as a user gives them. */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+} oracle_hparams;
+
+/* The per-step float scalars of the update, each computed once in double
+ * from the hyper-parameters and the step count t, then rounded to float. */
+typedef struct {
+    float step_size;   /* lr / (1 - beta1^t)              */
+    float bc2_sqrt;    /* sqrt(1 - beta2^t)               */
+    float decay;       /* 1 - lr * weight_decay           */
+    float beta1, beta2;
+    float one_minus_beta1, one_minus_beta2;
+    float eps;
+    float denom_rm;    /* (float)(R * M)                  */
+} oracle_scalars;
+
+/* bf16 <-> float, written from the format definition (sign, 8-bit exponent,
+ * 7-bit fraction = the high half of an IEEE binary32). */
+uint16_t oracle_bf16_rne(float x);
+float    oracle_bf16_to_float(uint16_t h);
+
+/* Per-step scalars (reading R1, R4). step >= 1. */
+void oracle_make_scalars(const oracle_hparams* hp, int64_t step, int32_t R,
+                         int32_t M, oracle_scalars* out);
+
+/* One AdamW update of one element (reading R1, R2). g is the averaged
+ * gradient; w, m, v are updated in place. */
+void oracle_adamw_elem(const oracle_scalars* s, float g, float* w, float* m,
+                       float* v);
+
+/* Averaged gradient of element i over R ranks x M micro-batches (R3, R4).
+ * G is an array of R*M pointers, entry r*M+j = rank r, micro-batch j. */
+float oracle_avg_grad(const uint16_t* const* G, int32_t R, int32_t M,
+                      int64_t i, float denom_rm);
+
+/* Unsharded data-parallel step: every rank all-reduces the gradients and
+ * applies the same AdamW update to a full copy of the state; the result is
+ * written to every rank's replica P[r] (R pointers, n bf16 each).
+ * W, m, v hold n floats.  Returns 0, or -1 on a bad argument. */
+int oracle_dp_step(int64_t n, int32_t R, int32_t M,
+                   const uint16_t* const* G, float* W, float* m, float* v,
+                   uint16_t* const* P, const oracle_hparams* hp, int64_t step);
+
+/* Same as oracle_dp_step, split over nthreads element ranges (the step is
+ * elementwise, so the result is bit-identical).  Used to time the oracle on
+ * all host cores; nthreads <= 0 means 1. */
+int oracle_dp_step_mt(int64_t n, int32_t R, int32_t M,
+                      const uint16_t* const* G, float* W, float* m, float* v,
+                      uint16_t* const* P, const oracle_hparams* hp,
+                      int64_t step, int32_t nthreads);
+
+/* Shard length S = roundup(ceil(n/R), align) (reading R6). align >= 1. */
+int64_t oracle_shard_len(int64_t n, int32_t R, int32_t align);
+
+/* ZeRO-1/2 step emulated card by card, each card a separate buffer:
+ *   1. reduce-scatter: card r receives, from every rank r', a copy of the
+ *      bf16 gradient chunk r of each of r's M micro-batches, and sums them
+ *      (R3) into its fp32 gradient shard, then divides by R*M (R4);
+ *   2. card r updates its own slice [r*S, r*S+len_r) of W, m, v (R*S floats
+ *      each, reading R6) with AdamW;
+ *   3. all-gather: card r casts its updated shard to bf16 (R7) and copies it
+ *      into every card's replica P[r'] (n bf16 each).
+ * Returns 0, -1 on a bad argument, -2 if a buffer cannot be allocated. */
+int oracle_zero_step(int64_t n, int32_t R, int32_t M, int64_t S,
+                     const uint16_t* const* G, float* W, float* m, float* v,
+                     uint16_t* const* P, const oracle_hparams* hp,
+                     int64_t step);
+
+/* Reduce-scatter alone (sum, no division): card r ends with chunk r of the
+ * element-wise sum over ranks; out[r] points to S floats (only the first
+ * len_r are written).  in[r] points to n floats.  Sum order as R3. */
+int oracle_reduce_scatter_sum(int64_t n, int32_t R, int64_t S,
+                              const float* const* in, float* const* out);
+
+/* Ring all-reduce over p cards (CS324 Lecture 9 notes, section 3.2): the
+ * arrays are cut into p chunks; p-1 reduce-scatter steps in which every card
+ * sends one chunk to the next card, which adds it to its own copy, then p-1
+ * all-gather steps in which the completed chunks are passed on and
+ * overwrite.  cards[k] points to n floats, updated in place; sent[k]
+ * receives the count of numbers card k sent.  Returns 0 or -1. */
+int oracle_ring_allreduce(float* const* cards, int32_t p, int64_t n,
+                          int64_t* sent);
+
+/* Per-device model-state bytes for N params on P ranks with b_p, b_g, b_o
+ * bytes of parameter, gradient and optimizer state per param:
+ *   out[0] DP = N(b_p + b_g + b_o)
+ *   out[1] Z1 = N(b_p + b_g) + N b_o / P
+ *   out[2] Z2 = N b_p + N(b_g + b_o) / P
+ *   out[3] Z3 = N(b_p + b_g + b_o) / P
+ * (CS25 V6 Lecture 4 notes, ZeRO-1/ZeRO-2 memory equations; Z3 from
+ *  CS324 Lecture 9 notes, exercise 1). */
+void oracle_zero_bytes(double N, int32_t P, double bp, double bg, double bo,
+                       double out[4]);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,63 @@
+"""Plant a mistake in a copy of the oracle and check that the pins catch it.
+
+Each mutant is the oracle's own C source with one plausible slip (a dropped
+term, a wrong sign, a transposed operand or index, a wrong divisor, a wrong
+offset), compiled on the CPU into a temporary library; the pin suites then
+run against it in a child process and must fail.  The real oracle is never
+modified.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "zero_oracle.c")
+
+MUTANTS = {
+    "drop_weight_decay": ("float wd = *w * s->decay;", "float wd = *w;"),
+    "update_sign": ("*w = wd - upd;", "*w = wd + upd;"),
+    "first_moment_reads_v": ("float a = s->beta1 * *m;", "float a = s->beta1 * *v;"),
+    "second_moment_not_squared": ("float e = d * g;", "float e = d;"),
+    "drop_bias_correction_2": ("float q = root / s->bc2_sqrt;", "float q = root;"),
+    "drop_bias_correction_1": ("out->step_size = (float)(lr / bc1);",
+                               "out->step_size = (float)lr;"),
+    "eps_inside_sqrt": ("float den = q + s->eps;",
+                        "float den = sqrtf(v1 + s->eps) / s->bc2_sqrt;"),
+    "grad_index_transposed": ("local = local + oracle_bf16_to_float(G[(int64_t)r * M + j][i]);",
+                              "local = local + oracle_bf16_to_float(G[(int64_t)j * R + r][i]);"),
+    "divide_by_R_only": ("return acc / denom_rm;", "return acc / (float)R;"),
+    "drop_last_rank": ("acc = (r == 0) ? local : acc + local;",
+                       "acc = (r == 0) ? local : (r == R - 1 ? acc : acc + local);"),
+    "bf16_truncates": ("u += 0x7FFFu + kept_lsb;", "u += 0u * kept_lsb;"),
+    "bf16_ties_away": ("u += 0x7FFFu + kept_lsb;", "u += 0x8000u + 0u * kept_lsb;"),
+    "shard_offset_off_by_one": ("int64_t lo = (int64_t)r * S;\n        int64_t len = n - lo < S ? n - lo : S;\n        if (len <= 0) continue;",
+                                "int64_t lo = (int64_t)r * S + (r > 0);\n        int64_t len = n - lo < S ? n - lo : S;\n        if (len <= 0) continue;"),
+    "all_gather_own_replica_only": ("memcpy(P[q] + lo, pshard", "memcpy(P[r] + lo + 0 * q, pshard"),
+    "ring_allgather_wrong_chunk": ("int32_t c = ((k + 1 - s) % p + p) % p;\n            int64_t lo = CH_LO(c), hi = CH_HI(c);\n            memcpy(msg",
+                                   "int32_t c = ((k - s) % p + p) % p;\n            int64_t lo = CH_LO(c), hi = CH_HI(c);\n            memcpy(msg"),
+    "zero2_formula_swapped": ("out[2] = N * bp + N * (bg + bo) / P;",
+                              "out[2] = N * (bp + bg) + N * bo / P;"),
+    "shard_len_no_roundup": ("return (per + align - 1) / align * align;", "return per + 0 * align;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique/present"
+    mut_src = tmp_path / "zero_oracle.c"
+    mut_src.write_text(src.replace(old, new))
+    hdr = os.path.join(ROOT, "oracle", "zero_oracle.h")
+    lib = tmp_path / "liboracle_mut.so"
+    subprocess.run(["gcc", *oracle.CFLAGS, "-I", os.path.dirname(hdr), "-o", str(lib),
+                    str(mut_src), "-lm", "-lpthread"], check=True)
+    env = dict(os.environ, ZERO_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        "tests/test_oracle_pins.py", "tests/test_oracle_collectives.py"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
