@@ -1,0 +1,457 @@
+"""Benchmark of the ZeRO-1/2 mixed-precision AdamW step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llama-3.2-1b] [--variant fused|staged]
+
+One "step" is one pass of the whole hot path (ordered reduce-scatter +
+average, AdamW on every shard, bf16 all-gather into all R replicas) over the
+workload's synthetic inputs, which are resident in HBM before the timed
+region starts.  The default workload is the Llama-3.2-1B-shaped parameter
+set (1,235,814,400 params, R=8 emulated ranks, M=1, ZeRO-2, step 100):
+69.2 GB of algorithmic traffic per step, far larger than the 129 MB L2, so
+no L2 flush is needed between steps.
+
+Timing: W warm-up steps, then K steps bracketed by a barrier and
+cuda.synchronize on both sides, CUDA events on the launching stream, max over
+ranks.  Each rank (one per GPU) runs its own emulated ZeRO group: the path
+has no cross-GPU exchange on this build, so N>1 runs N independent replicas
+("weak" scaling).  The JSON line also carries the roofline of the dominant
+kernel, the end-to-end number through the host-buffer entry point, the
+oracle timed on the host cores, and the SM clocks sampled during the timed
+region.
+
+--impl reference times the CPU oracle (the plain C definition the kernels
+are checked against) on a bounded sample of the same workload, on the host
+cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ZeRO AdamW step: params/s and HBM GB/s (% of ~8 TB/s roofline), 1 GB300"
+UNIT = "params/s"
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms in the
+    background; read-only queries."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.5)
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_stop(self):
+        self.t_stop = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        import datetime
+
+        def ts(p):
+            try:
+                return datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return None
+
+        inside = [p for p in rows if self.t_start and self.t_stop and ts(p) is not None
+                  and self.t_start - 0.1 <= ts(p) <= self.t_stop + 0.1]
+        use = inside or rows
+        sm, reasons, sm_max = [], set(), None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in use:
+            try:
+                mhz, mx = float(p[2]), float(p[3])
+            except ValueError:
+                continue
+            sm_max = mx
+            sm.append(mhz)
+            for name, flag in zip(names, p[6:10]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": sm_max, "reasons": sorted(reasons),
+                "samples": len(sm), "in_timed_region": bool(inside)}
+
+
+def gpu_uuid(device_index: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(device_index)
+
+
+# --------------------------------------------------------- oracle (CPU) --
+
+def oracle_prepare(wl, n, threads=None):
+    """Host inputs of the first n params of the workload (seeded generator,
+    built in parallel chunks) for timing the oracle."""
+    import numpy as np
+    from concurrent.futures import ThreadPoolExecutor
+
+    from zgen import workloads as W
+
+    threads = threads or os.cpu_count() or 1
+    chunks = [(lo, min(n, lo + (1 << 20))) for lo in range(0, n, 1 << 20)]
+    G = [np.empty(n, np.uint16) for _ in range(wl.R * wl.M)]
+    W0 = np.empty(n, np.float32)
+    m0 = np.empty(n, np.float32)
+    v0 = np.empty(n, np.float32)
+
+    def work(c):
+        lo, hi = c
+        idx = np.arange(lo, hi, dtype=np.int64)
+        for g, src in zip(G, W.host_grads_at(wl, wl.step, idx)):
+            g[lo:hi] = src
+        W0[lo:hi] = W.host_w0_at(wl, idx)
+        a, b = W.host_mv0_at(wl, idx)
+        m0[lo:hi], v0[lo:hi] = a, b
+
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(work, chunks))
+    P = [np.empty(n, np.uint16) for _ in range(wl.R)]
+    return {"G": G, "W0": W0, "m0": m0, "v0": v0, "P": P, "threads": threads, "n": n}
+
+
+def oracle_pass(wl, ctx):
+    """One timed pass of the oracle (unchanged) over the prepared sample;
+    returns seconds."""
+    import oracle
+    Wc, mc, vc = ctx["W0"].copy(), ctx["m0"].copy(), ctx["v0"].copy()
+    hp = oracle.hparams(**wl.hparams())
+    t0 = time.perf_counter()
+    oracle.dp_step(ctx["G"], Wc, mc, vc, ctx["P"], hp, wl.step, wl.R, wl.M,
+                   nthreads=ctx["threads"])
+    return time.perf_counter() - t0
+
+
+def oracle_sample_rate(wl, target_s=12.0, sample_elems=1 << 24, threads=None):
+    """Time the oracle on the first sample_elems params of the workload,
+    repeated until target_s of CPU time; returns params/s, cores, text."""
+    n = min(sample_elems, wl.N)
+    ctx = oracle_prepare(wl, n, threads)
+    reps, elapsed = 0, 0.0
+    while elapsed < target_s or reps == 0:
+        elapsed += oracle_pass(wl, ctx)
+        reps += 1
+    desc = (f"oracle_dp_step_mt over the first {n:,} params of the workload "
+            f"(same R, M, distributions), {reps} passes, {elapsed:.1f} s")
+    return n * reps / elapsed, ctx["threads"], desc
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The maximum of a per-rank float over all ranks of the default process
+    group (the identity without one).  Timing only: no step data crosses
+    ranks."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ our arm --
+
+def traffic_per_param():
+    """Measured DRAM bytes per parameter of the fused kernel, from the
+    committed ncu summary, if it was taken on the current kernel source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)
+        src = os.path.join(ROOT, "zero_optimizer_step_rs_gb300", "csrc", "zero_step.cu")
+        with open(src, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+        if rec.get("source_sha256_16") != h:
+            return None, rec
+        return rec, rec
+    except (OSError, ValueError):
+        return None, None
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import zero_optimizer_step_rs_gb300 as z
+    from tests import harness as H
+    from zgen import workloads as W
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = W.by_name(args.workload)
+    variant = z.ZERO_VARIANT_STAGED if args.variant == "staged" else z.ZERO_VARIANT_FUSED
+    stream = torch.cuda.current_stream()
+
+    ds = H.DeviceState(wl, str(dev), staged_scratch=(variant == z.ZERO_VARIANT_STAGED))
+    ds.fill_state_device()
+    t = wl.first_step()
+    while t < wl.step:                     # prior steps build the moments
+        ds.fill_grads_device(t)
+        ds.step(t, variant=variant)
+        t += 1
+    ds.fill_grads_device(wl.step)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    step_t = wl.step
+    for _ in range(args.warmup):
+        ds.step(step_t, variant=variant)
+        step_t += 1
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_uuid(local_rank))
+    sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    e_all0, e_all1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    sampler.mark_start()
+    e_all0.record(stream)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        ds.step(step_t, variant=variant)
+        ev[k][1].record(stream)
+        step_t += 1
+    e_all1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    sampler.mark_stop()
+    clocks = sampler.stop()
+    total_ms = e_all0.elapsed_time(e_all1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+
+    total_ms = max_over_ranks(total_ms, dev)
+
+    N = wl.N
+    ms_per_step = total_ms / args.steps
+    value = N * args.steps * world / (total_ms / 1e3)
+    bpp = wl.bytes_per_param() if variant == z.ZERO_VARIANT_FUSED else (
+        2 * wl.R * wl.M + 4 + 4 + 24 + 4 + 2 * wl.R)
+    alg_bytes = bpp * N
+    avg_launch_s = float(np.mean(launch_ms)) / 1e3
+    achieved_gbs = alg_bytes / avg_launch_s / 1e9
+    peaks = measured_peaks()
+    if peaks and "hbm_gbs" in peaks:
+        peak, peak_src = float(peaks["hbm_gbs"]), "measured"
+    else:
+        peak, peak_src = 6800.0, "fallback"
+    rec, _ = traffic_per_param()
+    traffic = None
+    if rec and variant == z.ZERO_VARIANT_FUSED and rec.get("R") == wl.R and rec.get("M") == wl.M:
+        traffic = round(rec["dram_bytes_per_param"] * N)
+    roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved_gbs / peak, 4), "traffic": traffic,
+                "peak_source": peak_src, "kernel": "k_fused" if variant == 0 else "staged trio",
+                "algorithmic_bytes_per_launch": alg_bytes, "bytes_per_param": bpp}
+
+    # -------- end to end through the host-buffer entry point
+    e2e = None
+    if not args.no_e2e and variant == z.ZERO_VARIANT_FUSED:
+        host_g = [torch.empty(N, dtype=torch.bfloat16, pin_memory=True) for _ in ds.grads]
+        for h, d in zip(host_g, ds.grads):
+            h.copy_(d[:N])
+        out = torch.empty(N, dtype=torch.bfloat16, pin_memory=True)
+        torch.cuda.synchronize()
+        k_e2e = max(2, min(args.steps, 5))
+        z.zero_step_host(ds.plan, host_g, ds.grads, ds.W, ds.m, ds.v, ds.params, out, ds.hp,
+                         step_t)
+        step_t += 1
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k_e2e):
+            z.zero_step_host(ds.plan, host_g, ds.grads, ds.W, ds.m, ds.v, ds.params, out, ds.hp,
+                             step_t)
+            step_t += 1
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        e2e_ms = max_over_ranks(e2e_ms, dev)
+        e2e = {"value": N * k_e2e * world / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": 2 * wl.R * wl.M * N, "d2h_bytes_per_step": 2 * N,
+               "ms_per_step": e2e_ms / k_e2e, "steps": k_e2e,
+               "path": "zero_step_host: R*M pinned host->device copies, fused step, "
+                       "replica 0 device->host"}
+        del host_g, out
+
+    launches_per_step = 1 if variant == z.ZERO_VARIANT_FUSED else 3
+    del ds
+    torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, cores, desc = oracle_sample_rate(wl)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded counter-based generator; shapes of the named parameter set)",
+        "config": {"workload": wl.name, "N": N, "R": wl.R, "M": wl.M, "stage": wl.stage,
+                   "step": wl.step, "variant": args.variant,
+                   "l2": "inputs (%.1f GB/step) far larger than the 129 MB L2; no flush"
+                         % (alg_bytes / 1e9),
+                   "parallelism": f"{world} independent replica(s) of an R={wl.R} "
+                                  "emulated ZeRO group"},
+        "hbm_gbs": round(alg_bytes / (ms_per_step / 1e3) / 1e9, 1),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    return line
+
+
+# ------------------------------------------------------- reference arm --
+
+def run_reference(args):
+    """The oracle as it stands, on the host cores: each step is one pass of
+    oracle_dp_step_mt over a bounded sample (the first 2^22 params) of the
+    workload."""
+    from zgen import workloads as W
+    wl = W.by_name(args.workload)
+    t0 = time.time()
+    sample = min(wl.N, 1 << 22)
+    ctx = oracle_prepare(wl, sample)
+    for _ in range(args.warmup):
+        oracle_pass(wl, ctx)
+    per_step = [oracle_pass(wl, ctx) for _ in range(args.steps)]
+    mean_s = sum(per_step) / len(per_step)
+    value = sample / mean_s
+    desc = (f"oracle_dp_step_mt over the first {sample:,} params of the workload "
+            f"(same R, M, distributions), {ctx['threads']} threads, one pass per step")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean_s,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded counter-based generator; shapes of the named parameter set)",
+        "config": {"workload": wl.name, "N": wl.N, "R": wl.R, "M": wl.M, "stage": wl.stage,
+                   "step": wl.step, "sample_params_per_step": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": ctx["threads"], "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": round(time.time() - t0, 1),
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama-3.2-1b")
+    ap.add_argument("--variant", choices=["fused", "staged"], default="fused")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local_rank = _env_int("LOCAL_RANK", 0)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

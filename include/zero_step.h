@@ -1,0 +1,218 @@
+/*
+ * zero_step.h - C ABI of the GB300 ZeRO-1/2 mixed-precision AdamW step.
+ *
+ * One optimizer step of data-parallel training with ZeRO stage 1 or 2,
+ * with R data-parallel ranks emulated as R separate buffers in one GPU's
+ * memory:
+ *
+ *   1. reduce-scatter + average: rank r owns shard r of the flat parameter
+ *      vector and receives the fp32 sum, in fixed rank order, of every
+ *      rank's bf16 gradients (each rank first accumulates its M
+ *      micro-batches), divided by R*M;
+ *   2. AdamW on the owned shard of the fp32 master weights and moments;
+ *   3. cast to bf16 and all-gather into every rank's full replica.
+ *
+ * Sources (lecture pages on distributed training):
+ *   - gradient accumulation g = (1/M) sum_j grad_j: CS25 V6 Lecture 4 notes,
+ *     "single-GPU baseline and gradient accumulation";
+ *     LLM infra 06 (3D parallelism), section 7.2
+ *   - DP averaging g = (1/P) sum_r g_r: CS25 V6 Lecture 4 notes, "replicate
+ *     the model, split the batch"; CS324 Lecture 9 notes, section 3.1
+ *   - ZeRO-1 / ZeRO-2 (shard the optimizer state, then the gradients; each
+ *     rank updates its shard; all-gather the new parameters): CS25 V6
+ *     Lecture 4 notes, "ZeRO-1" and "ZeRO-2"; CS324 Lecture 9 notes,
+ *     section 3.4; CS336 Lecture 7 summary, Q2
+ *   - reduce-scatter / all-gather semantics: CS336 Lecture 7 book,
+ *     sections 2.3 and 4.3 (reduce_scatter_tensor, all_gather_into_tensor);
+ *     LLM infra 06, section 2.0
+ *   - 16 bytes/param state (bf16 param + bf16 grad + fp32 master, m, v):
+ *     CS324 Lecture 9 notes, section 2.1; CS336 Lecture 7 summary, Q3
+ *   - fp32 reduction of gradients: LLM infra 06, section 15.3
+ *
+ * Arithmetic (the pages leave it open; this library fixes it and the CPU
+ * oracle in the repository follows the same definition):
+ *   acc_r = G[r][0][i] + G[r][1][i] + ... (fp32, micro-batches ascending)
+ *   acc   = acc_0 + acc_1 + ... + acc_{R-1} (fp32, ranks ascending)
+ *   g     = acc / (float)(R*M)              (IEEE division)
+ *   torch.optim.AdamW's algorithm, every float operation rounded on its own
+ *   (no fused multiply-add):
+ *   w = W[i]*(1-lr*wd); m = b1*m + (1-b1)*g; v = b2*v + ((1-b2)*g)*g;
+ *   W[i] = w - (lr/(1-b1^t)) * (m / (sqrt(v)/sqrt(1-b2^t) + eps));
+ *   P[r][i] = bf16(W[i]) for every r (round to nearest even; every NaN
+ *   becomes 0x7FC0).  The scalars lr/(1-b1^t), sqrt(1-b2^t), 1-lr*wd, 1-b1
+ *   and 1-b2 are computed once per step in double and rounded to float.
+ *
+ * Conventions for every entry point:
+ *   - Returns a zero_status; ZERO_OK (0) on success.  Argument, plan,
+ *     alignment, size and overlap errors are returned synchronously and
+ *     nothing is launched.  ZERO_ERR_CUDA means a launch or copy failed
+ *     (cudaGetLastError after the launches).  Conditions found on the device
+ *     are OR-ed into an optional caller-owned device status word.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and is asynchronous with respect to the host.
+ *   - The caller allocates and owns every device buffer (PyTorch in the
+ *     bundled binding).  The library allocates only the host-side plan.
+ *   - bf16 buffers are passed as uint16_t* (raw bf16 bits).  Device buffers
+ *     must be 16-byte aligned.
+ *   - No exceptions and no global state cross the ABI; entry points are
+ *     thread-safe for distinct buffers.
+ */
+#ifndef ZERO_STEP_H
+#define ZERO_STEP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ZERO_ABI_VERSION 1
+#define ZERO_MAX_R 64        /* emulated ranks */
+#define ZERO_MAX_RM 256      /* gradient buffers (ranks x micro-batches) */
+
+typedef enum {
+    ZERO_OK = 0,
+    ZERO_ERR_INVALID_ARG = -1,     /* R, M, stage, step, variant, hparams, ... */
+    ZERO_ERR_NULL = -2,            /* a required pointer is NULL              */
+    ZERO_ERR_ALIGN = -3,           /* a device pointer is not 16-byte aligned  */
+    ZERO_ERR_SIZE = -4,            /* sizes beyond the limits / scratch too small */
+    ZERO_ERR_OVERLAP = -5,         /* an output overlaps another buffer        */
+    ZERO_ERR_CUDA = -6,            /* a CUDA launch or copy failed             */
+    ZERO_ERR_DEVICE_TIMEOUT = -7,  /* reserved for device-side bounded waits   */
+    ZERO_ERR_NONFINITE = -8        /* reported through the device status word  */
+} zero_status;
+
+/* Bits OR-ed into the optional device status word. */
+#define ZERO_DEV_NONFINITE 1       /* an averaged gradient was Inf or NaN   */
+
+/* Flags for zero_step / zero_rs_avg. */
+#define ZERO_FLAG_CHECK_FINITE 1   /* set ZERO_DEV_NONFINITE when g is non-finite */
+
+/* Variants for zero_step. */
+#define ZERO_VARIANT_FUSED 0       /* one pass: rs -> adamw -> ag per element  */
+#define ZERO_VARIANT_STAGED 1      /* rs_avg, adamw_shard, ag_cast, fp32 g in scratch */
+
+/*
+ * Shard layout of a flat parameter vector (the tensors concatenated in the
+ * given order, no per-tensor padding): N = sum of numels,
+ * S = roundup(ceil(N / R), align_elems), owner(i) = i / S.  The fp32 state
+ * arrays (master, m, v) hold padded = R*S floats with shard r at offset r*S,
+ * so element i lives at index i; pad elements [N, R*S) are never read or
+ * written.  Replicas and gradient buffers hold exactly N elements.
+ * Byte accounting per rank (CS25 V6 Lecture 4 notes, ZeRO-1/ZeRO-2 memory
+ * equations; CS324 Lecture 9 notes, exercise 1), with b_p = b_g = 2 bytes
+ * (bf16) and b_o = 12 bytes (fp32 master, m, v), sharded parts counted with
+ * the padded shard S:
+ *   dp = N(b_p + b_g + b_o); z1 = N(b_p + b_g) + S b_o;
+ *   z2 = N b_p + S(b_g + b_o); z3 = S(b_p + b_g + b_o).
+ */
+typedef struct {
+    int64_t N;                     /* real parameter count                     */
+    int64_t S;                     /* shard length (elements)                  */
+    int64_t padded;                /* R * S                                    */
+    int32_t R, M;                  /* ranks, micro-batches                     */
+    int32_t stage;                 /* 1 or 2 (same numbers; accounting only)   */
+    int32_t align_elems;           /* shard alignment, a multiple of 4         */
+    int32_t n_tensors;
+    const int64_t* tensor_offsets; /* n_tensors + 1 entries, owned by the plan */
+    int64_t bytes_per_rank_dp, bytes_per_rank_z1, bytes_per_rank_z2, bytes_per_rank_z3;
+    int64_t bytes_per_rank;        /* the one for `stage`                      */
+    int64_t scratch_bytes_staged;  /* scratch the staged variant needs: 4*R*S  */
+} zero_plan_t;
+
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+} zero_adamw_hparams;
+
+/* ABI version (ZERO_ABI_VERSION). */
+int32_t zero_abi_version(void);
+
+/* Static, human-readable name of a status code. */
+const char* zero_status_string(zero_status s);
+
+/*
+ * Build the shard layout for n_tensors tensors of the given element counts
+ * (host array, read only), R ranks (1..ZERO_MAX_R), M micro-batches
+ * (R*M <= ZERO_MAX_RM), ZeRO stage 1 or 2, shard alignment align_elems
+ * (0 -> 64; otherwise a positive multiple of 4).  Host only: needs no GPU.
+ * On success *out owns a new plan (free with zero_plan_destroy).
+ * Errors: ZERO_ERR_NULL, ZERO_ERR_INVALID_ARG (a negative numel, R, M,
+ * stage or alignment out of range), ZERO_ERR_SIZE (N overflows).
+ */
+zero_status zero_plan_create(const int64_t* tensor_numels, int32_t n_tensors, int32_t R,
+                             int32_t M, int32_t stage, int32_t align_elems, zero_plan_t** out);
+
+/* Free a plan (NULL is ignored). */
+void zero_plan_destroy(zero_plan_t* plan);
+
+/* Rank owning element i (i / S), or -1 if i is outside [0, N). */
+int32_t zero_plan_owner(const zero_plan_t* plan, int64_t i);
+
+/*
+ * One optimizer step (see the top of this file for the arithmetic).
+ *   rank_grads  host array of R*M device pointers, entry r*M + j = rank r,
+ *               micro-batch j; each N bf16, read only (entries may alias
+ *               one another).
+ *   master, m, v  device, plan->padded floats each, updated in place.
+ *   rank_params host array of R device pointers, each N bf16, written.
+ *   hp          AdamW hyper-parameters (0 <= beta1, beta2 < 1; lr, eps,
+ *               weight_decay finite; eps >= 0).
+ *   step        the step count t >= 1 used for bias correction.
+ *   variant     ZERO_VARIANT_FUSED or ZERO_VARIANT_STAGED.
+ *   scratch     device scratch of scratch_bytes bytes; the staged variant
+ *               needs plan->scratch_bytes_staged (fp32 reduced gradient of
+ *               every shard); ignored (may be NULL) for the fused variant.
+ *   flags       0 or ZERO_FLAG_CHECK_FINITE.
+ *   dev_status  optional device int32 the kernels OR ZERO_DEV_* bits into.
+ * Outputs (master, m, v, replicas, scratch) must not overlap one another or
+ * any gradient buffer (ZERO_ERR_OVERLAP).  The two variants give identical
+ * bits.
+ */
+zero_status zero_step(const zero_plan_t* plan, const uint16_t* const* rank_grads,
+                      float* master, float* m, float* v, uint16_t* const* rank_params,
+                      const zero_adamw_hparams* hp, int64_t step, int32_t variant,
+                      void* scratch, int64_t scratch_bytes, int32_t flags,
+                      int32_t* dev_status, void* stream);
+
+/*
+ * Staged step 1, reduce-scatter + average: for each rank r and each element
+ * i of shard r, g_shards[i] = (ordered fp32 sum of the R*M gradients at i) /
+ * (R*M).  g_shards: device, plan->padded floats (shard r at r*S); elements
+ * [N, padded) are not written.  Same pointer rules as zero_step.
+ */
+zero_status zero_rs_avg(const zero_plan_t* plan, const uint16_t* const* rank_grads,
+                        float* g_shards, int32_t flags, int32_t* dev_status, void* stream);
+
+/*
+ * Staged step 2, AdamW on every rank's shard: reads g_shards (from
+ * zero_rs_avg) and updates master, m, v in place at the N real elements.
+ */
+zero_status zero_adamw_shard(const zero_plan_t* plan, const float* g_shards, float* master,
+                             float* m, float* v, const zero_adamw_hparams* hp, int64_t step,
+                             void* stream);
+
+/*
+ * Staged step 3, cast + all-gather: every rank r casts its shard of master
+ * to bf16 and writes it into all R replicas.
+ */
+zero_status zero_ag_cast(const zero_plan_t* plan, const float* master,
+                         uint16_t* const* rank_params, void* stream);
+
+/*
+ * End-to-end step from host memory: copies the R*M gradient buffers from
+ * host_grads (host pointers; pinned memory lets the copies run at full
+ * speed) into dev_grads (device), runs the fused step, and copies replica 0
+ * (every replica holds the same bits) into host_params_out (host, N bf16).
+ * All on `stream`; the host buffers must stay valid until the stream has
+ * finished.  Same argument rules as zero_step.
+ */
+zero_status zero_step_host(const zero_plan_t* plan, const uint16_t* const* host_grads,
+                           uint16_t* const* dev_grads, float* master, float* m, float* v,
+                           uint16_t* const* rank_params, uint16_t* host_params_out,
+                           const zero_adamw_hparams* hp, int64_t step, int32_t flags,
+                           int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

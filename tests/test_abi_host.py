@@ -1,0 +1,217 @@
+"""Host-side checks of the C-ABI library (no GPU needed).
+
+The library loads, exports every entry point include/zero_step.h declares,
+its plan reproduces the pages' accounting, and every argument error is
+returned synchronously before anything touches a GPU (so these calls are
+safe without one: the library returns before any CUDA call).
+"""
+import os
+import re
+
+import pytest
+import torch
+
+import zero_optimizer_step_rs_gb300 as z
+from zero_optimizer_step_rs_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from zero_optimizer_step_rs_gb300 import build
+    build.build()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "zero_step.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(zero_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_symbols()
+    assert len(names) >= 10
+    L = B.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(B.EXPORTED) == names
+
+
+def test_version_and_status_strings():
+    assert z.zero_abi_version() == 1
+    for code in range(-8, 1):
+        assert z.zero_status_string(code) != "unknown status"
+    assert z.zero_status_string(-99) == "unknown status"
+
+
+@pytest.mark.parametrize("numels,R,M,align,S,padded", [
+    ([65536], 4, 2, 0, 16384, 65536),
+    ([100_000_007], 7, 4, 64, 14_285_760, 100_000_320),
+    ([5], 4, 1, 64, 64, 256),
+    ([3, 4, 5], 3, 1, 4, 4, 12),
+    ([], 2, 1, 0, 0, 0),
+])
+def test_plan_layout(numels, R, M, align, S, padded):
+    p = z.Plan(numels, R, M, 2, align)
+    assert (p.N, p.S, p.padded, p.R, p.M) == (sum(numels), S, padded, R, M)
+    assert p.tensor_offsets()[-1] == sum(numels)
+    assert p.scratch_bytes_staged == 4 * padded
+
+
+def test_plan_owner():
+    p = z.Plan([1000], 3, 1, 1, 4)            # S = roundup(334, 4) = 336
+    assert p.S == 336
+    assert [p.owner(i) for i in (0, 335, 336, 671, 672, 999)] == [0, 0, 1, 1, 2, 2]
+    assert p.owner(-1) == -1 and p.owner(1000) == -1
+
+
+def test_plan_accounting_matches_pages_exercise_1():
+    # CS324 Lecture 9 notes, exercise 1: 7B params, 8 cards, 2+2+12 bytes:
+    # DP 112, ZeRO-1 38.5, ZeRO-2 26.25, ZeRO-3 14 GB (S divides exactly)
+    p = z.Plan([7_000_000_000], 8, 1, 1)
+    got = [p.bytes_per_rank_dp, p.bytes_per_rank_z1, p.bytes_per_rank_z2, p.bytes_per_rank_z3]
+    assert [g / 1e9 for g in got] == [112.0, 38.5, 26.25, 14.0]
+    assert p.bytes_per_rank == p.bytes_per_rank_z1
+
+
+def test_plan_accounting_matches_pages_summary_item_5():
+    # same notes, summary item 5: 7.5B params on 64 cards: 120 / 31.4 / 16.6 / 1.88 GB
+    p = z.Plan([7_500_000_000], 64, 1, 2)
+    got = [p.bytes_per_rank_dp, p.bytes_per_rank_z1, p.bytes_per_rank_z2, p.bytes_per_rank_z3]
+    assert [round(got[0] / 1e9, 1), round(got[1] / 1e9, 1), round(got[2] / 1e9, 1),
+            round(got[3] / 1e9, 2)] == [120.0, 31.4, 16.6, 1.88]
+    assert p.bytes_per_rank == p.bytes_per_rank_z2
+
+
+@pytest.mark.parametrize("args,code", [
+    (([10], 0, 1, 1, 0), B.ZERO_ERR_INVALID_ARG),
+    (([10], 65, 1, 1, 0), B.ZERO_ERR_INVALID_ARG),
+    (([10], 4, 0, 1, 0), B.ZERO_ERR_INVALID_ARG),
+    (([10], 16, 17, 1, 0), B.ZERO_ERR_INVALID_ARG),    # R*M > 256
+    (([10], 4, 1, 3, 0), B.ZERO_ERR_INVALID_ARG),
+    (([10], 4, 1, 1, 6), B.ZERO_ERR_INVALID_ARG),      # alignment not a multiple of 4
+    (([10], 4, 1, 1, -4), B.ZERO_ERR_INVALID_ARG),
+    (([10, -1], 4, 1, 1, 0), B.ZERO_ERR_INVALID_ARG),
+    (([2**62, 2**62], 4, 1, 1, 0), B.ZERO_ERR_SIZE),
+])
+def test_plan_create_errors(args, code):
+    with pytest.raises(B.ZeroError) as e:
+        z.Plan(*args)
+    assert e.value.code == code
+
+
+# ---------------------------------------------------- step argument errors --
+# Fake, 256-byte-aligned, non-overlapping addresses: every case below fails
+# validation, which happens on the host before any CUDA call.
+
+BASE = 1 << 40
+
+
+def fake_bufs(plan, gap=1 << 30):
+    c = plan.c
+    addr = [BASE + k * gap for k in range(c.R * c.M + c.R + 5)]
+    grads = addr[:c.R * c.M]
+    params = addr[c.R * c.M:c.R * c.M + c.R]
+    Wp, mp, vp, scr, st = addr[c.R * c.M + c.R:]
+    return grads, Wp, mp, vp, params, scr, st
+
+
+def call_step(plan, grads, Wp, mp, vp, params, hp=None, step=1, variant=0, scratch=None,
+              sbytes=0, flags=0, status=None):
+    import ctypes
+    L = B.lib()
+    ga = B._ptrs(grads)
+    pa = B._ptrs(params)
+    hp = hp if hp is not None else z.hparams()
+    return L.zero_step(plan.ptr, ctypes.addressof(ga), Wp, mp, vp, ctypes.addressof(pa),
+                       ctypes.byref(hp), step, variant, scratch, sbytes, flags, status, None)
+
+
+@pytest.fixture
+def plan():
+    return z.Plan([100_000], 4, 2, 2)
+
+
+def test_step_null_and_align(plan):
+    g, Wp, mp, vp, P, scr, st = fake_bufs(plan)
+    assert call_step(plan, [0] + g[1:], Wp, mp, vp, P) == B.ZERO_ERR_NULL
+    assert call_step(plan, g, 0, mp, vp, P) == B.ZERO_ERR_NULL
+    assert call_step(plan, g, Wp, mp, vp, P[:-1] + [0]) == B.ZERO_ERR_NULL
+    assert call_step(plan, [g[0] + 2] + g[1:], Wp, mp, vp, P) == B.ZERO_ERR_ALIGN
+    assert call_step(plan, g, Wp + 8, mp, vp, P) == B.ZERO_ERR_ALIGN
+    assert call_step(plan, g, Wp, mp, vp, [P[0] + 4] + P[1:]) == B.ZERO_ERR_ALIGN
+
+
+def test_step_invalid_args(plan):
+    g, Wp, mp, vp, P, scr, st = fake_bufs(plan)
+    assert call_step(plan, g, Wp, mp, vp, P, step=0) == B.ZERO_ERR_INVALID_ARG
+    assert call_step(plan, g, Wp, mp, vp, P, variant=2) == B.ZERO_ERR_INVALID_ARG
+    assert call_step(plan, g, Wp, mp, vp, P, flags=4) == B.ZERO_ERR_INVALID_ARG
+    assert call_step(plan, g, Wp, mp, vp, P, flags=1) == B.ZERO_ERR_NULL     # no status word
+    for bad in (dict(beta1=1.0), dict(beta2=1.5), dict(beta1=-0.1), dict(eps=-1.0),
+                dict(lr=float("nan")), dict(weight_decay=float("inf"))):
+        hp = z.hparams(**bad)
+        assert call_step(plan, g, Wp, mp, vp, P, hp=hp) == B.ZERO_ERR_INVALID_ARG, bad
+
+
+def test_step_overlap(plan):
+    g, Wp, mp, vp, P, scr, st = fake_bufs(plan)
+    assert call_step(plan, g, Wp, Wp, vp, P) == B.ZERO_ERR_OVERLAP            # master == m
+    assert call_step(plan, g, Wp, mp, vp, [g[0]] + P[1:]) == B.ZERO_ERR_OVERLAP
+    assert call_step(plan, g, Wp, mp, vp, [P[1]] + P[1:]) == B.ZERO_ERR_OVERLAP
+    # W's range is 4*padded bytes: m starting inside it overlaps
+    assert call_step(plan, g, Wp, Wp + 4 * plan.padded - 16, vp, P) == B.ZERO_ERR_OVERLAP
+    assert call_step(plan, g, Wp, mp, vp, P, status=Wp) == B.ZERO_ERR_OVERLAP
+
+
+def test_step_staged_scratch(plan):
+    g, Wp, mp, vp, P, scr, st = fake_bufs(plan)
+    need = plan.scratch_bytes_staged
+    assert call_step(plan, g, Wp, mp, vp, P, variant=1, scratch=None) == B.ZERO_ERR_NULL
+    assert call_step(plan, g, Wp, mp, vp, P, variant=1, scratch=scr,
+                     sbytes=need - 4) == B.ZERO_ERR_SIZE
+    assert call_step(plan, g, Wp, mp, vp, P, variant=1, scratch=Wp,
+                     sbytes=need) == B.ZERO_ERR_OVERLAP
+
+
+def test_staged_entry_errors(plan):
+    import ctypes
+    L = B.lib()
+    g, Wp, mp, vp, P, scr, st = fake_bufs(plan)
+    ga, pa = B._ptrs(g), B._ptrs(P)
+    assert L.zero_rs_avg(plan.ptr, ctypes.addressof(ga), None, 0, None, None) == B.ZERO_ERR_NULL
+    assert L.zero_rs_avg(plan.ptr, ctypes.addressof(ga), g[0], 0, None, None) == B.ZERO_ERR_OVERLAP
+    hp = z.hparams()
+    assert L.zero_adamw_shard(plan.ptr, scr, Wp, mp, vp, ctypes.byref(hp), 0,
+                              None) == B.ZERO_ERR_INVALID_ARG
+    assert L.zero_adamw_shard(plan.ptr, Wp, Wp, mp, vp, ctypes.byref(hp), 1,
+                              None) == B.ZERO_ERR_OVERLAP
+    assert L.zero_ag_cast(plan.ptr, Wp + 4, ctypes.addressof(pa), None) == B.ZERO_ERR_ALIGN
+    assert L.zero_ag_cast(None, Wp, ctypes.addressof(pa), None) == B.ZERO_ERR_NULL
+
+
+def test_step_host_errors(plan):
+    import ctypes
+    L = B.lib()
+    g, Wp, mp, vp, P, scr, st = fake_bufs(plan)
+    host = [BASE * 2 + k * 4096 for k in range(len(g))]
+    ha, da, pa = B._ptrs(host), B._ptrs(g), B._ptrs(P)
+    hp = z.hparams()
+    assert L.zero_step_host(plan.ptr, ctypes.addressof(ha), ctypes.addressof(da), Wp, mp, vp,
+                            ctypes.addressof(pa), None, ctypes.byref(hp), 1, 0, None,
+                            None) == B.ZERO_ERR_NULL
+    dup = B._ptrs([g[0]] * len(g))                 # copies would overwrite each other
+    assert L.zero_step_host(plan.ptr, ctypes.addressof(ha), ctypes.addressof(dup), Wp, mp, vp,
+                            ctypes.addressof(pa), BASE * 3, ctypes.byref(hp), 1, 0, None,
+                            None) == B.ZERO_ERR_OVERLAP
+
+
+def test_binding_rejects_host_tensors_for_device_arguments():
+    p = z.Plan([1000], 2, 1, 1)
+    cpu = [torch.zeros(1000, dtype=torch.bfloat16) for _ in range(2)]
+    st = [torch.zeros(p.padded, dtype=torch.float32) for _ in range(3)]
+    with pytest.raises(ValueError):
+        z.zero_step(p, cpu, *st, cpu, z.hparams(), 1, stream=0)
+    with pytest.raises(TypeError):
+        z.zero_step(p, [t.float() for t in cpu], *st, cpu, z.hparams(), 1, stream=0)

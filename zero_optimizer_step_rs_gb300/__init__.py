@@ -1,0 +1,15 @@
+"""GB300-native ZeRO-1/2 mixed-precision AdamW step.
+
+R data-parallel ranks are emulated as R buffers in one GPU's HBM; one call
+reduce-scatters their bf16 gradients in fixed rank order with fp32
+accumulation, updates each rank's shard of the fp32 master weights and Adam
+moments, and all-gathers the bf16 result into every rank's replica.  The
+work runs in the hand-written sm_103a kernels of libzero_step.so (C ABI in
+include/zero_step.h); this package is its thin binding.
+"""
+from .binding import (  # noqa: F401
+    EXPORTED, Plan, ZeroError, hparams, lib, zero_abi_version, zero_adamw_shard, zero_ag_cast,
+    zero_plan_create, zero_plan_destroy, zero_plan_owner, zero_rs_avg, zero_status_string,
+    zero_step, zero_step_host, ZERO_DEV_NONFINITE, ZERO_FLAG_CHECK_FINITE, ZERO_VARIANT_FUSED,
+    ZERO_VARIANT_STAGED,
+)

@@ -1,0 +1,296 @@
+"""Thin ctypes binding of libzero_step.so (include/zero_step.h).
+
+Argument marshalling only: tensors become device pointers, the current
+torch stream becomes the cudaStream_t, and status codes become exceptions.
+Every step of the optimizer runs in the library's CUDA kernels; there is no
+fallback.  If the library has not been built the import of the functions
+fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libzero_step.so")
+
+ZERO_OK = 0
+ZERO_ERR_INVALID_ARG = -1
+ZERO_ERR_NULL = -2
+ZERO_ERR_ALIGN = -3
+ZERO_ERR_SIZE = -4
+ZERO_ERR_OVERLAP = -5
+ZERO_ERR_CUDA = -6
+ZERO_ERR_DEVICE_TIMEOUT = -7
+ZERO_ERR_NONFINITE = -8
+ZERO_DEV_NONFINITE = 1
+ZERO_FLAG_CHECK_FINITE = 1
+ZERO_VARIANT_FUSED = 0
+ZERO_VARIANT_STAGED = 1
+ZERO_MAX_R = 64
+ZERO_MAX_RM = 256
+
+EXPORTED = ("zero_abi_version", "zero_status_string", "zero_plan_create", "zero_plan_destroy",
+            "zero_plan_owner", "zero_step", "zero_rs_avg", "zero_adamw_shard", "zero_ag_cast",
+            "zero_step_host")
+
+
+class ZeroError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {zero_status_string(code)} ({code})")
+
+
+class zero_plan_t(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int64), ("S", ctypes.c_int64), ("padded", ctypes.c_int64),
+                ("R", ctypes.c_int32), ("M", ctypes.c_int32), ("stage", ctypes.c_int32),
+                ("align_elems", ctypes.c_int32), ("n_tensors", ctypes.c_int32),
+                ("tensor_offsets", ctypes.POINTER(ctypes.c_int64)),
+                ("bytes_per_rank_dp", ctypes.c_int64), ("bytes_per_rank_z1", ctypes.c_int64),
+                ("bytes_per_rank_z2", ctypes.c_int64), ("bytes_per_rank_z3", ctypes.c_int64),
+                ("bytes_per_rank", ctypes.c_int64), ("scratch_bytes_staged", ctypes.c_int64)]
+
+
+class zero_adamw_hparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float)]
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "zero_optimizer_step_rs_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        P = ctypes.POINTER
+        L.zero_abi_version.argtypes = []
+        L.zero_abi_version.restype = i32
+        L.zero_status_string.argtypes = [ctypes.c_int]
+        L.zero_status_string.restype = ctypes.c_char_p
+        L.zero_plan_create.argtypes = [vp, i32, i32, i32, i32, i32, P(P(zero_plan_t))]
+        L.zero_plan_create.restype = ctypes.c_int
+        L.zero_plan_destroy.argtypes = [P(zero_plan_t)]
+        L.zero_plan_destroy.restype = None
+        L.zero_plan_owner.argtypes = [P(zero_plan_t), i64]
+        L.zero_plan_owner.restype = i32
+        L.zero_step.argtypes = [P(zero_plan_t), vp, vp, vp, vp, vp, P(zero_adamw_hparams), i64,
+                                i32, vp, i64, i32, vp, vp]
+        L.zero_step.restype = ctypes.c_int
+        L.zero_rs_avg.argtypes = [P(zero_plan_t), vp, vp, i32, vp, vp]
+        L.zero_rs_avg.restype = ctypes.c_int
+        L.zero_adamw_shard.argtypes = [P(zero_plan_t), vp, vp, vp, vp, P(zero_adamw_hparams),
+                                       i64, vp]
+        L.zero_adamw_shard.restype = ctypes.c_int
+        L.zero_ag_cast.argtypes = [P(zero_plan_t), vp, vp, vp]
+        L.zero_ag_cast.restype = ctypes.c_int
+        L.zero_step_host.argtypes = [P(zero_plan_t), vp, vp, vp, vp, vp, vp, vp,
+                                     P(zero_adamw_hparams), i64, i32, vp, vp]
+        L.zero_step_host.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def zero_abi_version() -> int:
+    return int(lib().zero_abi_version())
+
+
+def zero_status_string(code: int) -> str:
+    return lib().zero_status_string(code).decode()
+
+
+def _check(code: int, where: str) -> None:
+    if code != ZERO_OK:
+        raise ZeroError(code, where)
+
+
+# ------------------------------------------------------------------ plan --
+
+class Plan:
+    """Owning handle of a zero_plan_t (the shard layout)."""
+
+    def __init__(self, tensor_numels: Sequence[int], R: int, M: int = 1, stage: int = 1,
+                 align_elems: int = 0):
+        arr = (ctypes.c_int64 * max(1, len(tensor_numels)))(*[int(n) for n in tensor_numels])
+        out = ctypes.POINTER(zero_plan_t)()
+        _check(lib().zero_plan_create(ctypes.addressof(arr), len(tensor_numels), R, M, stage,
+                                      align_elems, ctypes.byref(out)), "zero_plan_create")
+        self._p = out
+
+    @property
+    def ptr(self):
+        return self._p
+
+    @property
+    def c(self) -> zero_plan_t:
+        return self._p.contents
+
+    def __getattr__(self, name):
+        if name.startswith("_"):
+            raise AttributeError(name)
+        return getattr(self._p.contents, name)
+
+    def tensor_offsets(self):
+        c = self.c
+        return [c.tensor_offsets[k] for k in range(c.n_tensors + 1)]
+
+    def owner(self, i: int) -> int:
+        return int(lib().zero_plan_owner(self._p, i))
+
+    def close(self):
+        if getattr(self, "_p", None):
+            lib().zero_plan_destroy(self._p)
+            self._p = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def zero_plan_create(tensor_numels, R, M=1, stage=1, align_elems=0) -> Plan:
+    return Plan(tensor_numels, R, M, stage, align_elems)
+
+
+def zero_plan_destroy(plan: Plan) -> None:
+    plan.close()
+
+
+def zero_plan_owner(plan: Plan, i: int) -> int:
+    return plan.owner(i)
+
+
+def hparams(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1) -> zero_adamw_hparams:
+    return zero_adamw_hparams(lr, beta1, beta2, eps, weight_decay)
+
+
+# ------------------------------------------------------------ marshalling --
+
+def _ptrs(values) -> ctypes.Array:
+    return (ctypes.c_void_p * max(1, len(values)))(*[int(v) if v else None for v in values])
+
+
+def _addr(x) -> Optional[int]:
+    """A device/host address from a torch tensor, an int, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check_tensor(t, dtype_name, numel, where, device="cuda"):
+    if isinstance(t, int) or t is None:
+        return
+    import torch
+    want = {"bf16": torch.bfloat16, "f32": torch.float32, "i32": torch.int32}[dtype_name]
+    if t.dtype != want:
+        raise TypeError(f"{where}: expected {want}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{where}: tensor must be contiguous")
+    if t.numel() < numel:
+        raise ValueError(f"{where}: need {numel} elements, got {t.numel()}")
+    if device == "cuda" and not t.is_cuda:
+        raise ValueError(f"{where}: must be a CUDA tensor")
+    if device == "cpu" and t.is_cuda:
+        raise ValueError(f"{where}: must be a host tensor")
+
+
+# -------------------------------------------------------------- the steps --
+
+def zero_step(plan: Plan, rank_grads, master, m, v, rank_params, hp: zero_adamw_hparams,
+              step: int, variant: int = ZERO_VARIANT_FUSED, scratch=None, flags: int = 0,
+              dev_status=None, stream=None) -> None:
+    c = plan.c
+    for k, g in enumerate(rank_grads):
+        _check_tensor(g, "bf16", c.N, f"rank_grads[{k}]")
+    for k, p in enumerate(rank_params):
+        _check_tensor(p, "bf16", c.N, f"rank_params[{k}]")
+    for nm, t in (("master", master), ("m", m), ("v", v)):
+        _check_tensor(t, "f32", c.padded, nm)
+    _check_tensor(dev_status, "i32", 1, "dev_status")
+    if len(rank_grads) != c.R * c.M or len(rank_params) != c.R:
+        raise ValueError(f"need {c.R * c.M} gradient buffers and {c.R} replicas")
+    sbytes = 0
+    if scratch is not None and not isinstance(scratch, int):
+        sbytes = scratch.numel() * scratch.element_size()
+    elif isinstance(scratch, int):
+        sbytes = c.scratch_bytes_staged
+    ga, pa = _ptrs([_addr(g) for g in rank_grads]), _ptrs([_addr(p) for p in rank_params])
+    _check(lib().zero_step(plan.ptr, ctypes.addressof(ga), _addr(master), _addr(m), _addr(v),
+                           ctypes.addressof(pa), ctypes.byref(hp), step, variant,
+                           _addr(scratch), sbytes, flags, _addr(dev_status), _stream(stream)),
+           "zero_step")
+
+
+def zero_rs_avg(plan: Plan, rank_grads, g_shards, flags: int = 0, dev_status=None,
+                stream=None) -> None:
+    c = plan.c
+    for k, g in enumerate(rank_grads):
+        _check_tensor(g, "bf16", c.N, f"rank_grads[{k}]")
+    _check_tensor(g_shards, "f32", c.padded, "g_shards")
+    if len(rank_grads) != c.R * c.M:
+        raise ValueError(f"need {c.R * c.M} gradient buffers")
+    ga = _ptrs([_addr(g) for g in rank_grads])
+    _check(lib().zero_rs_avg(plan.ptr, ctypes.addressof(ga), _addr(g_shards), flags,
+                             _addr(dev_status), _stream(stream)), "zero_rs_avg")
+
+
+def zero_adamw_shard(plan: Plan, g_shards, master, m, v, hp: zero_adamw_hparams, step: int,
+                     stream=None) -> None:
+    c = plan.c
+    for nm, t in (("g_shards", g_shards), ("master", master), ("m", m), ("v", v)):
+        _check_tensor(t, "f32", c.padded, nm)
+    _check(lib().zero_adamw_shard(plan.ptr, _addr(g_shards), _addr(master), _addr(m), _addr(v),
+                                  ctypes.byref(hp), step, _stream(stream)), "zero_adamw_shard")
+
+
+def zero_ag_cast(plan: Plan, master, rank_params, stream=None) -> None:
+    c = plan.c
+    _check_tensor(master, "f32", c.padded, "master")
+    for k, p in enumerate(rank_params):
+        _check_tensor(p, "bf16", c.N, f"rank_params[{k}]")
+    if len(rank_params) != c.R:
+        raise ValueError(f"need {c.R} replicas")
+    pa = _ptrs([_addr(p) for p in rank_params])
+    _check(lib().zero_ag_cast(plan.ptr, _addr(master), ctypes.addressof(pa), _stream(stream)),
+           "zero_ag_cast")
+
+
+def zero_step_host(plan: Plan, host_grads, dev_grads, master, m, v, rank_params,
+                   host_params_out, hp: zero_adamw_hparams, step: int, flags: int = 0,
+                   dev_status=None, stream=None) -> None:
+    c = plan.c
+    for k, g in enumerate(host_grads):
+        _check_tensor(g, "bf16", c.N, f"host_grads[{k}]", device="cpu")
+    for k, g in enumerate(dev_grads):
+        _check_tensor(g, "bf16", c.N, f"dev_grads[{k}]")
+    for k, p in enumerate(rank_params):
+        _check_tensor(p, "bf16", c.N, f"rank_params[{k}]")
+    for nm, t in (("master", master), ("m", m), ("v", v)):
+        _check_tensor(t, "f32", c.padded, nm)
+    _check_tensor(host_params_out, "bf16", c.N, "host_params_out", device="cpu")
+    if len(host_grads) != c.R * c.M or len(dev_grads) != c.R * c.M or len(rank_params) != c.R:
+        raise ValueError("wrong number of buffers")
+    ha = _ptrs([_addr(g) for g in host_grads])
+    da = _ptrs([_addr(g) for g in dev_grads])
+    pa = _ptrs([_addr(p) for p in rank_params])
+    _check(lib().zero_step_host(plan.ptr, ctypes.addressof(ha), ctypes.addressof(da),
+                                _addr(master), _addr(m), _addr(v), ctypes.addressof(pa),
+                                _addr(host_params_out), ctypes.byref(hp), step, flags,
+                                _addr(dev_status), _stream(stream)), "zero_step_host")
