@@ -105,8 +105,12 @@ def compare(got, want, rel_tol=1e-6):
     for name, a, b in (("W", gW, eW), ("m", gm, em), ("v", gv, ev)):
         na, nb = np.isnan(a), np.isnan(b)
         fin = ~(na | nb)
-        rel = np.abs(a[fin].astype(np.float64) - b[fin]) / np.maximum(np.abs(b[fin]), 1e-38)
-        out[name] = int(np.sum(na != nb) + np.sum(rel > rel_tol))
+        a64, b64 = a[fin].astype(np.float64), b[fin].astype(np.float64)
+        same = a64 == b64                          # includes equal infinities
+        with np.errstate(invalid="ignore", over="ignore"):
+            rel = np.abs(a64 - b64) / np.maximum(np.abs(b64), 1e-38)
+        bad = ~same & ~(rel <= rel_tol)            # NaN rel (inf vs -inf) is bad
+        out[name] = int(np.sum(na != nb) + np.sum(bad))
         out[name + "_bits"] = int(np.sum(a.view(np.uint32)[fin] != b.view(np.uint32)[fin]))
     out["replicas"] = int(sum(np.sum(p != eP[0]) for p in gP))
     out["replica_vs_oracle"] = int(sum(np.sum(p != q) for p, q in zip(gP, eP)))
