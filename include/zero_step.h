@@ -212,6 +212,38 @@ zero_status zero_step_host(const zero_plan_t* plan, const uint16_t* const* host_
                            const zero_adamw_hparams* hp, int64_t step, int32_t flags,
                            int32_t* dev_status, void* stream);
 
+/*
+ * Staged step that allocates nothing and takes no scratch argument.
+ * (The lecture pages have no counterpart; this entry point exists for
+ * callers, not for the method.)  Some callers cannot allocate device memory
+ * at all: a host runtime that has already reserved the GPU's memory for its
+ * own pool and forbids other allocations, or a latency-critical caller for
+ * which cudaMalloc, which can synchronize the device, is not allowed.  They
+ * can still run the staged step through this call.  The fp32 reduced
+ * gradient lives in a fixed array of ZERO_NOALLOC_MAX_ELEMS floats (16 MiB)
+ * that this library places in device memory; every GPU that loads the
+ * library holds that array until the process exits.
+ *   - The plan must have plan->padded <= ZERO_NOALLOC_MAX_ELEMS, else
+ *     ZERO_ERR_SIZE is returned and nothing is launched.
+ *   - The first call on a device looks up the array's device address
+ *     (once per device, with that device current); make that first call
+ *     before any stream capture.  A failed lookup returns ZERO_ERR_CUDA.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Every call on a device shares the one array and it keeps the last
+ *     call's contents; nothing needs clearing, because the reduce-scatter
+ *     writes every element the AdamW kernel then reads.  Calls that overlap
+ *     on the GPU (e.g. on two streams at once) race on the array: order
+ *     them on one stream.
+ * Arguments, results and errors are otherwise those of zero_step with
+ * variant ZERO_VARIANT_STAGED; the bits are the same.
+ */
+#define ZERO_NOALLOC_MAX_ELEMS (4 * 1024 * 1024)
+zero_status zero_step_staged_noalloc(const zero_plan_t* plan, const uint16_t* const* rank_grads,
+                                     float* master, float* m, float* v,
+                                     uint16_t* const* rank_params, const zero_adamw_hparams* hp,
+                                     int64_t step, int32_t flags, int32_t* dev_status,
+                                     void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,10 +30,11 @@ ZERO_VARIANT_FUSED = 0
 ZERO_VARIANT_STAGED = 1
 ZERO_MAX_R = 64
 ZERO_MAX_RM = 256
+ZERO_NOALLOC_MAX_ELEMS = 4 * 1024 * 1024
 
 EXPORTED = ("zero_abi_version", "zero_status_string", "zero_plan_create", "zero_plan_destroy",
             "zero_plan_owner", "zero_step", "zero_rs_avg", "zero_adamw_shard", "zero_ag_cast",
-            "zero_step_host")
+            "zero_step_host", "zero_step_staged_noalloc")
 
 
 class ZeroError(RuntimeError):
@@ -92,6 +93,9 @@ def lib():
         L.zero_step_host.argtypes = [P(zero_plan_t), vp, vp, vp, vp, vp, vp, vp,
                                      P(zero_adamw_hparams), i64, i32, vp, vp]
         L.zero_step_host.restype = ctypes.c_int
+        L.zero_step_staged_noalloc.argtypes = [P(zero_plan_t), vp, vp, vp, vp, vp,
+                                               P(zero_adamw_hparams), i64, i32, vp, vp]
+        L.zero_step_staged_noalloc.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -294,3 +298,28 @@ def zero_step_host(plan: Plan, host_grads, dev_grads, master, m, v, rank_params,
                                 _addr(master), _addr(m), _addr(v), ctypes.addressof(pa),
                                 _addr(host_params_out), ctypes.byref(hp), step, flags,
                                 _addr(dev_status), _stream(stream)), "zero_step_host")
+
+
+def zero_step_staged_noalloc(plan: Plan, rank_grads, master, m, v, rank_params,
+                             hp: zero_adamw_hparams, step: int, flags: int = 0, dev_status=None,
+                             stream=None) -> None:
+    """The staged step without a scratch argument, for callers that cannot
+    allocate device memory: the library keeps the reduced gradient in a fixed
+    16 MiB device array (plans with more than ZERO_NOALLOC_MAX_ELEMS padded
+    elements are refused).  The first call on a device looks up that array's
+    address; calls that overlap on the GPU share the array and race."""
+    c = plan.c
+    for k, g in enumerate(rank_grads):
+        _check_tensor(g, "bf16", c.N, f"rank_grads[{k}]")
+    for k, p in enumerate(rank_params):
+        _check_tensor(p, "bf16", c.N, f"rank_params[{k}]")
+    for nm, t in (("master", master), ("m", m), ("v", v)):
+        _check_tensor(t, "f32", c.padded, nm)
+    _check_tensor(dev_status, "i32", 1, "dev_status")
+    if len(rank_grads) != c.R * c.M or len(rank_params) != c.R:
+        raise ValueError(f"need {c.R * c.M} gradient buffers and {c.R} replicas")
+    ga, pa = _ptrs([_addr(g) for g in rank_grads]), _ptrs([_addr(p) for p in rank_params])
+    _check(lib().zero_step_staged_noalloc(plan.ptr, ctypes.addressof(ga), _addr(master),
+                                          _addr(m), _addr(v), ctypes.addressof(pa),
+                                          ctypes.byref(hp), step, flags, _addr(dev_status),
+                                          _stream(stream)), "zero_step_staged_noalloc")

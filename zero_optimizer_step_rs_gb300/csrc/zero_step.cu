@@ -815,3 +815,83 @@ extern "C" zero_status zero_step_host(const zero_plan_t* plan, const uint16_t* c
         return ZERO_ERR_CUDA;
     return ZERO_OK;
 }
+
+// ================================================ staged step, no allocation ==
+// zero_step_staged_noalloc: the staged trio with its fp32 reduced-gradient
+// scratch in a fixed device array of this file instead of a caller buffer,
+// for callers that cannot allocate device memory.  The array's address is a
+// device address only on the device side; host code looks it up once per
+// device with cudaGetSymbolAddress (with that device current) and passes it
+// to the kernels like any other scratch pointer.
+namespace {
+
+static __device__ __align__(256) float g_noalloc_scratch[ZERO_NOALLOC_MAX_ELEMS];
+
+std::mutex g_noalloc_mu;
+float* g_noalloc_addr[64] = {};            // per device ordinal, looked up once
+
+zero_status noalloc_scratch(float** out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ZERO_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();            // clear it so later launch checks do not see it
+            return ZERO_ERR_CUDA;
+        }
+        g_noalloc_addr[dev] = static_cast<float*>(p);
+    }
+    *out = g_noalloc_addr[dev];
+    return ZERO_OK;
+}
+
+}  // namespace
+
+extern "C" zero_status zero_step_staged_noalloc(const zero_plan_t* plan,
+                                                const uint16_t* const* rank_grads, float* master,
+                                                float* m, float* v,
+                                                uint16_t* const* rank_params,
+                                                const zero_adamw_hparams* hp, int64_t step,
+                                                int32_t flags, int32_t* dev_status, void* stream)
+{
+    if (zero_status e = check_plan(plan)) return e;
+    if (plan->padded > (int64_t)ZERO_NOALLOC_MAX_ELEMS) return ZERO_ERR_SIZE;
+    if (zero_status e = check_hparams(hp, step)) return e;
+    if (flags & ~ZERO_FLAG_CHECK_FINITE) return ZERO_ERR_INVALID_ARG;
+    if ((flags & ZERO_FLAG_CHECK_FINITE) && !dev_status) return ZERO_ERR_NULL;
+    if (plan->N == 0) return ZERO_OK;
+
+    Range rs[ZERO_MAX_RM + ZERO_MAX_R + 4];
+    int nr = 0;
+    if (zero_status e = check_grads(plan, rank_grads, rs, nr)) return e;
+    if (zero_status e = check_replicas(plan, rank_params, rs, nr)) return e;
+    if (zero_status e = check_state(plan, master, m, v, rs, nr)) return e;
+    if (dev_status) rs[nr++] = rng(dev_status, 4, true);
+    if (zero_status e = check_overlap(rs, nr)) return e;
+
+    float* scratch = nullptr;
+    if (zero_status e = noalloc_scratch(&scratch)) return e;
+
+    StagedArgs a{};
+    fill_grad_ptrs(a.g, plan, rank_grads);
+    fill_replica_ptrs(a.P, plan, rank_params);
+    a.gs = scratch;
+    a.gs_out = scratch;
+    a.W = master;
+    a.m = m;
+    a.v = v;
+    a.n = plan->N;
+    a.S = plan->S;
+    a.R = plan->R;
+    a.M = plan->M;
+    a.s = step_scalars(*hp, step, plan->R, plan->M);
+    a.status = dev_status;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool check = (flags & ZERO_FLAG_CHECK_FINITE) != 0;
+    cudaError_t err = check ? launch_rs<true>(a, st) : launch_rs<false>(a, st);
+    if (err == cudaSuccess) err = launch_adamw(a, st);
+    if (err == cudaSuccess) err = launch_ag(a, st);
+    return cuda_status(err);
+}
