@@ -223,20 +223,29 @@ def max_over_ranks(x: float, device=None) -> float:
 
 # ------------------------------------------------------------ our arm --
 
+KERNEL_SRC = os.path.join(ROOT, "zero_optimizer_step_rs_gb300", "csrc", "zero_step.cu")
+NOALLOC_MARKER = "// ================================================ staged step, no allocation =="
+
+
+def kernel_source_hash() -> str:
+    """Hash of the kernel source the fused path is compiled from: zero_step.cu
+    up to its allocation-free section (which holds no code of k_fused)."""
+    with open(KERNEL_SRC) as f:
+        body = f.read().split(NOALLOC_MARKER)[0].rstrip()
+    return hashlib.sha256(body.encode()).hexdigest()[:16]
+
+
 def traffic_per_param():
-    """Measured DRAM bytes per parameter of the fused kernel, from the
+    """Measured DRAM bytes per parameter of the fused kernel from the
     committed ncu summary, if it was taken on the current kernel source."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)
-        src = os.path.join(ROOT, "zero_optimizer_step_rs_gb300", "csrc", "zero_step.cu")
-        with open(src, "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()[:16]
-        if rec.get("source_sha256_16") != h:
-            return None, rec
-        return rec, rec
     except (OSError, ValueError):
         return None, None
+    if rec.get("source_sha256_16") != kernel_source_hash():
+        return None, rec
+    return rec, rec
 
 
 def run_ours(args, rank, world, local_rank):
