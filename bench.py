@@ -338,26 +338,34 @@ def run_ours(args, rank, world, local_rank):
         out = torch.empty(N, dtype=torch.bfloat16, pin_memory=True)
         torch.cuda.synchronize()
         k_e2e = max(2, min(args.steps, 5))
-        z.zero_step_host(ds.plan, host_g, ds.grads, ds.W, ds.m, ds.v, ds.params, out, ds.hp,
-                         step_t)
-        step_t += 1
-        torch.cuda.synchronize()
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(k_e2e):
-            z.zero_step_host(ds.plan, host_g, ds.grads, ds.W, ds.m, ds.v, ds.params, out, ds.hp,
-                             step_t)
+
+        def e2e_run(dev_grads):
+            nonlocal step_t
+            z.zero_step_host(ds.plan, host_g, dev_grads, ds.W, ds.m, ds.v, ds.params, out,
+                             ds.hp, step_t)
             step_t += 1
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1)
-        e2e_ms = max_over_ranks(e2e_ms, dev)
-        e2e = {"value": N * k_e2e * world / (e2e_ms / 1e3), "unit": UNIT,
+            torch.cuda.synchronize()
+            barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(k_e2e):
+                z.zero_step_host(ds.plan, host_g, dev_grads, ds.W, ds.m, ds.v, ds.params, out,
+                                 ds.hp, step_t)
+                step_t += 1
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return max_over_ranks(e0.elapsed_time(e1), dev)
+
+        zc_ms = e2e_run(None)                    # zero-copy: kernel reads host memory
+        ce_ms = e2e_run(ds.grads)                # copy engine: copies in, step, copy out
+        e2e = {"value": N * k_e2e * world / (zc_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": 2 * wl.R * wl.M * N, "d2h_bytes_per_step": 2 * N,
-               "ms_per_step": e2e_ms / k_e2e, "steps": k_e2e,
-               "path": "zero_step_host: R*M pinned host->device copies, fused step, "
-                       "replica 0 device->host"}
+               "ms_per_step": zc_ms / k_e2e, "steps": k_e2e,
+               "path": "zero_step_host, zero-copy mode: the fused kernel reads the R*M "
+                       "gradient buffers from pinned host memory over the host link and writes "
+                       "replica 0 back to pinned host memory",
+               "copy_engine_value": N * k_e2e * world / (ce_ms / 1e3),
+               "copy_engine_ms_per_step": ce_ms / k_e2e}
         del host_g, out
 
     launches_per_step = 1 if variant == z.ZERO_VARIANT_FUSED else 3
@@ -390,6 +398,85 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
     }
     return line
+
+
+# -------------------------------------------------------------- table --
+
+def run_table(args):
+    """Every workload (fused and staged) and the flat sweep: median kernel
+    time over reps with an L2 flush before each rep, params/s, GB/s of
+    algorithmic bytes and the fraction of the measured copy peak; the oracle
+    on 1 core and on all host cores for each workload."""
+    import numpy as np
+    import torch
+
+    import zero_optimizer_step_rs_gb300 as z
+    from tests import harness as H
+    from zgen import workloads as W
+
+    torch.cuda.set_device(0)
+    peaks = measured_peaks() or {}
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    rows = []
+
+    def timed(ds, variant, reps):
+        ts = []
+        t = ds.wl.step
+        for k in range(3 + reps):
+            flush.fill_(k & 0xFF)                      # evict L2 (256 MB > 129 MB)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            ds.step(t, variant=variant)
+            e1.record()
+            torch.cuda.synchronize()
+            t += 1
+            if k >= 3:
+                ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+    def bpp(wl, variant):
+        return wl.bytes_per_param() if variant == 0 else 2 * wl.R * wl.M + 36 + 2 * wl.R
+
+    def measure(wl, label, reps, variants=(0, 1)):
+        ds = H.DeviceState(wl, staged_scratch=True)
+        ds.fill_state_device()
+        ds.fill_grads_device(wl.step)
+        torch.cuda.synchronize()
+        for variant in variants:
+            ms = timed(ds, variant, reps)
+            gbs = bpp(wl, variant) * wl.N / (ms / 1e3) / 1e9
+            row = {"workload": label, "R": wl.R, "M": wl.M, "N": wl.N,
+                   "variant": "fused" if variant == 0 else "staged", "ms": round(ms, 4),
+                   "params_per_s": wl.N / (ms / 1e3), "bytes_per_param": bpp(wl, variant),
+                   "GB_s": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
+                   "l2_resident": bpp(wl, variant) * wl.N < 129e6}
+            rows.append(row)
+            print(json.dumps(row), flush=True)
+        del ds
+        torch.cuda.empty_cache()
+
+    for name in ("tiny", "gpt2-small", "llama-3.2-1b", "uneven", "large"):
+        measure(W.ALL[name](), name, reps=20 if name != "large" else 10)
+    for R in (2, 4, 8):
+        S = 1024
+        while S <= 256 * 1024 * 1024:
+            measure(W.sweep_point(R, S), f"sweep R={R} S={S}", reps=20, variants=(0,))
+            S *= 4
+
+    # oracle on 1 core and on all cores, per workload, first 2^22 params
+    for name in ("tiny", "gpt2-small", "llama-3.2-1b", "uneven", "large"):
+        wl = W.ALL[name]()
+        n = min(wl.N, 1 << 22)
+        for th in (1, os.cpu_count() or 1):
+            ctx = oracle_prepare(wl, n, threads=th)
+            tpass = min(oracle_pass(wl, ctx) for _ in range(3))
+            row = {"workload": name, "oracle_threads": th, "sample_params": n,
+                   "params_per_s": n / tpass,
+                   "GB_s": round(wl.bytes_per_param() * n / tpass / 1e9, 2)}
+            rows.append(row)
+            print(json.dumps(row), flush=True)
+    return rows
 
 
 # ------------------------------------------------------- reference arm --
@@ -434,6 +521,8 @@ def main():
     ap.add_argument("--variant", choices=["fused", "staged"], default="fused")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--table", action="store_true",
+                    help="every workload and the flat sweep, one JSON line each")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -441,6 +530,10 @@ def main():
     world = _env_int("WORLD_SIZE", 1)
     rank = _env_int("RANK", 0)
     local_rank = _env_int("LOCAL_RANK", 0)
+
+    if args.table:
+        run_table(args)
+        return 0
 
     if args.impl == "reference":
         if rank != 0:

@@ -199,12 +199,21 @@ zero_status zero_ag_cast(const zero_plan_t* plan, const float* master,
                          uint16_t* const* rank_params, void* stream);
 
 /*
- * End-to-end step from host memory: copies the R*M gradient buffers from
- * host_grads (host pointers; pinned memory lets the copies run at full
- * speed) into dev_grads (device), runs the fused step, and copies replica 0
- * (every replica holds the same bits) into host_params_out (host, N bf16).
+ * End-to-end step from host memory.  host_grads: R*M host pointers to the
+ * gradient buffers (N bf16 each); host_params_out: host, N bf16, receives
+ * replica 0 (every replica holds the same bits).  Two modes:
+ *   dev_grads == NULL (zero-copy): the fused kernel reads the gradients
+ *     straight from host memory over the host link and writes replica 0's
+ *     bits to host_params_out as well as to the R device replicas, so the
+ *     transfers overlap the HBM work.  The host buffers must be reachable by
+ *     the GPU: pinned memory (cudaHostAlloc / cudaHostRegister), or any host
+ *     memory on systems where the GPU uses the host page tables; otherwise
+ *     ZERO_ERR_INVALID_ARG.
+ *   dev_grads != NULL (copy engine): R*M cudaMemcpyAsync copies into
+ *     dev_grads (device, N bf16 each, must not overlap), the fused step,
+ *     then one copy of replica 0 to host_params_out.
  * All on `stream`; the host buffers must stay valid until the stream has
- * finished.  Same argument rules as zero_step.
+ * finished.  Same argument rules as zero_step otherwise.
  */
 zero_status zero_step_host(const zero_plan_t* plan, const uint16_t* const* host_grads,
                            uint16_t* const* dev_grads, float* master, float* m, float* v,

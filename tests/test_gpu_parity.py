@@ -246,7 +246,8 @@ def test_zero_emulation_oracle_agrees_with_gpu():
         assert np.array_equal(p, q)
 
 
-def test_step_from_host_buffers():
+@pytest.mark.parametrize("mode", ["zero_copy", "copy_engine"])
+def test_step_from_host_buffers(mode):
     wl = W.llama32_1b().scaled(100_000)
     G, W0, m0, v0 = H.host_inputs(wl, wl.step)
     want = H.oracle_run(wl, {wl.step: G}, W0, m0, v0, [wl.step])
@@ -255,11 +256,33 @@ def test_step_from_host_buffers():
     host_g = [torch.from_numpy(g.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
               for g in G]
     out = torch.empty(wl.N, dtype=torch.bfloat16).pin_memory()
-    z.zero_step_host(ds.plan, host_g, ds.grads, ds.W, ds.m, ds.v, ds.params, out, ds.hp,
-                     wl.step)
+    z.zero_step_host(ds.plan, host_g, ds.grads if mode == "copy_engine" else None, ds.W, ds.m,
+                     ds.v, ds.params, out, ds.hp, wl.step, flags=z.ZERO_FLAG_CHECK_FINITE,
+                     dev_status=ds.status)
     torch.cuda.synchronize()
     assert np.array_equal(out.view(torch.int16).numpy().view(np.uint16), want[3][0])
     _assert_parity(H.compare(ds.result(), want))
+    assert int(ds.status.item()) == 0
+
+
+def test_step_from_host_pageable_memory():
+    # pageable host memory: refused (ZERO_ERR_INVALID_ARG) unless the GPU can
+    # reach it through the host page tables, in which case the step runs and
+    # must give the same bits as the device replica
+    wl = W.flat(2, 1, 4096)
+    G, W0, m0, v0 = H.host_inputs(wl, 1)
+    ds = H.DeviceState(wl)
+    ds.upload_state(W0, m0, v0)
+    host_g = [torch.from_numpy(g.view(np.int16).copy()).view(torch.bfloat16) for g in G]
+    out = torch.empty(wl.N, dtype=torch.bfloat16)
+    try:
+        z.zero_step_host(ds.plan, host_g, None, ds.W, ds.m, ds.v, ds.params, out, ds.hp, 1)
+        torch.cuda.synchronize()
+    except z.ZeroError as e:
+        assert e.code == -1
+        return
+    want = H.oracle_run(wl, {1: G}, W0, m0, v0, [1])
+    assert np.array_equal(out.view(torch.int16).numpy().view(np.uint16), want[3][0])
 
 
 def test_generator_device_matches_host():

@@ -279,22 +279,29 @@ def zero_ag_cast(plan: Plan, master, rank_params, stream=None) -> None:
 def zero_step_host(plan: Plan, host_grads, dev_grads, master, m, v, rank_params,
                    host_params_out, hp: zero_adamw_hparams, step: int, flags: int = 0,
                    dev_status=None, stream=None) -> None:
+    """End-to-end step from host buffers.  dev_grads=None selects the
+    zero-copy mode (the kernel reads pinned host gradients directly); a list
+    of device buffers selects the copy-engine mode."""
     c = plan.c
     for k, g in enumerate(host_grads):
         _check_tensor(g, "bf16", c.N, f"host_grads[{k}]", device="cpu")
-    for k, g in enumerate(dev_grads):
-        _check_tensor(g, "bf16", c.N, f"dev_grads[{k}]")
+    if dev_grads is not None:
+        for k, g in enumerate(dev_grads):
+            _check_tensor(g, "bf16", c.N, f"dev_grads[{k}]")
+        if len(dev_grads) != c.R * c.M:
+            raise ValueError("wrong number of device gradient buffers")
     for k, p in enumerate(rank_params):
         _check_tensor(p, "bf16", c.N, f"rank_params[{k}]")
     for nm, t in (("master", master), ("m", m), ("v", v)):
         _check_tensor(t, "f32", c.padded, nm)
     _check_tensor(host_params_out, "bf16", c.N, "host_params_out", device="cpu")
-    if len(host_grads) != c.R * c.M or len(dev_grads) != c.R * c.M or len(rank_params) != c.R:
+    if len(host_grads) != c.R * c.M or len(rank_params) != c.R:
         raise ValueError("wrong number of buffers")
     ha = _ptrs([_addr(g) for g in host_grads])
-    da = _ptrs([_addr(g) for g in dev_grads])
     pa = _ptrs([_addr(p) for p in rank_params])
-    _check(lib().zero_step_host(plan.ptr, ctypes.addressof(ha), ctypes.addressof(da),
+    da = _ptrs([_addr(g) for g in dev_grads]) if dev_grads is not None else None
+    _check(lib().zero_step_host(plan.ptr, ctypes.addressof(ha),
+                                ctypes.addressof(da) if da is not None else None,
                                 _addr(master), _addr(m), _addr(v), ctypes.addressof(pa),
                                 _addr(host_params_out), ctypes.byref(hp), step, flags,
                                 _addr(dev_status), _stream(stream)), "zero_step_host")

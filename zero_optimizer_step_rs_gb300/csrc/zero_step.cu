@@ -93,6 +93,7 @@ struct FusedArgs {
     int32_t R, M;
     StepScalars s;
     int32_t* status;
+    uint16_t* extra_rep;  // optional extra copy of the replica (e.g. in host memory)
 };
 
 struct StagedArgs {
@@ -238,7 +239,10 @@ __device__ __forceinline__ void report_nonfinite(bool bad, int32_t* status)
 
 // ---------------------------------------------------------- fused step --
 
-template <int RC, int MC, int U, bool CHECK>
+// XREP: also write the replica bits to a.extra_rep (the host-buffer entry
+// point's zero-copy mode); a template switch so the plain path carries no
+// extra branch or register pressure.
+template <int RC, int MC, int U, bool CHECK, bool XREP>
 __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ FusedArgs a)
 {
     const int R = RC > 0 ? RC : a.R;
@@ -282,6 +286,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ Fuse
             } else {
                 for (int r = 0; r < R; ++r) st_stream(a.P.p[r] + e, p);
             }
+            if constexpr (XREP) st_stream(a.extra_rep + e, p);
         }
     }
 
@@ -298,6 +303,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ Fuse
             a.v[i] = v;
             const uint16_t p = to_bf16(w);
             for (int r = 0; r < R; ++r) a.P.p[r][i] = p;
+            if constexpr (XREP) a.extra_rep[i] = p;
         }
     }
     report_nonfinite<CHECK>(bad, a.status);
@@ -446,19 +452,22 @@ unsigned grid_for(const void* kernel, int64_t work_blocks)
 
 // ----------------------------------------------------- fused dispatch --
 
-template <int RC, int MC, bool CHECK>
+template <int RC, int MC, bool CHECK, bool XREP = false>
 cudaError_t launch_fused_t(const FusedArgs& a, cudaStream_t st)
 {
     constexpr int U = 2;
-    const void* k = reinterpret_cast<const void*>(&k_fused<RC, MC, U, CHECK>);
+    const void* k = reinterpret_cast<const void*>(&k_fused<RC, MC, U, CHECK, XREP>);
     const int64_t tiles = (a.n + kUnit * U - 1) / (kUnit * U);
-    k_fused<RC, MC, U, CHECK><<<grid_for(k, tiles), kThreads, 0, st>>>(a);
+    k_fused<RC, MC, U, CHECK, XREP><<<grid_for(k, tiles), kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 
 template <bool CHECK>
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st)
 {
+    // the zero-copy host path is bound by the host link, not by HBM: one
+    // run-time (R, M) instantiation serves it
+    if (a.extra_rep) return launch_fused_t<0, 0, CHECK, true>(a, st);
     const int R = a.R, M = a.M;
 #define ZERO_CASE(r_, m_) \
     if (R == r_ && M == m_) return launch_fused_t<r_, m_, CHECK>(a, st);
@@ -771,6 +780,23 @@ extern "C" zero_status zero_ag_cast(const zero_plan_t* plan, const float* master
     return cuda_status(launch_ag(a, static_cast<cudaStream_t>(stream)));
 }
 
+// Device-side address of a host buffer the kernels may read or write over the
+// host link: pinned (cudaHostAlloc / cudaHostRegister) memory maps to a
+// device pointer; on systems where the GPU walks the host page tables any
+// host pointer is usable as is.  Returns nullptr when the GPU cannot reach it.
+static const void* device_view_of_host(const void* p, bool pageable_ok)
+{
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return pageable_ok ? p : nullptr;
+    }
+    if (at.type == cudaMemoryTypeHost && at.devicePointer) return at.devicePointer;
+    if (at.type == cudaMemoryTypeManaged) return p;
+    if (at.type == cudaMemoryTypeUnregistered && pageable_ok) return p;
+    return nullptr;
+}
+
 extern "C" zero_status zero_step_host(const zero_plan_t* plan, const uint16_t* const* host_grads,
                                       uint16_t* const* dev_grads, float* master, float* m,
                                       float* v, uint16_t* const* rank_params,
@@ -780,13 +806,18 @@ extern "C" zero_status zero_step_host(const zero_plan_t* plan, const uint16_t* c
 {
     if (zero_status e = check_plan(plan)) return e;
     if (zero_status e = check_hparams(hp, step)) return e;
-    if (!host_grads || !dev_grads || !host_params_out) return ZERO_ERR_NULL;
+    if (!host_grads || !host_params_out) return ZERO_ERR_NULL;
+    if (flags & ~ZERO_FLAG_CHECK_FINITE) return ZERO_ERR_INVALID_ARG;
+    if ((flags & ZERO_FLAG_CHECK_FINITE) && !dev_status) return ZERO_ERR_NULL;
     if (plan->N == 0) return ZERO_OK;
     const int RM = plan->R * plan->M;
     for (int q = 0; q < RM; ++q)
         if (!host_grads[q]) return ZERO_ERR_NULL;
-    // validate the device side before any copy is enqueued
-    {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t gbytes = (size_t)plan->N * 2;
+
+    if (dev_grads) {
+        // copy-engine mode: validate the device side before any copy is enqueued
         Range rs[ZERO_MAX_RM + ZERO_MAX_R + 5];
         int nr = 0;
         const uint16_t* const* dg = dev_grads;
@@ -799,21 +830,55 @@ extern "C" zero_status zero_step_host(const zero_plan_t* plan, const uint16_t* c
         Range gr[ZERO_MAX_RM];
         for (int q = 0; q < RM; ++q) gr[q] = rng(dev_grads[q], 2 * plan->N, true);
         if (zero_status e = check_overlap(gr, RM)) return e;
-    }
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const size_t gbytes = (size_t)plan->N * 2;
-    for (int q = 0; q < RM; ++q)
-        if (cudaMemcpyAsync(dev_grads[q], host_grads[q], gbytes, cudaMemcpyHostToDevice, st) !=
-            cudaSuccess)
+        for (int q = 0; q < RM; ++q)
+            if (cudaMemcpyAsync(dev_grads[q], host_grads[q], gbytes, cudaMemcpyHostToDevice,
+                                st) != cudaSuccess)
+                return ZERO_ERR_CUDA;
+        zero_status e = zero_step(plan, dg, master, m, v, rank_params, hp, step,
+                                  ZERO_VARIANT_FUSED, nullptr, 0, flags, dev_status, stream);
+        if (e != ZERO_OK) return e;
+        if (cudaMemcpyAsync(host_params_out, rank_params[0], gbytes, cudaMemcpyDeviceToHost,
+                            st) != cudaSuccess)
             return ZERO_ERR_CUDA;
-    const uint16_t* const* dg = dev_grads;
-    zero_status e = zero_step(plan, dg, master, m, v, rank_params, hp, step, ZERO_VARIANT_FUSED,
-                              nullptr, 0, flags, dev_status, stream);
-    if (e != ZERO_OK) return e;
-    if (cudaMemcpyAsync(host_params_out, rank_params[0], gbytes, cudaMemcpyDeviceToHost, st) !=
-        cudaSuccess)
-        return ZERO_ERR_CUDA;
-    return ZERO_OK;
+        return ZERO_OK;
+    }
+
+    // zero-copy mode: the fused kernel reads the gradients from host memory and
+    // writes replica 0's bits to host_params_out as well as to the R device
+    // replicas, so the host-link transfers overlap the HBM work
+    int dev = 0, pageable = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_ERR_CUDA;
+    cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev);
+    FusedArgs a{};
+    Range rs[ZERO_MAX_RM + ZERO_MAX_R + 6];
+    int nr = 0;
+    for (int q = 0; q < RM; ++q) {
+        const void* dp = device_view_of_host(host_grads[q], pageable != 0);
+        if (!dp) return ZERO_ERR_INVALID_ARG;
+        if (!aligned16(dp)) return ZERO_ERR_ALIGN;
+        a.g.p[q] = static_cast<const uint16_t*>(dp);
+        rs[nr++] = rng(dp, 2 * plan->N, false);
+    }
+    void* out = const_cast<void*>(device_view_of_host(host_params_out, pageable != 0));
+    if (!out) return ZERO_ERR_INVALID_ARG;
+    if (!aligned16(out)) return ZERO_ERR_ALIGN;
+    rs[nr++] = rng(out, 2 * plan->N, true);
+    if (zero_status e = check_replicas(plan, rank_params, rs, nr)) return e;
+    if (zero_status e = check_state(plan, master, m, v, rs, nr)) return e;
+    if (dev_status) rs[nr++] = rng(dev_status, 4, true);
+    if (zero_status e = check_overlap(rs, nr)) return e;
+    fill_replica_ptrs(a.P, plan, rank_params);
+    a.extra_rep = static_cast<uint16_t*>(out);
+    a.W = master;
+    a.m = m;
+    a.v = v;
+    a.n = plan->N;
+    a.R = plan->R;
+    a.M = plan->M;
+    a.s = step_scalars(*hp, step, plan->R, plan->M);
+    a.status = dev_status;
+    const bool check = (flags & ZERO_FLAG_CHECK_FINITE) != 0;
+    return cuda_status(check ? launch_fused<true>(a, st) : launch_fused<false>(a, st));
 }
 
 // ================================================ staged step, no allocation ==
