@@ -103,6 +103,16 @@ def lib():
             L.oracle_zero_bytes.argtypes = [ctypes.c_double, i32, ctypes.c_double,
                                             ctypes.c_double, ctypes.c_double, vp]
             L.oracle_zero_bytes.restype = None
+            L.oracle_grad_sumsq.argtypes = [vp, i64]
+            L.oracle_grad_sumsq.restype = ctypes.c_double
+            L.oracle_clip_coef.argtypes = [ctypes.c_double, ctypes.c_float,
+                                           ctypes.POINTER(ctypes.c_int32)]
+            L.oracle_clip_coef.restype = ctypes.c_float
+            L.oracle_dp_step_clipped.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp,
+                                                 ctypes.POINTER(HParams), i64, ctypes.c_float,
+                                                 i32, ctypes.POINTER(ctypes.c_double),
+                                                 ctypes.POINTER(ctypes.c_int32)]
+            L.oracle_dp_step_clipped.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -229,3 +239,38 @@ def zero_bytes(N: float, P: int, bp: float, bg: float, bo: float):
     out = np.zeros(4, np.float64)
     lib().oracle_zero_bytes(float(N), P, float(bp), float(bg), float(bo), _ptr(out))
     return out
+
+
+def grad_sumsq(g: np.ndarray) -> float:
+    """Pairwise fp64 sum of squares of a float32 vector (reading R10)."""
+    _check(g, np.float32, None, "g")
+    return float(lib().oracle_grad_sumsq(_ptr(g), g.size))
+
+
+def clip_coef(sumsq: float, max_norm: float):
+    clip = ctypes.c_int32(0)
+    c = lib().oracle_clip_coef(sumsq, max_norm, ctypes.byref(clip))
+    return float(c), bool(clip.value)
+
+
+def dp_step_clipped(G, W, m, v, P, hp: HParams, step: int, R: int, M: int,
+                    max_norm: float, skip_nonfinite: bool = False):
+    """DP step with global-norm clipping, in place; returns (sumsq, skipped)."""
+    n = W.size
+    if len(G) != R * M or len(P) != R:
+        raise ValueError("need R*M gradient buffers and R replicas")
+    for k, g in enumerate(G):
+        _check(g, np.uint16, n, f"G[{k}]")
+    for k, p in enumerate(P):
+        _check(p, np.uint16, n, f"P[{k}]")
+    for nm, a in (("W", W), ("m", m), ("v", v)):
+        _check(a, np.float32, n, nm)
+    ga, pa = _ptr_array(G), _ptr_array(P)
+    ss = ctypes.c_double(0.0)
+    sk = ctypes.c_int32(0)
+    rc = lib().oracle_dp_step_clipped(n, R, M, ctypes.addressof(ga), _ptr(W), _ptr(m), _ptr(v),
+                                      ctypes.addressof(pa), ctypes.byref(hp), step, max_norm,
+                                      int(skip_nonfinite), ctypes.byref(ss), ctypes.byref(sk))
+    if rc != 0:
+        raise RuntimeError(f"oracle_dp_step_clipped failed: {rc}")
+    return ss.value, bool(sk.value)

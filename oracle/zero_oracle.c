@@ -356,3 +356,69 @@ void oracle_zero_bytes(double N, int32_t P, double bp, double bg, double bo,
     out[2] = N * bp + N * (bg + bo) / P;
     out[3] = N * (bp + bg + bo) / P;
 }
+
+/* ------------------------------------------------------------ clipping -- */
+
+/* the pairwise tree over [lo, lo + len), len a power of two */
+static double sumsq_tree(const float* g, int64_t n, int64_t lo, int64_t len)
+{
+    if (len == 1) {
+        if (lo >= n) return 0.0;
+        double x = (double)g[lo];
+        return x * x;
+    }
+    int64_t half = len / 2;
+    if (lo >= n) return 0.0;                       /* an all-padding subtree */
+    return sumsq_tree(g, n, lo, half) + sumsq_tree(g, n, lo + half, half);
+}
+
+double oracle_grad_sumsq(const float* g, int64_t n)
+{
+    if (n <= 0) return 0.0;
+    int64_t len = 1;
+    while (len < n) len *= 2;
+    return sumsq_tree(g, n, 0, len);
+}
+
+float oracle_clip_coef(double sumsq, float max_norm, int32_t* clip)
+{
+    double norm = sqrt(sumsq);
+    double coef = (double)max_norm / (norm + 1e-6);
+    if (coef < 1.0) {
+        *clip = 1;
+        return (float)coef;
+    }
+    *clip = 0;                 /* also when coef is NaN: no clipping applied */
+    return 1.0f;
+}
+
+int oracle_dp_step_clipped(int64_t n, int32_t R, int32_t M,
+                           const uint16_t* const* G, float* W, float* m, float* v,
+                           uint16_t* const* P, const oracle_hparams* hp,
+                           int64_t step, float max_norm, int32_t skip_nonfinite,
+                           double* sumsq_out, int32_t* skipped_out)
+{
+    if (check_args(n, R, M, G, W, m, v, P, hp, step)) return -1;
+    oracle_scalars s;
+    oracle_make_scalars(hp, step, R, M, &s);
+    float* g = (float*)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1));
+    if (!g) return -2;
+    for (int64_t i = 0; i < n; ++i) g[i] = oracle_avg_grad(G, R, M, i, s.denom_rm);
+    double sumsq = oracle_grad_sumsq(g, n);
+    if (sumsq_out) *sumsq_out = sumsq;
+    int32_t skipped = 0;
+    if (!isfinite(sumsq) && skip_nonfinite) skipped = 1;
+    if (skipped_out) *skipped_out = skipped;
+    if (!skipped) {
+        int32_t clip = 0;
+        float coef = oracle_clip_coef(sumsq, max_norm, &clip);
+        for (int64_t i = 0; i < n; ++i) {
+            float gi = clip ? g[i] * coef : g[i];
+            oracle_adamw_elem(&s, gi, &W[i], &m[i], &v[i]);
+            uint16_t p = oracle_bf16_rne(W[i]);
+            for (int32_t r = 0; r < R; ++r) P[r][i] = p;
+        }
+    }
+    free(g);
+    return 0;
+}

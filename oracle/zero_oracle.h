@@ -159,6 +159,43 @@ int oracle_ring_allreduce(float* const* cards, int32_t p, int64_t n,
 void oracle_zero_bytes(double N, int32_t P, double bp, double bg, double bo,
                        double out[4]);
 
+/* ------------------------------------------------------------------------
+ * Global gradient-norm clipping with a non-finite check, before the update
+ * (the training recipe "AdamW + gradient clipping", CS324 Lecture 9 notes,
+ * section 7.4; fp32 gradient reduction, LLM infra 06, section 15.3).
+ * Readings (listed in the repository's design notes):
+ *   R10 the squared norm is the fp64 pairwise (binary-tree) sum of the
+ *       leaves (double)g_i * (double)g_i, i < n, padded with zeros to the
+ *       next power of two: one fixed order, so every implementation that
+ *       follows the tree gets the same bits;
+ *   R11 norm = sqrt(sumsq); coef = max_norm / (norm + 1e-6) in double (the
+ *       clip_grad_norm_ formula); when coef < 1 every averaged gradient is
+ *       multiplied by (float)coef, otherwise it is left alone;
+ *   R12 a non-finite sumsq is reported; with skip_nonfinite the whole step
+ *       is skipped (state and replicas untouched), otherwise the formula
+ *       runs on as IEEE arithmetic gives it.
+ * ---------------------------------------------------------------------- */
+
+/* Pairwise fp64 sum of g[i]^2 over n leaves padded to a power of two. */
+double oracle_grad_sumsq(const float* g, int64_t n);
+
+/* Clip coefficient from the squared norm: returns the float multiplier and
+ * sets *clip to 1 when coef < 1; otherwise (coef >= 1, or coef NaN because
+ * the norm is NaN) returns 1.0f and sets *clip to 0. */
+float oracle_clip_coef(double sumsq, float max_norm, int32_t* clip);
+
+/* DP step with global-norm clipping: averaged gradients (as oracle_dp_step),
+ * squared norm (R10), coefficient (R11), non-finite handling (R12), then the
+ * AdamW update and the replica write of oracle_dp_step.  *sumsq_out (may be
+ * NULL) receives the squared norm; *skipped_out (may be NULL) is set to 1 when
+ * the step was skipped.  Returns 0, -1 on a bad argument, -2 on allocation
+ * failure. */
+int oracle_dp_step_clipped(int64_t n, int32_t R, int32_t M,
+                           const uint16_t* const* G, float* W, float* m, float* v,
+                           uint16_t* const* P, const oracle_hparams* hp,
+                           int64_t step, float max_norm, int32_t skip_nonfinite,
+                           double* sumsq_out, int32_t* skipped_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -42,6 +42,16 @@ MUTANTS = {
     "zero2_formula_swapped": ("out[2] = N * bp + N * (bg + bo) / P;",
                               "out[2] = N * (bp + bg) + N * bo / P;"),
     "shard_len_no_roundup": ("return (per + align - 1) / align * align;", "return per + 0 * align;"),
+    "sumsq_left_to_right": ("return sumsq_tree(g, n, 0, len);",
+                            "double acc = 0.0; for (int64_t i = 0; i < n; ++i) acc += (double)g[i] * (double)g[i]; return acc + 0.0 * len;"),
+    "sumsq_float_squares": ("double x = (double)g[lo];\n        return x * x;",
+                            "return (double)(g[lo] * g[lo]);"),
+    "clip_coef_without_epsilon": ("double coef = (double)max_norm / (norm + 1e-6);",
+                                  "double coef = (double)max_norm / norm;"),
+    "clip_condition_inverted": ("if (coef < 1.0) {", "if (coef > 1.0) {"),
+    "clip_divides": ("float gi = clip ? g[i] * coef : g[i];", "float gi = clip ? g[i] / coef : g[i];"),
+    "skip_ignores_flag": ("if (!isfinite(sumsq) && skip_nonfinite) skipped = 1;",
+                          "if (!isfinite(sumsq) || skip_nonfinite < 0) skipped = 1;"),
 }
 
 
@@ -58,6 +68,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
                     str(mut_src), "-lm", "-lpthread"], check=True)
     env = dict(os.environ, ZERO_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        "tests/test_oracle_pins.py", "tests/test_oracle_collectives.py"],
+                        "tests/test_oracle_pins.py", "tests/test_oracle_collectives.py",
+                        "tests/test_oracle_clip.py"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
