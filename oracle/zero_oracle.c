@@ -359,17 +359,20 @@ void oracle_zero_bytes(double N, int32_t P, double bp, double bg, double bo,
 
 /* ------------------------------------------------------------ clipping -- */
 
-/* the pairwise tree over [lo, lo + len), len a power of two */
-static double sumsq_tree(const float* g, int64_t n, int64_t lo, int64_t len)
+/* the pairwise tree over [lo, lo + len), len a power of two; every leaf is
+ * the fp32 product g*g and every node an fp32 sum (reading R10) */
+static float sumsq_tree(const float* g, int64_t n, int64_t lo, int64_t len)
 {
     if (len == 1) {
-        if (lo >= n) return 0.0;
-        double x = (double)g[lo];
+        if (lo >= n) return 0.0f;
+        float x = g[lo];
         return x * x;
     }
     int64_t half = len / 2;
-    if (lo >= n) return 0.0;                       /* an all-padding subtree */
-    return sumsq_tree(g, n, lo, half) + sumsq_tree(g, n, lo + half, half);
+    if (lo >= n) return 0.0f;                      /* an all-padding subtree */
+    float left = sumsq_tree(g, n, lo, half);
+    float right = sumsq_tree(g, n, lo + half, half);
+    return left + right;
 }
 
 double oracle_grad_sumsq(const float* g, int64_t n)
@@ -377,7 +380,7 @@ double oracle_grad_sumsq(const float* g, int64_t n)
     if (n <= 0) return 0.0;
     int64_t len = 1;
     while (len < n) len *= 2;
-    return sumsq_tree(g, n, 0, len);
+    return (double)sumsq_tree(g, n, 0, len);
 }
 
 float oracle_clip_coef(double sumsq, float max_norm, int32_t* clip)

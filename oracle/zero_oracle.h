@@ -164,10 +164,11 @@ void oracle_zero_bytes(double N, int32_t P, double bp, double bg, double bo,
  * (the training recipe "AdamW + gradient clipping", CS324 Lecture 9 notes,
  * section 7.4; fp32 gradient reduction, LLM infra 06, section 15.3).
  * Readings (listed in the repository's design notes):
- *   R10 the squared norm is the fp64 pairwise (binary-tree) sum of the
- *       leaves (double)g_i * (double)g_i, i < n, padded with zeros to the
+ *   R10 the squared norm is the fp32 pairwise (binary-tree) sum of the
+ *       leaves g_i * g_i (fp32 products), i < n, padded with zeros to the
  *       next power of two: one fixed order, so every implementation that
- *       follows the tree gets the same bits;
+ *       follows the tree gets the same bits (fp32, the precision
+ *       clip_grad_norm_ uses for fp32 gradients);
  *   R11 norm = sqrt(sumsq); coef = max_norm / (norm + 1e-6) in double (the
  *       clip_grad_norm_ formula); when coef < 1 every averaged gradient is
  *       multiplied by (float)coef, otherwise it is left alone;
@@ -176,10 +177,12 @@ void oracle_zero_bytes(double N, int32_t P, double bp, double bg, double bo,
  *       runs on as IEEE arithmetic gives it.
  * ---------------------------------------------------------------------- */
 
-/* Pairwise fp64 sum of g[i]^2 over n leaves padded to a power of two. */
+/* Pairwise fp32 sum of g[i]*g[i] over n leaves padded to a power of two
+ * (returned widened to double). */
 double oracle_grad_sumsq(const float* g, int64_t n);
 
-/* Clip coefficient from the squared norm: returns the float multiplier and
+/* Clip coefficient from the squared norm (norm = sqrt(sumsq) and the
+ * quotient in double): returns the float multiplier and
  * sets *clip to 1 when coef < 1; otherwise (coef >= 1, or coef NaN because
  * the norm is NaN) returns 1.0f and sets *clip to 0. */
 float oracle_clip_coef(double sumsq, float max_norm, int32_t* clip);

@@ -30,8 +30,9 @@ def test_sumsq_of_ones(n):
     assert oracle.grad_sumsq(np.ones(n, np.float32)) == float(n)
 
 
-@pytest.mark.parametrize("n", [1, 2, 17, 4096])
+@pytest.mark.parametrize("n", [1, 2, 17, 64, 300])
 def test_sumsq_of_integers_closed_form(n):
+    # every partial sum stays below 2^24, so the fp32 tree is exact
     g = np.arange(n, dtype=np.float32)
     assert oracle.grad_sumsq(g) == (n - 1) * n * (2 * n - 1) // 6
 
@@ -41,19 +42,20 @@ def test_sumsq_tree_order_hand_worked():
     for k in ("8", "16"):
         g = np.array(gd["g" + k], np.float32)
         got = oracle.grad_sumsq(g)
-        assert got == 2.0 ** 54 + gd[f"sumsq{k}_minus_2p54"]
+        assert got == 2.0 ** 24 + gd[f"sumsq{k}_minus_2p24"]
         assert got != math.fsum(float(x) ** 2 for x in g)          # not the exact sum
-        seq = 0.0
+        seq = np.float32(0.0)
         for x in g:
-            seq += float(x) ** 2
-        assert got != seq                                          # not left to right
+            seq = np.float32(seq + np.float32(x) * np.float32(x))
+        assert got != float(seq)                                   # not left to right
 
 
 def test_sumsq_close_to_exact_sum():
+    # fp32 pairwise error bound: about log2(n) half-ulps, 17 * 2^-24 here
     rng = np.random.default_rng(4)
     g = rng.normal(0, 1e-3, 100_003).astype(np.float32)
     exact = math.fsum(float(x) ** 2 for x in g)
-    assert abs(oracle.grad_sumsq(g) - exact) <= 1e-14 * exact
+    assert abs(oracle.grad_sumsq(g) - exact) <= 18 * 2.0 ** -24 * exact
 
 
 def test_clip_coef_cases():
@@ -100,10 +102,9 @@ def test_no_clipping_equals_plain_step(R, M):
 @pytest.mark.parametrize("R,M", [(1, 1), (4, 2), (3, 1)])
 def test_clipping_scales_the_averaged_gradient(R, M):
     # At step 1 with m = v = 0 the moments are m' = (1-b1) g' and
-    # v' = ((1-b2) g') g', so they expose g' = g * coef directly.  The
-    # coefficient is formed here from a math.fsum norm, independent of the
-    # oracle's tree (the two agree unless the float rounding of coef sits on a
-    # boundary, which these seeds avoid).
+    # v' = ((1-b2) g') g', so they expose g' = g * coef directly.  The norm is
+    # checked against math.fsum; the coefficient is then formed from the
+    # oracle's own squared norm (pinned above) to test where it is applied.
     n = 2049
     G, W0, _, _ = _inputs(n, R, M, 11 * R + M)
     g = None
@@ -115,13 +116,13 @@ def test_clipping_scales_the_averaged_gradient(R, M):
     g = (g / np.float32(R * M)).astype(np.float32)
     norm = math.sqrt(math.fsum(float(x) ** 2 for x in g))
     max_norm = float(np.float32(0.3 * norm))
-    coef = np.float32(max_norm / (norm + 1e-6))
-    gp = (g * coef).astype(np.float32)
     hp = oracle.hparams()
     W, m, v = W0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
     ss, sk = oracle.dp_step_clipped(G, W, m, v, [np.zeros(n, np.uint16)] * R, hp, 1, R, M,
                                     max_norm=max_norm)
-    assert not sk and abs(math.sqrt(ss) - norm) <= 1e-15 * norm
+    assert not sk and abs(math.sqrt(ss) - norm) <= 1e-6 * norm
+    coef = np.float32(max_norm / (math.sqrt(ss) + 1e-6))
+    gp = (g * coef).astype(np.float32)
     omb1, omb2 = np.float32(1.0 - np.float64(np.float32(0.9))), \
         np.float32(1.0 - np.float64(np.float32(0.95)))
     assert np.array_equal(m, (omb1 * gp).astype(np.float32))

@@ -42,10 +42,12 @@ MUTANTS = {
     "zero2_formula_swapped": ("out[2] = N * bp + N * (bg + bo) / P;",
                               "out[2] = N * (bp + bg) + N * bo / P;"),
     "shard_len_no_roundup": ("return (per + align - 1) / align * align;", "return per + 0 * align;"),
-    "sumsq_left_to_right": ("return sumsq_tree(g, n, 0, len);",
-                            "double acc = 0.0; for (int64_t i = 0; i < n; ++i) acc += (double)g[i] * (double)g[i]; return acc + 0.0 * len;"),
-    "sumsq_float_squares": ("double x = (double)g[lo];\n        return x * x;",
-                            "return (double)(g[lo] * g[lo]);"),
+    "sumsq_left_to_right": ("return (double)sumsq_tree(g, n, 0, len);",
+                            "float acc = 0.0f; for (int64_t i = 0; i < n; ++i) acc += g[i] * g[i]; return (double)acc + 0.0 * len;"),
+    "sumsq_double_accumulation": ("return (double)sumsq_tree(g, n, 0, len);",
+                                  "double acc = 0.0; for (int64_t i = 0; i < n; ++i) acc += (double)g[i] * (double)g[i]; return acc + 0.0 * len;"),
+    "sumsq_leaf_not_squared": ("float x = g[lo];\n        return x * x;",
+                               "float x = g[lo];\n        return fabsf(x);"),
     "clip_coef_without_epsilon": ("double coef = (double)max_norm / (norm + 1e-6);",
                                   "double coef = (double)max_norm / norm;"),
     "clip_condition_inverted": ("if (coef < 1.0) {", "if (coef > 1.0) {"),
