@@ -208,6 +208,14 @@ def oracle_sample_rate(wl, target_s=12.0, sample_elems=1 << 24, threads=None):
     return n * reps / elapsed, ctx["threads"], desc
 
 
+def _tree_levels(N: int):
+    """Partial counts of the clipped step's norm tree (2048 leaves a block)."""
+    lv = [max(1, -(-N // 2048))]
+    while lv[-1] > 1:
+        lv.append(-(-lv[-1] // 2048))
+    return lv
+
+
 def max_over_ranks(x: float, device=None) -> float:
     """The maximum of a per-rank float over all ranks of the default process
     group (the identity without one).  Timing only: no step data crosses
@@ -260,9 +268,12 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     wl = W.by_name(args.workload)
     variant = z.ZERO_VARIANT_STAGED if args.variant == "staged" else z.ZERO_VARIANT_FUSED
+    clipped = args.variant == "clipped"
     stream = torch.cuda.current_stream()
 
     ds = H.DeviceState(wl, str(dev), staged_scratch=(variant == z.ZERO_VARIANT_STAGED))
+    if clipped:
+        ds.step = lambda t, variant=0, flags=0: ds.step_clipped(t, args.max_norm, flags=flags)
     ds.fill_state_device()
     t = wl.first_step()
     while t < wl.step:                     # prior steps build the moments
@@ -310,8 +321,12 @@ def run_ours(args, rank, world, local_rank):
     N = wl.N
     ms_per_step = total_ms / args.steps
     value = N * args.steps * world / (total_ms / 1e3)
-    bpp = wl.bytes_per_param() if variant == z.ZERO_VARIANT_FUSED else (
-        2 * wl.R * wl.M + 4 + 4 + 24 + 4 + 2 * wl.R)
+    if clipped:
+        bpp = 2 * wl.R * wl.M + 4 + 4 + 24 + 2 * wl.R      # stash written and read back
+    elif variant == z.ZERO_VARIANT_FUSED:
+        bpp = wl.bytes_per_param()
+    else:
+        bpp = 2 * wl.R * wl.M + 4 + 4 + 24 + 4 + 2 * wl.R
     alg_bytes = bpp * N
     avg_launch_s = float(np.mean(launch_ms)) / 1e3
     achieved_gbs = alg_bytes / avg_launch_s / 1e9
@@ -322,16 +337,19 @@ def run_ours(args, rank, world, local_rank):
         peak, peak_src = 6800.0, "fallback"
     rec, _ = traffic_per_param()
     traffic = None
-    if rec and variant == z.ZERO_VARIANT_FUSED and rec.get("R") == wl.R and rec.get("M") == wl.M:
+    if (rec and variant == z.ZERO_VARIANT_FUSED and not clipped and rec.get("R") == wl.R
+            and rec.get("M") == wl.M):
         traffic = round(rec["dram_bytes_per_param"] * N)
     roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved_gbs / peak, 4), "traffic": traffic,
-                "peak_source": peak_src, "kernel": "k_fused" if variant == 0 else "staged trio",
+                "peak_source": peak_src,
+                "kernel": ("clipped step (k_rs_norm, k_tree, k_clip_coef, k_adamw_ag)" if clipped
+                           else "k_fused" if variant == 0 else "staged trio"),
                 "algorithmic_bytes_per_launch": alg_bytes, "bytes_per_param": bpp}
 
     # -------- end to end through the host-buffer entry point
     e2e = None
-    if not args.no_e2e and variant == z.ZERO_VARIANT_FUSED:
+    if not args.no_e2e and variant == z.ZERO_VARIANT_FUSED and not clipped:
         host_g = [torch.empty(N, dtype=torch.bfloat16, pin_memory=True) for _ in ds.grads]
         for h, d in zip(host_g, ds.grads):
             h.copy_(d[:N])
@@ -368,7 +386,10 @@ def run_ours(args, rank, world, local_rank):
                "copy_engine_ms_per_step": ce_ms / k_e2e}
         del host_g, out
 
-    launches_per_step = 1 if variant == z.ZERO_VARIANT_FUSED else 3
+    if clipped:
+        launches_per_step = 2 + len(_tree_levels(N))   # rs_norm, tree levels, coef, update
+    else:
+        launches_per_step = 1 if variant == z.ZERO_VARIANT_FUSED else 3
     del ds
     torch.cuda.empty_cache()
 
@@ -386,6 +407,7 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded counter-based generator; shapes of the named parameter set)",
         "config": {"workload": wl.name, "N": N, "R": wl.R, "M": wl.M, "stage": wl.stage,
                    "step": wl.step, "variant": args.variant,
+                   **({"max_norm": args.max_norm} if clipped else {}),
                    "l2": "inputs (%.1f GB/step) far larger than the 129 MB L2; no flush"
                          % (alg_bytes / 1e9),
                    "parallelism": f"{world} independent replica(s) of an R={wl.R} "
@@ -518,7 +540,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama-3.2-1b")
-    ap.add_argument("--variant", choices=["fused", "staged"], default="fused")
+    ap.add_argument("--variant", choices=["fused", "staged", "clipped"], default="fused")
+    ap.add_argument("--max-norm", type=float, default=1.0,
+                    help="global-norm clip threshold for --variant clipped")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--table", action="store_true",

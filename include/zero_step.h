@@ -83,10 +83,12 @@ typedef enum {
 } zero_status;
 
 /* Bits OR-ed into the optional device status word. */
-#define ZERO_DEV_NONFINITE 1       /* an averaged gradient was Inf or NaN   */
+#define ZERO_DEV_NONFINITE 1       /* an averaged gradient (or the norm) was Inf or NaN */
+#define ZERO_DEV_SKIPPED 4         /* zero_step_clipped skipped the update      */
 
 /* Flags for zero_step / zero_rs_avg. */
 #define ZERO_FLAG_CHECK_FINITE 1   /* set ZERO_DEV_NONFINITE when g is non-finite */
+#define ZERO_FLAG_SKIP_NONFINITE 2 /* zero_step_clipped: skip the update on a non-finite norm */
 
 /* Variants for zero_step. */
 #define ZERO_VARIANT_FUSED 0       /* one pass: rs -> adamw -> ag per element  */
@@ -197,6 +199,34 @@ zero_status zero_adamw_shard(const zero_plan_t* plan, const float* g_shards, flo
  */
 zero_status zero_ag_cast(const zero_plan_t* plan, const float* master,
                          uint16_t* const* rank_params, void* stream);
+
+/*
+ * Step with global gradient-norm clipping (the training recipe "AdamW +
+ * gradient clipping", CS324 Lecture 9 notes, section 7.4; fp32 gradient
+ * reduction, LLM infra 06, section 15.3).  After the reduce-scatter and
+ * average, the squared global norm is the fp32 pairwise (binary-tree) sum of
+ * the squares g_i*g_i with the leaves padded by zeros to a power of two (one
+ * fixed order, identical for any grid); norm = sqrt(sumsq) and
+ * coef = max_norm / (norm + 1e-6) in double; when coef < 1 every averaged
+ * gradient is multiplied by (float)coef, then AdamW and the all-gather run as
+ * in zero_step.  A non-finite squared norm sets ZERO_DEV_NONFINITE in
+ * dev_status; with ZERO_FLAG_SKIP_NONFINITE the update is skipped (state and
+ * replicas untouched) and ZERO_DEV_SKIPPED is set.
+ *   max_norm   > 0 and finite.
+ *   scratch    device, at least zero_clip_scratch_bytes(plan) bytes: the
+ *              fp32 averaged gradients, the tree levels and a control record.
+ *   dev_sumsq  optional device double: receives the squared norm.
+ * Traffic: 2RM + 4 bytes/param (reduce-scatter, gradient stash) plus
+ * 4 + 24 + 2R (update and all-gather) plus 4/2048 for the tree.
+ */
+zero_status zero_step_clipped(const zero_plan_t* plan, const uint16_t* const* rank_grads,
+                              float* master, float* m, float* v, uint16_t* const* rank_params,
+                              const zero_adamw_hparams* hp, int64_t step, float max_norm,
+                              void* scratch, int64_t scratch_bytes, int32_t flags,
+                              int32_t* dev_status, double* dev_sumsq, void* stream);
+
+/* Scratch bytes zero_step_clipped needs for this plan (-1 for a bad plan). */
+int64_t zero_clip_scratch_bytes(const zero_plan_t* plan);
 
 /*
  * End-to-end step from host memory.  host_grads: R*M host pointers to the

@@ -69,6 +69,14 @@ class DeviceState:
                     variant=variant, scratch=self.scratch if variant else None, flags=flags,
                     dev_status=self.status)
 
+    def step_clipped(self, t, max_norm, flags=0, sumsq=None):
+        if getattr(self, "clip_scratch", None) is None:
+            self.clip_scratch = torch.empty(z.zero_clip_scratch_bytes(self.plan),
+                                            dtype=torch.uint8, device=self.dev)
+        z.zero_step_clipped(self.plan, self.grads, self.W, self.m, self.v, self.params, self.hp,
+                            t, max_norm, self.clip_scratch, flags=flags, dev_status=self.status,
+                            dev_sumsq=sumsq)
+
     def result(self):
         N = self.N
         return (self.W[:N].cpu().numpy().copy(), self.m[:N].cpu().numpy().copy(),

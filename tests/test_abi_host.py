@@ -215,3 +215,38 @@ def test_binding_rejects_host_tensors_for_device_arguments():
         z.zero_step(p, cpu, *st, cpu, z.hparams(), 1, stream=0)
     with pytest.raises(TypeError):
         z.zero_step(p, [t.float() for t in cpu], *st, cpu, z.hparams(), 1, stream=0)
+
+
+def test_clip_scratch_bytes_layout():
+    # fp32 gradient stash (4 * padded) + one 256-byte-rounded segment per tree
+    # level (ceil(N/2048) partials, then ceil(./2048) ... down to 1) + control
+    p = z.Plan([65536], 4, 2, 1)
+    assert z.zero_clip_scratch_bytes(p) == 4 * 65536 + 256 + 256 + 256
+    p = z.Plan([1_235_814_400], 8, 1, 2)             # 603,425 -> 295 -> 1 partials
+    levels = [603_425, 295, 1]
+    want = 4 * p.padded + sum(-(-4 * n // 256) * 256 for n in levels) + 256
+    assert z.zero_clip_scratch_bytes(p) == want
+
+
+def test_clipped_step_argument_errors():
+    import ctypes
+    plan = z.Plan([100_000], 4, 2, 2)
+    g, Wp, mp, vp, P, scr, st = fake_bufs(plan)
+    ga, pa = B._ptrs(g), B._ptrs(P)
+    hp = z.hparams()
+    need = z.zero_clip_scratch_bytes(plan)
+    L = B.lib()
+
+    def call(max_norm=1.0, scratch=scr, sbytes=need, flags=0, status=None, sumsq=None):
+        return L.zero_step_clipped(plan.ptr, ctypes.addressof(ga), Wp, mp, vp,
+                                   ctypes.addressof(pa), ctypes.byref(hp), 1, max_norm, scratch,
+                                   sbytes, flags, status, sumsq, None)
+    assert call(max_norm=0.0) == B.ZERO_ERR_INVALID_ARG
+    assert call(max_norm=float("inf")) == B.ZERO_ERR_INVALID_ARG
+    assert call(max_norm=float("nan")) == B.ZERO_ERR_INVALID_ARG
+    assert call(sbytes=need - 1) == B.ZERO_ERR_SIZE
+    assert call(scratch=None) == B.ZERO_ERR_NULL
+    assert call(scratch=Wp) == B.ZERO_ERR_OVERLAP
+    assert call(flags=8) == B.ZERO_ERR_INVALID_ARG
+    assert call(flags=B.ZERO_FLAG_CHECK_FINITE) == B.ZERO_ERR_NULL
+    assert call(sumsq=st + 4) == B.ZERO_ERR_ALIGN

@@ -25,7 +25,9 @@ ZERO_ERR_CUDA = -6
 ZERO_ERR_DEVICE_TIMEOUT = -7
 ZERO_ERR_NONFINITE = -8
 ZERO_DEV_NONFINITE = 1
+ZERO_DEV_SKIPPED = 4
 ZERO_FLAG_CHECK_FINITE = 1
+ZERO_FLAG_SKIP_NONFINITE = 2
 ZERO_VARIANT_FUSED = 0
 ZERO_VARIANT_STAGED = 1
 ZERO_MAX_R = 64
@@ -34,7 +36,8 @@ ZERO_NOALLOC_MAX_ELEMS = 4 * 1024 * 1024
 
 EXPORTED = ("zero_abi_version", "zero_status_string", "zero_plan_create", "zero_plan_destroy",
             "zero_plan_owner", "zero_step", "zero_rs_avg", "zero_adamw_shard", "zero_ag_cast",
-            "zero_step_host", "zero_step_staged_noalloc")
+            "zero_step_host", "zero_step_staged_noalloc", "zero_step_clipped",
+            "zero_clip_scratch_bytes")
 
 
 class ZeroError(RuntimeError):
@@ -96,6 +99,11 @@ def lib():
         L.zero_step_staged_noalloc.argtypes = [P(zero_plan_t), vp, vp, vp, vp, vp,
                                                P(zero_adamw_hparams), i64, i32, vp, vp]
         L.zero_step_staged_noalloc.restype = ctypes.c_int
+        L.zero_step_clipped.argtypes = [P(zero_plan_t), vp, vp, vp, vp, vp, P(zero_adamw_hparams),
+                                        i64, ctypes.c_float, vp, i64, i32, vp, vp, vp]
+        L.zero_step_clipped.restype = ctypes.c_int
+        L.zero_clip_scratch_bytes.argtypes = [P(zero_plan_t)]
+        L.zero_clip_scratch_bytes.restype = i64
         _lib = L
     return _lib
 
@@ -330,3 +338,32 @@ def zero_step_staged_noalloc(plan: Plan, rank_grads, master, m, v, rank_params,
                                           _addr(m), _addr(v), ctypes.addressof(pa),
                                           ctypes.byref(hp), step, flags, _addr(dev_status),
                                           _stream(stream)), "zero_step_staged_noalloc")
+
+
+def zero_clip_scratch_bytes(plan: Plan) -> int:
+    return int(lib().zero_clip_scratch_bytes(plan.ptr))
+
+
+def zero_step_clipped(plan: Plan, rank_grads, master, m, v, rank_params, hp: zero_adamw_hparams,
+                      step: int, max_norm: float, scratch, flags: int = 0, dev_status=None,
+                      dev_sumsq=None, stream=None) -> None:
+    """Step with global gradient-norm clipping; scratch holds at least
+    zero_clip_scratch_bytes(plan) bytes; dev_sumsq (optional, float64
+    device tensor of 1) receives the squared norm."""
+    c = plan.c
+    for k, g in enumerate(rank_grads):
+        _check_tensor(g, "bf16", c.N, f"rank_grads[{k}]")
+    for k, p in enumerate(rank_params):
+        _check_tensor(p, "bf16", c.N, f"rank_params[{k}]")
+    for nm, t in (("master", master), ("m", m), ("v", v)):
+        _check_tensor(t, "f32", c.padded, nm)
+    _check_tensor(dev_status, "i32", 1, "dev_status")
+    if len(rank_grads) != c.R * c.M or len(rank_params) != c.R:
+        raise ValueError(f"need {c.R * c.M} gradient buffers and {c.R} replicas")
+    sbytes = scratch.numel() * scratch.element_size() if not isinstance(scratch, int) else \
+        zero_clip_scratch_bytes(plan)
+    ga, pa = _ptrs([_addr(g) for g in rank_grads]), _ptrs([_addr(p) for p in rank_params])
+    _check(lib().zero_step_clipped(plan.ptr, ctypes.addressof(ga), _addr(master), _addr(m),
+                                   _addr(v), ctypes.addressof(pa), ctypes.byref(hp), step,
+                                   max_norm, _addr(scratch), sbytes, flags, _addr(dev_status),
+                                   _addr(dev_sumsq), _stream(stream)), "zero_step_clipped")
