@@ -113,6 +113,12 @@ def lib():
                                                  i32, ctypes.POINTER(ctypes.c_double),
                                                  ctypes.POINTER(ctypes.c_int32)]
             L.oracle_dp_step_clipped.restype = ctypes.c_int
+            L.oracle_zero3_step.argtypes = [i64, i32, i32, i64, vp, vp, vp, vp, vp,
+                                            ctypes.POINTER(HParams), i64, vp]
+            L.oracle_zero3_step.restype = ctypes.c_int
+            L.oracle_zero3_gather.argtypes = [i64, i32, i64, vp, i64, i64, i32, vp,
+                                              ctypes.POINTER(ctypes.c_int64)]
+            L.oracle_zero3_gather.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -274,3 +280,33 @@ def dp_step_clipped(G, W, m, v, P, hp: HParams, step: int, R: int, M: int,
     if rc != 0:
         raise RuntimeError(f"oracle_dp_step_clipped failed: {rc}")
     return ss.value, bool(sk.value)
+
+
+def zero3_step(G, W, m, v, Pshard, hp: HParams, step: int, R: int, M: int, n: int, S: int):
+    """ZeRO-3 step card by card, in place; returns the per-card count of
+    gradient numbers received from other cards."""
+    for k, g in enumerate(G):
+        _check(g, np.uint16, n, f"G[{k}]")
+    for nm, a in (("W", W), ("m", m), ("v", v)):
+        _check(a, np.float32, R * S, nm)
+    _check(Pshard, np.uint16, R * S, "Pshard")
+    ga = _ptr_array(G)
+    recv = np.zeros(R, np.int64)
+    rc = lib().oracle_zero3_step(n, R, M, S, ctypes.addressof(ga), _ptr(W), _ptr(m), _ptr(v),
+                                 _ptr(Pshard), ctypes.byref(hp), step, _ptr(recv))
+    if rc != 0:
+        raise RuntimeError(f"oracle_zero3_step failed: {rc}")
+    return recv
+
+
+def zero3_gather(Pshard, n: int, R: int, S: int, lo: int, hi: int, card: int = 0):
+    """All-gather of unit [lo, hi) for `card`; returns (values, numbers
+    received from other cards)."""
+    _check(Pshard, np.uint16, R * S, "Pshard")
+    out = np.zeros(max(1, hi - lo), np.uint16)
+    recv = ctypes.c_int64(0)
+    rc = lib().oracle_zero3_gather(n, R, S, _ptr(Pshard), lo, hi, card, _ptr(out),
+                                   ctypes.byref(recv))
+    if rc != 0:
+        raise RuntimeError(f"oracle_zero3_gather failed: {rc}")
+    return out[:hi - lo], recv.value

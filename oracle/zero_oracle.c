@@ -425,3 +425,64 @@ int oracle_dp_step_clipped(int64_t n, int32_t R, int32_t M,
     free(g);
     return 0;
 }
+
+/* --------------------------------------------------------------- ZeRO-3 -- */
+
+int oracle_zero3_step(int64_t n, int32_t R, int32_t M, int64_t S,
+                      const uint16_t* const* G, float* W, float* m, float* v,
+                      uint16_t* Pshard, const oracle_hparams* hp, int64_t step,
+                      int64_t* recv)
+{
+    if (check_args(n, R, M, G, W, m, v, (const void*)Pshard, hp, step)) return -1;
+    if (S < 0 || S * R < n) return -1;
+    oracle_scalars s;
+    oracle_make_scalars(hp, step, R, M, &s);
+    int32_t RM = R * M;
+    int rc = 0;
+    for (int32_t r = 0; r < R && rc == 0; ++r) {        /* card r */
+        int64_t lo = (int64_t)r * S;
+        int64_t len = n - lo < S ? n - lo : S;
+        if (recv) recv[r] = 0;
+        if (len <= 0) continue;
+        /* reduce-scatter: card r receives chunk r of every rank's gradients
+         * (its own M micro-batches stay local) */
+        uint16_t* buf = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)RM * (size_t)len);
+        const uint16_t** ptr = (const uint16_t**)malloc(sizeof(void*) * (size_t)RM);
+        if (!buf || !ptr) {
+            rc = -2;
+        } else {
+            for (int32_t k = 0; k < RM; ++k) {
+                memcpy(buf + (int64_t)k * len, G[k] + lo, sizeof(uint16_t) * (size_t)len);
+                ptr[k] = buf + (int64_t)k * len;
+                /* traffic: one number per other rank and element (a rank sums
+                 * its micro-batches locally before the reduce-scatter) */
+                if (recv && k % M == 0 && k / M != r) recv[r] += len;
+            }
+            /* shard update, then the cast into the card's own parameter shard */
+            for (int64_t k = 0; k < len; ++k) {
+                float g = oracle_avg_grad((const uint16_t* const*)ptr, R, M, k, s.denom_rm);
+                oracle_adamw_elem(&s, g, &W[lo + k], &m[lo + k], &v[lo + k]);
+                Pshard[lo + k] = oracle_bf16_rne(W[lo + k]);
+            }
+        }
+        free(buf);
+        free(ptr);
+    }
+    return rc;
+}
+
+int oracle_zero3_gather(int64_t n, int32_t R, int64_t S, const uint16_t* Pshard,
+                        int64_t lo, int64_t hi, int32_t card, uint16_t* out,
+                        int64_t* recv)
+{
+    if (n < 0 || R < 1 || S < 0 || S * R < n || !Pshard || !out) return -1;
+    if (lo < 0 || hi < lo || hi > n || card < 0 || card >= R) return -1;
+    int64_t from_others = 0;
+    for (int64_t i = lo; i < hi; ++i) {
+        int32_t owner = (int32_t)(i / S);
+        out[i - lo] = Pshard[i];          /* the owner's shard holds element i */
+        if (owner != card) ++from_others;
+    }
+    if (recv) *recv = from_others;
+    return 0;
+}

@@ -199,6 +199,36 @@ int oracle_dp_step_clipped(int64_t n, int32_t R, int32_t M,
                            int64_t step, float max_norm, int32_t skip_nonfinite,
                            double* sumsq_out, int32_t* skipped_out);
 
+/* ------------------------------------------------------------------------
+ * ZeRO-3 (CS25 V6 Lecture 4 notes, "ZeRO-3 / FSDP": parameters are sharded
+ * too and materialised per unit just before use; CS324 Lecture 9 notes,
+ * section 3.4 and exercise 7: bit-identical to DP, per-card traffic
+ * 3(p-1)/p Psi against 2(p-1)/p for DP / ZeRO-1 / ZeRO-2).
+ * Reading R13: each card keeps its bf16 parameter shard in the same padded
+ * layout as the fp32 state (R*S elements, shard r at r*S); the step is the
+ * ZeRO-2 reduce-scatter and shard update followed by a cast into the
+ * card's own shard, with no all-gather; a unit [lo, hi) of the flat vector
+ * is all-gathered on demand into a card's transient buffer.
+ * ---------------------------------------------------------------------- */
+
+/* ZeRO-3 step emulated card by card.  Pshard holds R*S bf16 (shard r at
+ * r*S).  recv (may be NULL, R entries) receives, per card, the count of
+ * gradient numbers it got from other cards in the reduce-scatter: one per
+ * other rank and element, since a rank sums its micro-batches before the
+ * reduce-scatter.
+ * Returns 0, -1 on a bad argument, -2 on allocation failure. */
+int oracle_zero3_step(int64_t n, int32_t R, int32_t M, int64_t S,
+                      const uint16_t* const* G, float* W, float* m, float* v,
+                      uint16_t* Pshard, const oracle_hparams* hp, int64_t step,
+                      int64_t* recv);
+
+/* All-gather of the unit [lo, hi) for card `card`: out[i - lo] is copied
+ * from the shard of owner(i).  *recv (may be NULL) receives the count of
+ * numbers that came from other cards.  Returns 0 or -1. */
+int oracle_zero3_gather(int64_t n, int32_t R, int64_t S, const uint16_t* Pshard,
+                        int64_t lo, int64_t hi, int32_t card, uint16_t* out,
+                        int64_t* recv);
+
 #ifdef __cplusplus
 }
 #endif

@@ -54,6 +54,11 @@ MUTANTS = {
     "clip_divides": ("float gi = clip ? g[i] * coef : g[i];", "float gi = clip ? g[i] / coef : g[i];"),
     "skip_ignores_flag": ("if (!isfinite(sumsq) && skip_nonfinite) skipped = 1;",
                           "if (!isfinite(sumsq) || skip_nonfinite < 0) skipped = 1;"),
+    "zero3_owner_off_by_one": ("int32_t owner = (int32_t)(i / S);", "int32_t owner = (int32_t)((i + 1) / S);"),
+    "zero3_counts_every_microbatch": ("if (recv && k % M == 0 && k / M != r) recv[r] += len;",
+                                      "if (recv && k / M != r) recv[r] += len;"),
+    "zero3_shard_cast_truncates": ("Pshard[lo + k] = oracle_bf16_rne(W[lo + k]);",
+                                   "Pshard[lo + k] = (uint16_t)(((union { float f; uint32_t u; }){W[lo + k]}).u >> 16);"),
 }
 
 
@@ -71,6 +76,6 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     env = dict(os.environ, ZERO_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         "tests/test_oracle_pins.py", "tests/test_oracle_collectives.py",
-                        "tests/test_oracle_clip.py"],
+                        "tests/test_oracle_clip.py", "tests/test_oracle_zero3.py"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
