@@ -480,6 +480,65 @@ def run_table(args):
 
     for name in ("tiny", "gpt2-small", "llama-3.2-1b", "uneven", "large"):
         measure(W.ALL[name](), name, reps=20 if name != "large" else 10)
+    # ZeRO-3: the step (cast into each rank's own shard) and the per-unit
+    # all-gather of the whole 1B-shaped model at three unit sizes
+    for name in ("gpt2-small", "llama-3.2-1b", "large"):
+        wl = W.ALL[name]()
+        ds = H.DeviceState(wl, staged_scratch=False)
+        ds.fill_state_device()
+        ds.fill_grads_device(wl.step)
+        shards = torch.empty(ds.padded, dtype=torch.bfloat16, device="cuda")
+        ts, t = [], wl.step
+        for k in range(3 + 10):
+            flush.fill_(k & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            z.zero3_step(ds.plan, ds.grads, ds.W, ds.m, ds.v, shards, ds.hp, t)
+            e1.record()
+            torch.cuda.synchronize()
+            t += 1
+            if k >= 3:
+                ts.append(e0.elapsed_time(e1))
+        ms = float(np.median(ts))
+        b = 2 * wl.R * wl.M + 26
+        row = {"workload": name, "R": wl.R, "M": wl.M, "N": wl.N, "variant": "zero3_step",
+               "ms": round(ms, 4), "params_per_s": wl.N / (ms / 1e3), "bytes_per_param": b,
+               "GB_s": round(b * wl.N / (ms / 1e3) / 1e9, 1),
+               "frac_of_measured_peak": round(b * wl.N / (ms / 1e3) / 1e9 / peak, 4),
+               "l2_resident": False}
+        rows.append(row)
+        print(json.dumps(row), flush=True)
+        if name == "llama-3.2-1b":
+            offs = [int(x) for x in wl.offsets]
+            layers = [0, offs[1]] + [offs[1 + 9 * (l + 1)] for l in range(16)] + [offs[-1]]
+            layers = sorted(set(layers))
+            full = torch.empty(wl.N, dtype=torch.bfloat16, device="cuda")
+            for label, cuts in (("unit = tensor (146 units)", offs),
+                                ("unit = layer (18 units)", layers),
+                                ("unit = whole model (1 unit)", [0, wl.N])):
+                ts = []
+                for k in range(3 + 10):
+                    flush.fill_(k & 0xFF)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    for lo, hi in zip(cuts[:-1], cuts[1:]):
+                        z.zero3_gather(ds.plan, shards, lo, hi, [full[:hi - lo]])
+                    e1.record()
+                    torch.cuda.synchronize()
+                    if k >= 3:
+                        ts.append(e0.elapsed_time(e1))
+                ms = float(np.median(ts))
+                row = {"workload": name, "variant": "zero3_gather", "unit": label,
+                       "launches": len(cuts) - 1, "ms": round(ms, 4),
+                       "GB_s": round(4 * wl.N / (ms / 1e3) / 1e9, 1),
+                       "frac_of_measured_peak": round(4 * wl.N / (ms / 1e3) / 1e9 / peak, 4)}
+                rows.append(row)
+                print(json.dumps(row), flush=True)
+            del full
+        del ds, shards
+        torch.cuda.empty_cache()
+
     for R in (2, 4, 8):
         S = 1024
         while S <= 256 * 1024 * 1024:

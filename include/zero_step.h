@@ -229,6 +229,35 @@ zero_status zero_step_clipped(const zero_plan_t* plan, const uint16_t* const* ra
 int64_t zero_clip_scratch_bytes(const zero_plan_t* plan);
 
 /*
+ * ZeRO-3 step (CS25 V6 Lecture 4 notes, "ZeRO-3 / FSDP": the parameters are
+ * sharded as well and materialised per unit just before use; CS324 Lecture
+ * 9 notes, section 3.4: bit-identical to plain DP).  The reduce-scatter,
+ * average and AdamW of zero_step, then each rank casts its updated shard to
+ * bf16 into its own parameter shard; there is no all-gather in the step.
+ *   param_shards  device, plan->padded bf16 in the padded layout of the
+ *                 state (shard r at r*S, element i at index i); the pad is
+ *                 never written.
+ * Traffic: 2RM + 24 + 2 bytes/param.  Other arguments as zero_step.
+ */
+zero_status zero3_step(const zero_plan_t* plan, const uint16_t* const* rank_grads,
+                       float* master, float* m, float* v, uint16_t* param_shards,
+                       const zero_adamw_hparams* hp, int64_t step, int32_t flags,
+                       int32_t* dev_status, void* stream);
+
+/*
+ * ZeRO-3 all-gather of one unit (a layer, or any range of the flat vector)
+ * before its use: outs[o][i - lo] = param_shards[i] for i in [lo, hi), where
+ * element i comes from the shard of rank i / S, for each of the n_out
+ * transient buffers (the ranks that materialise the unit, 1 <= n_out <= R).
+ *   0 <= lo <= hi <= N; lo may be any element (units start at arbitrary
+ *   tensor offsets).  outs: host array of n_out device pointers, each
+ *   (hi - lo) bf16, 16-byte aligned, not overlapping each other or the
+ *   shards.  Traffic: 2 + 2 n_out bytes per element.
+ */
+zero_status zero3_gather(const zero_plan_t* plan, const uint16_t* param_shards, int64_t lo,
+                         int64_t hi, uint16_t* const* outs, int32_t n_out, void* stream);
+
+/*
  * End-to-end step from host memory.  host_grads: R*M host pointers to the
  * gradient buffers (N bf16 each); host_params_out: host, N bf16, receives
  * replica 0 (every replica holds the same bits).  Two modes:

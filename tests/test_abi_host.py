@@ -26,7 +26,7 @@ def built():
 def declared_symbols():
     src = open(os.path.join(ROOT, "include", "zero_step.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(zero_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(zero[0-9]*_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_every_declared_symbol_is_exported():

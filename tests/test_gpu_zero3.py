@@ -1,0 +1,134 @@
+"""GPU parity of the ZeRO-3 step and the per-unit all-gather.
+
+zero3_step and zero3_gather through the C ABI against oracle.zero3_step and
+oracle.zero3_gather: shard buffer and fp32 state bit for bit, pad and guard
+bands untouched, every unit misalignment (lo mod 8), units at the very end
+of an unpadded buffer, 1..R destinations; at full size (Llama-3.2-1B-shaped)
+on sampled elements, and the gathered model equals the shards everywhere.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import zero_optimizer_step_rs_gb300 as z
+from tests import harness as H
+from zgen import workloads as W
+
+pytestmark = pytest.mark.gpu
+CANARY = 0x5A5A
+
+
+def _zero3_run(wl, steps):
+    _, W0, m0, v0 = H.host_inputs(wl, steps[0])
+    idx = np.arange(wl.N, dtype=np.int64)
+    plan = z.Plan(wl.numels, wl.R, wl.M, wl.stage, wl.align)
+    S, N, padded = plan.S, plan.N, plan.padded
+    # oracle, card by card
+    Wz = np.zeros(padded, np.float32)
+    mz, vz = Wz.copy(), Wz.copy()
+    Wz[:N], mz[:N], vz[:N] = W0, m0, v0
+    Ps = np.full(padded, CANARY, np.uint16)
+    hp = oracle.hparams(**wl.hparams())
+    # GPU
+    ds = H.DeviceState(wl, staged_scratch=False)
+    ds.upload_state(W0, m0, v0)
+    shards = torch.full((padded,), CANARY, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    for t in steps:
+        G = W.host_grads_at(wl, t, idx)
+        oracle.zero3_step(G, Wz, mz, vz, Ps, hp, t, wl.R, wl.M, N, S)
+        ds.upload_grads(G)
+        z.zero3_step(ds.plan, ds.grads, ds.W, ds.m, ds.v, shards, ds.hp, t,
+                     flags=z.ZERO_FLAG_CHECK_FINITE, dev_status=ds.status)
+    torch.cuda.synchronize()
+    return plan, ds, shards, (Wz, mz, vz, Ps)
+
+
+@pytest.mark.parametrize("name,target", [("uneven", 200_000), ("llama-3.2-1b", 300_000),
+                                         ("gpt2-small", 150_000)])
+def test_zero3_step_matches_oracle(name, target):
+    import dataclasses
+    wl = W.ALL[name]().scaled(target)
+    if wl.state == "prior":
+        wl = dataclasses.replace(wl, step=3, prior_steps=2)
+    plan, ds, shards, (Wz, mz, vz, Ps) = _zero3_run(wl, list(range(wl.first_step(), wl.step + 1)))
+    got_s = H.u16_from_bf16(shards)
+    assert np.array_equal(got_s, Ps)                       # includes the untouched pad
+    for t, a in ((ds.W, Wz), (ds.m, mz), (ds.v, vz)):
+        assert np.array_equal(t.cpu().numpy().view(np.uint32)[:plan.N],
+                              a.view(np.uint32)[:plan.N])
+    assert int(ds.status.item()) == 0
+
+
+@pytest.mark.parametrize("n,R", [(1, 2), (7, 4), (2049, 3), (4096 * 8, 8), (100_003, 7)])
+def test_zero3_step_ragged(n, R):
+    wl = W.flat(R, 1, n, seed=n, step=2)
+    plan, ds, shards, (Wz, mz, vz, Ps) = _zero3_run(wl, [2])
+    assert np.array_equal(H.u16_from_bf16(shards), Ps)
+
+
+def _gather_case(plan, shards_np, shards, lo, hi, n_out):
+    L = hi - lo
+    G = 64                                                 # guard elements (128 B)
+    bufs = [torch.full((L + 2 * G + 8,), -7, dtype=torch.int16, device="cuda")
+            for _ in range(n_out)]
+    outs = [b[G:G + L].view(torch.bfloat16) for b in bufs]
+    z.zero3_gather(plan, shards, lo, hi, outs)
+    torch.cuda.synchronize()
+    for card, (b, o) in enumerate(zip(bufs, outs)):
+        want, _ = oracle.zero3_gather(shards_np, plan.N, plan.R, plan.S, lo, hi, card % plan.R)
+        assert np.array_equal(H.u16_from_bf16(o), want), (lo, hi)
+        assert torch.all(b[:G] == -7) and torch.all(b[G + L:] == -7), (lo, hi)
+
+
+def test_gather_every_alignment_and_length():
+    N, R = 8 * 4096, 8                                     # no padding: the last shard ends the buffer
+    plan = z.Plan([N], R, 1, 2, 64)
+    assert plan.padded == N
+    rng = np.random.default_rng(0)
+    shards_np = rng.integers(0, 2 ** 16, N, dtype=np.uint16)
+    shards = torch.from_numpy(shards_np.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    cases = []
+    for lo in list(range(0, 24)) + [N - 40 + k for k in range(8)]:
+        for L in (0, 1, 3, 7, 8, 9, 15, 16, 17, 31, 33):
+            if lo + L <= N:
+                cases.append((lo, lo + L))
+    for s in range(8):                                     # units that end exactly at N
+        cases.append((N - 1000 - s, N))
+        cases.append((s, N))
+    cases += [(4096 * 3 - 5, 4096 * 5 + 3)]               # crosses two shard boundaries
+    for k, (lo, hi) in enumerate(cases):
+        _gather_case(plan, shards_np, shards, lo, hi, n_out=1 + k % R)
+
+
+def test_full_size_zero3_llama():
+    wl = W.llama32_1b()
+    ds = H.DeviceState(wl, staged_scratch=False)
+    ds.fill_state_device()
+    ds.fill_grads_device(wl.step)
+    shards = torch.empty(ds.padded, dtype=torch.bfloat16, device="cuda")
+    z.zero3_step(ds.plan, ds.grads, ds.W, ds.m, ds.v, shards, ds.hp, wl.step,
+                 flags=z.ZERO_FLAG_CHECK_FINITE, dev_status=ds.status)
+    # gather every tensor as its own unit; each must equal its slice of the shards
+    offs = wl.offsets
+    for lo, hi in zip(offs[:-1], offs[1:]):
+        lo, hi = int(lo), int(hi)
+        unit = torch.empty(hi - lo, dtype=torch.bfloat16, device="cuda")
+        z.zero3_gather(ds.plan, shards, lo, hi, [unit])
+        assert torch.equal(unit.view(torch.int16), shards[lo:hi].view(torch.int16)), (lo, hi)
+    full = torch.empty(ds.N, dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(2)
+    pick = np.unique(np.concatenate([rng.integers(0, ds.N, 20_000), np.arange(ds.N - 3000, ds.N)]))
+    it = torch.from_numpy(pick).cuda()
+    W0 = W.host_w0_at(wl, pick)
+    m0, v0 = W.host_mv0_at(wl, pick)
+    want = H.oracle_run(wl, {wl.step: W.host_grads_at(wl, wl.step, pick)}, W0, m0, v0, [wl.step])
+    got_s = H.u16_from_bf16(shards[it])
+    assert np.array_equal(got_s, want[3][0])
+    assert np.array_equal(ds.W[it].cpu().numpy().view(np.uint32), want[0].view(np.uint32))
+    assert int(ds.status.item()) == 0
+    # the whole model gathered in one unit equals the shards, element for element
+    z.zero3_gather(ds.plan, shards, 0, ds.N, [full])
+    torch.cuda.synchronize()
+    assert torch.equal(full.view(torch.int16), shards[:ds.N].view(torch.int16))

@@ -37,7 +37,7 @@ ZERO_NOALLOC_MAX_ELEMS = 4 * 1024 * 1024
 EXPORTED = ("zero_abi_version", "zero_status_string", "zero_plan_create", "zero_plan_destroy",
             "zero_plan_owner", "zero_step", "zero_rs_avg", "zero_adamw_shard", "zero_ag_cast",
             "zero_step_host", "zero_step_staged_noalloc", "zero_step_clipped",
-            "zero_clip_scratch_bytes")
+            "zero_clip_scratch_bytes", "zero3_step", "zero3_gather")
 
 
 class ZeroError(RuntimeError):
@@ -104,6 +104,11 @@ def lib():
         L.zero_step_clipped.restype = ctypes.c_int
         L.zero_clip_scratch_bytes.argtypes = [P(zero_plan_t)]
         L.zero_clip_scratch_bytes.restype = i64
+        L.zero3_step.argtypes = [P(zero_plan_t), vp, vp, vp, vp, vp, P(zero_adamw_hparams), i64,
+                                 i32, vp, vp]
+        L.zero3_step.restype = ctypes.c_int
+        L.zero3_gather.argtypes = [P(zero_plan_t), vp, i64, i64, vp, i32, vp]
+        L.zero3_gather.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -367,3 +372,33 @@ def zero_step_clipped(plan: Plan, rank_grads, master, m, v, rank_params, hp: zer
                                    _addr(v), ctypes.addressof(pa), ctypes.byref(hp), step,
                                    max_norm, _addr(scratch), sbytes, flags, _addr(dev_status),
                                    _addr(dev_sumsq), _stream(stream)), "zero_step_clipped")
+
+
+def zero3_step(plan: Plan, rank_grads, master, m, v, param_shards, hp: zero_adamw_hparams,
+               step: int, flags: int = 0, dev_status=None, stream=None) -> None:
+    """ZeRO-3 step: reduce-scatter, AdamW, cast into each rank's own shard of
+    param_shards (plan.padded bf16, padded layout); no all-gather."""
+    c = plan.c
+    for k, g in enumerate(rank_grads):
+        _check_tensor(g, "bf16", c.N, f"rank_grads[{k}]")
+    for nm, t in (("master", master), ("m", m), ("v", v)):
+        _check_tensor(t, "f32", c.padded, nm)
+    _check_tensor(param_shards, "bf16", c.padded, "param_shards")
+    _check_tensor(dev_status, "i32", 1, "dev_status")
+    if len(rank_grads) != c.R * c.M:
+        raise ValueError(f"need {c.R * c.M} gradient buffers")
+    ga = _ptrs([_addr(g) for g in rank_grads])
+    _check(lib().zero3_step(plan.ptr, ctypes.addressof(ga), _addr(master), _addr(m), _addr(v),
+                            _addr(param_shards), ctypes.byref(hp), step, flags,
+                            _addr(dev_status), _stream(stream)), "zero3_step")
+
+
+def zero3_gather(plan: Plan, param_shards, lo: int, hi: int, outs, stream=None) -> None:
+    """All-gather of unit [lo, hi) into each of the transient buffers in outs."""
+    c = plan.c
+    _check_tensor(param_shards, "bf16", c.padded, "param_shards")
+    for k, o in enumerate(outs):
+        _check_tensor(o, "bf16", hi - lo, f"outs[{k}]")
+    oa = _ptrs([_addr(o) for o in outs])
+    _check(lib().zero3_gather(plan.ptr, _addr(param_shards), lo, hi, ctypes.addressof(oa),
+                              len(outs), _stream(stream)), "zero3_gather")

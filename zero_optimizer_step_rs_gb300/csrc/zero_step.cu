@@ -94,6 +94,7 @@ struct FusedArgs {
     StepScalars s;
     int32_t* status;
     uint16_t* extra_rep;  // optional extra copy of the replica (e.g. in host memory)
+    int32_t zero3;        // host-side dispatch: write one sharded buffer (P.p[0])
 };
 
 struct StagedArgs {
@@ -239,10 +240,14 @@ __device__ __forceinline__ void report_nonfinite(bool bad, int32_t* status)
 
 // ---------------------------------------------------------- fused step --
 
-// XREP: also write the replica bits to a.extra_rep (the host-buffer entry
-// point's zero-copy mode); a template switch so the plain path carries no
-// extra branch or register pressure.
-template <int RC, int MC, int U, bool CHECK, bool XREP>
+// OUT selects where the bf16 result goes, as a template switch so the plain
+// path carries no extra branch or register pressure:
+//   0  the R replicas a.P.p[0..R)                       (ZeRO-1/2 all-gather)
+//   1  the R replicas and a.extra_rep (the host-buffer entry point's
+//      zero-copy mode writes replica 0 to host memory as well)
+//   2  one buffer a.P.p[0] in the padded layout of the state: each rank
+//      casts into its own parameter shard, no all-gather   (ZeRO-3)
+template <int RC, int MC, int U, bool CHECK, int OUT>
 __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ FusedArgs a)
 {
     const int R = RC > 0 ? RC : a.R;
@@ -280,13 +285,15 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ Fuse
             st_stream(a.m + e, mm[u]);
             st_stream(a.v + e, vv[u]);
             const uint2 p = make_uint2(pack_bf16x2(w[u].x, w[u].y), pack_bf16x2(w[u].z, w[u].w));
-            if constexpr (RC > 0) {
+            if constexpr (OUT == 2) {
+                st_stream(a.P.p[0] + e, p);
+            } else if constexpr (RC > 0) {
 #pragma unroll
                 for (int r = 0; r < RC; ++r) st_stream(a.P.p[r] + e, p);
             } else {
                 for (int r = 0; r < R; ++r) st_stream(a.P.p[r] + e, p);
             }
-            if constexpr (XREP) st_stream(a.extra_rep + e, p);
+            if constexpr (OUT == 1) st_stream(a.extra_rep + e, p);
         }
     }
 
@@ -302,8 +309,12 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ Fuse
             a.m[i] = m;
             a.v[i] = v;
             const uint16_t p = to_bf16(w);
-            for (int r = 0; r < R; ++r) a.P.p[r][i] = p;
-            if constexpr (XREP) a.extra_rep[i] = p;
+            if constexpr (OUT == 2) {
+                a.P.p[0][i] = p;
+            } else {
+                for (int r = 0; r < R; ++r) a.P.p[r][i] = p;
+            }
+            if constexpr (OUT == 1) a.extra_rep[i] = p;
         }
     }
     report_nonfinite<CHECK>(bad, a.status);
@@ -452,14 +463,26 @@ unsigned grid_for(const void* kernel, int64_t work_blocks)
 
 // ----------------------------------------------------- fused dispatch --
 
-template <int RC, int MC, bool CHECK, bool XREP = false>
+template <int RC, int MC, bool CHECK, int OUT = 0>
 cudaError_t launch_fused_t(const FusedArgs& a, cudaStream_t st)
 {
     constexpr int U = 2;
-    const void* k = reinterpret_cast<const void*>(&k_fused<RC, MC, U, CHECK, XREP>);
+    const void* k = reinterpret_cast<const void*>(&k_fused<RC, MC, U, CHECK, OUT>);
     const int64_t tiles = (a.n + kUnit * U - 1) / (kUnit * U);
-    k_fused<RC, MC, U, CHECK, XREP><<<grid_for(k, tiles), kThreads, 0, st>>>(a);
+    k_fused<RC, MC, U, CHECK, OUT><<<grid_for(k, tiles), kThreads, 0, st>>>(a);
     return cudaGetLastError();
+}
+
+template <bool CHECK, int OUT>
+cudaError_t launch_fused_table(const FusedArgs& a, cudaStream_t st)
+{
+    const int R = a.R, M = a.M;
+#define ZERO_CASE(r_, m_) \
+    if (R == r_ && M == m_) return launch_fused_t<r_, m_, CHECK, OUT>(a, st);
+    ZERO_CASE(8, 1) ZERO_CASE(4, 1) ZERO_CASE(2, 1) ZERO_CASE(1, 1) ZERO_CASE(16, 1)
+    ZERO_CASE(4, 2) ZERO_CASE(7, 4) ZERO_CASE(8, 2) ZERO_CASE(4, 4) ZERO_CASE(2, 2)
+#undef ZERO_CASE
+    return launch_fused_t<0, 0, CHECK, OUT>(a, st);
 }
 
 template <bool CHECK>
@@ -467,14 +490,9 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st)
 {
     // the zero-copy host path is bound by the host link, not by HBM: one
     // run-time (R, M) instantiation serves it
-    if (a.extra_rep) return launch_fused_t<0, 0, CHECK, true>(a, st);
-    const int R = a.R, M = a.M;
-#define ZERO_CASE(r_, m_) \
-    if (R == r_ && M == m_) return launch_fused_t<r_, m_, CHECK>(a, st);
-    ZERO_CASE(8, 1) ZERO_CASE(4, 1) ZERO_CASE(2, 1) ZERO_CASE(1, 1) ZERO_CASE(16, 1)
-    ZERO_CASE(4, 2) ZERO_CASE(7, 4) ZERO_CASE(8, 2) ZERO_CASE(4, 4) ZERO_CASE(2, 2)
-#undef ZERO_CASE
-    return launch_fused_t<0, 0, CHECK>(a, st);
+    if (a.extra_rep) return launch_fused_t<0, 0, CHECK, 1>(a, st);
+    if (a.zero3) return launch_fused_table<CHECK, 2>(a, st);
+    return launch_fused_table<CHECK, 0>(a, st);
 }
 
 template <bool CHECK>
@@ -1211,6 +1229,171 @@ extern "C" zero_status zero_step_clipped(const zero_plan_t* plan,
     }
     if (err == cudaSuccess) err = launch_adamw_ag(a, st);
     return cuda_status(err);
+}
+
+// ================================================================ ZeRO-3 ==
+// zero3_step: the fused reduce-scatter + AdamW with the bf16 result cast
+// into each rank's own parameter shard (one buffer in the padded layout of
+// the state); no all-gather.  zero3_gather: the all-gather of one unit
+// [lo, hi) of the flat vector from the shards into n_out transient buffers
+// (the ranks that need the unit), on demand before its use.
+//
+// k_gather copies 8 elements (16 bytes) per thread to every destination.
+// A unit can start at any element, so the source window of a destination
+// vector is shifted by SHIFT = lo mod 8 elements: the thread loads the two
+// aligned 16-byte source vectors that cover it and funnel-shifts them into
+// place (SHIFT is a template parameter: 8 instantiations).  Vectors whose
+// source window would cross the end of the shard buffer, and the last
+// partial vector, are copied element by element.
+namespace {
+
+struct GatherArgs {
+    ReplicaPtrs out;
+    const uint16_t* src;
+    int64_t src_len;       // elements in the shard buffer (plan->padded)
+    int64_t lo, len;
+    int32_t n_out;
+};
+
+template <int SHIFT>
+__device__ __forceinline__ uint4 realign8(uint4 A, uint4 B)
+{
+    const uint32_t w[8] = {A.x, A.y, A.z, A.w, B.x, B.y, B.z, B.w};
+    constexpr int h = SHIFT / 2;
+    uint4 r;
+    if constexpr (SHIFT % 2 == 0) {
+        r.x = w[h];
+        r.y = w[h + 1];
+        r.z = w[h + 2];
+        r.w = w[h + 3];
+    } else {
+        r.x = __funnelshift_r(w[h], w[h + 1], 16);
+        r.y = __funnelshift_r(w[h + 1], w[h + 2], 16);
+        r.z = __funnelshift_r(w[h + 2], w[h + 3], 16);
+        r.w = __funnelshift_r(w[h + 3], w[h + 4], 16);
+    }
+    return r;
+}
+
+template <int SHIFT>
+__global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ GatherArgs a)
+{
+    const int64_t base = a.lo - SHIFT;            // 8-element (16-byte) aligned
+    const int64_t nvec = a.len / 8;
+    constexpr int64_t window = SHIFT ? 16 : 8;
+    for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < nvec;
+         k += (int64_t)gridDim.x * kThreads) {
+        const int64_t sb = base + 8 * k;
+        uint4 v;
+        if (sb + window <= a.src_len) {
+            const uint4 A = __ldcs(reinterpret_cast<const uint4*>(a.src + sb));
+            if constexpr (SHIFT == 0) {
+                v = A;
+            } else {
+                const uint4 B = __ldcs(reinterpret_cast<const uint4*>(a.src + sb + 8));
+                v = realign8<SHIFT>(A, B);
+            }
+        } else {
+            uint16_t t[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) t[j] = a.src[a.lo + 8 * k + j];
+            v.x = (uint32_t)t[0] | ((uint32_t)t[1] << 16);
+            v.y = (uint32_t)t[2] | ((uint32_t)t[3] << 16);
+            v.z = (uint32_t)t[4] | ((uint32_t)t[5] << 16);
+            v.w = (uint32_t)t[6] | ((uint32_t)t[7] << 16);
+        }
+        for (int o = 0; o < a.n_out; ++o) __stcs(reinterpret_cast<uint4*>(a.out.p[o] + 8 * k), v);
+    }
+    if (blockIdx.x == 0) {
+        for (int64_t d = nvec * 8 + threadIdx.x; d < a.len; d += kThreads) {
+            const uint16_t x = a.src[a.lo + d];
+            for (int o = 0; o < a.n_out; ++o) a.out.p[o][d] = x;
+        }
+    }
+}
+
+cudaError_t launch_gather(const GatherArgs& a, cudaStream_t st)
+{
+    const int64_t work = (a.len / 8 + kThreads - 1) / kThreads;
+    auto go = [&](const void* k, auto kern) {
+        kern<<<grid_for(k, work < 1 ? 1 : work), kThreads, 0, st>>>(a);
+        return cudaGetLastError();
+    };
+    switch ((int)(a.lo & 7)) {
+    case 0: return go(reinterpret_cast<const void*>(&k_gather<0>), k_gather<0>);
+    case 1: return go(reinterpret_cast<const void*>(&k_gather<1>), k_gather<1>);
+    case 2: return go(reinterpret_cast<const void*>(&k_gather<2>), k_gather<2>);
+    case 3: return go(reinterpret_cast<const void*>(&k_gather<3>), k_gather<3>);
+    case 4: return go(reinterpret_cast<const void*>(&k_gather<4>), k_gather<4>);
+    case 5: return go(reinterpret_cast<const void*>(&k_gather<5>), k_gather<5>);
+    case 6: return go(reinterpret_cast<const void*>(&k_gather<6>), k_gather<6>);
+    default: return go(reinterpret_cast<const void*>(&k_gather<7>), k_gather<7>);
+    }
+}
+
+}  // namespace
+
+extern "C" zero_status zero3_step(const zero_plan_t* plan, const uint16_t* const* rank_grads,
+                                  float* master, float* m, float* v, uint16_t* param_shards,
+                                  const zero_adamw_hparams* hp, int64_t step, int32_t flags,
+                                  int32_t* dev_status, void* stream)
+{
+    if (zero_status e = check_plan(plan)) return e;
+    if (zero_status e = check_hparams(hp, step)) return e;
+    if (flags & ~ZERO_FLAG_CHECK_FINITE) return ZERO_ERR_INVALID_ARG;
+    if ((flags & ZERO_FLAG_CHECK_FINITE) && !dev_status) return ZERO_ERR_NULL;
+    if (plan->N == 0) return ZERO_OK;
+    Range rs[ZERO_MAX_RM + 6];
+    int nr = 0;
+    if (zero_status e = check_grads(plan, rank_grads, rs, nr)) return e;
+    if (zero_status e = check_state(plan, master, m, v, rs, nr)) return e;
+    if (zero_status e = check_ptr(param_shards)) return e;
+    rs[nr++] = rng(param_shards, 2 * plan->padded, true);
+    if (dev_status) rs[nr++] = rng(dev_status, 4, true);
+    if (zero_status e = check_overlap(rs, nr)) return e;
+    FusedArgs a{};
+    fill_grad_ptrs(a.g, plan, rank_grads);
+    a.P.p[0] = param_shards;
+    a.zero3 = 1;
+    a.W = master;
+    a.m = m;
+    a.v = v;
+    a.n = plan->N;
+    a.R = plan->R;
+    a.M = plan->M;
+    a.s = step_scalars(*hp, step, plan->R, plan->M);
+    a.status = dev_status;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool check = (flags & ZERO_FLAG_CHECK_FINITE) != 0;
+    return cuda_status(check ? launch_fused<true>(a, st) : launch_fused<false>(a, st));
+}
+
+extern "C" zero_status zero3_gather(const zero_plan_t* plan, const uint16_t* param_shards,
+                                    int64_t lo, int64_t hi, uint16_t* const* outs, int32_t n_out,
+                                    void* stream)
+{
+    if (zero_status e = check_plan(plan)) return e;
+    if (lo < 0 || hi < lo || hi > plan->N) return ZERO_ERR_INVALID_ARG;
+    if (n_out < 1 || n_out > plan->R) return ZERO_ERR_INVALID_ARG;
+    if (hi == lo) return ZERO_OK;
+    if (!outs) return ZERO_ERR_NULL;
+    Range rs[ZERO_MAX_R + 1];
+    int nr = 0;
+    if (zero_status e = check_ptr(param_shards)) return e;
+    rs[nr++] = rng(param_shards, 2 * plan->padded, false);
+    for (int o = 0; o < n_out; ++o) {
+        if (zero_status e = check_ptr(outs[o])) return e;
+        rs[nr++] = rng(outs[o], 2 * (hi - lo), true);
+    }
+    if (zero_status e = check_overlap(rs, nr)) return e;
+    GatherArgs a{};
+    for (int o = 0; o < n_out; ++o) a.out.p[o] = outs[o];
+    a.src = param_shards;
+    a.src_len = plan->padded;
+    a.lo = lo;
+    a.len = hi - lo;
+    a.n_out = n_out;
+    return cuda_status(launch_gather(a, static_cast<cudaStream_t>(stream)));
 }
 
 // ================================================ staged step, no allocation ==
