@@ -79,7 +79,9 @@ typedef enum {
     ZERO_ERR_OVERLAP = -5,         /* an output overlaps another buffer        */
     ZERO_ERR_CUDA = -6,            /* a CUDA launch or copy failed             */
     ZERO_ERR_DEVICE_TIMEOUT = -7,  /* reserved for device-side bounded waits   */
-    ZERO_ERR_NONFINITE = -8        /* reported through the device status word  */
+    ZERO_ERR_NONFINITE = -8,       /* reported through the device status word  */
+    ZERO_ERR_IO = -9,              /* a checkpoint file could not be written/read */
+    ZERO_ERR_CORRUPT = -10         /* a checkpoint header or checksum is wrong  */
 } zero_status;
 
 /* Bits OR-ed into the optional device status word. */
@@ -311,6 +313,79 @@ zero_status zero_step_staged_noalloc(const zero_plan_t* plan, const uint16_t* co
                                      uint16_t* const* rank_params, const zero_adamw_hparams* hp,
                                      int64_t step, int32_t flags, int32_t* dev_status,
                                      void* stream);
+
+/* ------------------------------------------------------------------------
+ * Sharded optimizer-state checkpoints and R -> R' resharding.
+ * One file per rank shard, "<dir>/shard-RRRRR-of-NNNNN.zck": a 128-byte
+ * header (layout R, rank, N, S, lo, len; step; AdamW hyper-parameters;
+ * Fletcher-64 checksums of payload and header), then the rank's elements
+ * [lo, lo+len) as bf16 params, fp32 master, m, v: 14 bytes per parameter,
+ * BLOOM's checkpoint layout (CS324 Lecture 9 notes, section 2.1).  Each file
+ * is written to "<name>.tmp", fsync'ed and renamed (sharded, atomic writes:
+ * LLM infra 06, section 15.4); one checkpoint per directory.  Loading under
+ * another plan (another R', same N) reads, for each new shard, the byte
+ * ranges of the old shards that overlap it: the merge a different card
+ * count needs (CS324 Lecture 9 notes, exercise 11).  A save followed by a
+ * load reproduces every bit, so training resumes bit-identically (section
+ * 3.1, PaLM).
+ * ---------------------------------------------------------------------- */
+
+typedef struct zero_ckpt_job zero_ckpt_job;
+
+/*
+ * Host layer (no GPU needed).  params: host, N bf16 (element i at [i]);
+ * master, m, v: host, element i at [i] (plan->padded or at least N floats).
+ * Writes every shard of `plan` into dir (created if missing), n_threads
+ * files at a time.  Errors: ZERO_ERR_NULL, ZERO_ERR_INVALID_ARG, ZERO_ERR_IO.
+ */
+zero_status zero_ckpt_write_host(const zero_plan_t* plan, const uint16_t* params,
+                                 const float* master, const float* m, const float* v,
+                                 int64_t step, const zero_adamw_hparams* hp, const char* dir,
+                                 int32_t n_threads);
+
+/*
+ * Host layer: read the checkpoint in dir into the layout of `plan` (same N,
+ * any R).  rank = -1 fills every element [0, N); rank = r fills only the
+ * elements of the new shard r (what rank r would load on its own GPU).
+ * The old shards touched are checksum-verified first.  step_out / hp_out may
+ * be NULL.  Errors: ZERO_ERR_IO (missing/short file), ZERO_ERR_CORRUPT (bad
+ * magic, header or payload checksum, inconsistent shards), ZERO_ERR_SIZE
+ * (the checkpoint has another N).
+ */
+zero_status zero_ckpt_read_host(const zero_plan_t* plan, const char* dir, int32_t rank,
+                                uint16_t* params, float* master, float* m, float* v,
+                                int64_t* step_out, zero_adamw_hparams* hp_out);
+
+/*
+ * Device layer, asynchronous save: enqueues device-to-host copies of the
+ * state (dev_params: N bf16, e.g. replica 0 or the ZeRO-3 shard buffer;
+ * dev_master/m/v: element i at [i]) into a pinned staging buffer on
+ * `stream`, then writes the shard files on a background thread once the
+ * copies have landed.  Later work on `stream` is ordered after the copies,
+ * so training can continue at once.  *job must be passed to
+ * zero_ckpt_job_wait, which joins the writer, frees the staging buffer and
+ * returns the write status.  The library allocates the staging buffer
+ * (14 bytes/param of pinned host memory).
+ */
+zero_status zero_ckpt_save_async(const zero_plan_t* plan, const uint16_t* dev_params,
+                                 const float* dev_master, const float* dev_m, const float* dev_v,
+                                 int64_t step, const zero_adamw_hparams* hp, const char* dir,
+                                 int32_t n_threads, void* stream, zero_ckpt_job** job);
+
+/* Wait for an asynchronous save; frees the job.  Returns its status. */
+zero_status zero_ckpt_job_wait(zero_ckpt_job* job);
+
+/*
+ * Device layer, load: reads the checkpoint in dir (any R) into the layout
+ * of `plan` and copies it to the device: dev_master/m/v element i at [i] (the
+ * pad is not written), the bf16 params into each of the n_params device
+ * buffers dev_params[k] (N bf16: the R replicas, or one ZeRO-3 shard
+ * buffer).  Synchronizes `stream` before returning.  Errors as
+ * zero_ckpt_read_host, plus ZERO_ERR_CUDA.
+ */
+zero_status zero_ckpt_load(const zero_plan_t* plan, const char* dir, uint16_t* const* dev_params,
+                           int32_t n_params, float* dev_master, float* dev_m, float* dev_v,
+                           int64_t* step_out, zero_adamw_hparams* hp_out, void* stream);
 
 #ifdef __cplusplus
 }

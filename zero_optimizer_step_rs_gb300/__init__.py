@@ -11,6 +11,8 @@ from .binding import (  # noqa: F401
     EXPORTED, Plan, ZeroError, hparams, lib, zero_abi_version, zero_adamw_shard, zero_ag_cast,
     zero_plan_create, zero_plan_destroy, zero_plan_owner, zero_rs_avg, zero_status_string,
     zero_step, zero_step_host, zero_step_staged_noalloc, zero_step_clipped,
-    zero_clip_scratch_bytes, ZERO_DEV_SKIPPED, ZERO_FLAG_SKIP_NONFINITE, zero3_step, zero3_gather, ZERO_DEV_NONFINITE, ZERO_FLAG_CHECK_FINITE, ZERO_VARIANT_FUSED,
+    zero_clip_scratch_bytes, ZERO_DEV_SKIPPED, ZERO_FLAG_SKIP_NONFINITE, zero3_step, zero3_gather,
+    zero_ckpt_write_host, zero_ckpt_read_host, zero_ckpt_save_async, zero_ckpt_job_wait,
+    zero_ckpt_load, ZERO_DEV_NONFINITE, ZERO_FLAG_CHECK_FINITE, ZERO_VARIANT_FUSED,
     ZERO_VARIANT_STAGED,
 )

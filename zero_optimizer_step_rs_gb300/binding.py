@@ -24,6 +24,8 @@ ZERO_ERR_OVERLAP = -5
 ZERO_ERR_CUDA = -6
 ZERO_ERR_DEVICE_TIMEOUT = -7
 ZERO_ERR_NONFINITE = -8
+ZERO_ERR_IO = -9
+ZERO_ERR_CORRUPT = -10
 ZERO_DEV_NONFINITE = 1
 ZERO_DEV_SKIPPED = 4
 ZERO_FLAG_CHECK_FINITE = 1
@@ -37,7 +39,9 @@ ZERO_NOALLOC_MAX_ELEMS = 4 * 1024 * 1024
 EXPORTED = ("zero_abi_version", "zero_status_string", "zero_plan_create", "zero_plan_destroy",
             "zero_plan_owner", "zero_step", "zero_rs_avg", "zero_adamw_shard", "zero_ag_cast",
             "zero_step_host", "zero_step_staged_noalloc", "zero_step_clipped",
-            "zero_clip_scratch_bytes", "zero3_step", "zero3_gather")
+            "zero_clip_scratch_bytes", "zero3_step", "zero3_gather", "zero_ckpt_write_host",
+            "zero_ckpt_read_host", "zero_ckpt_save_async", "zero_ckpt_job_wait",
+            "zero_ckpt_load")
 
 
 class ZeroError(RuntimeError):
@@ -109,6 +113,21 @@ def lib():
         L.zero3_step.restype = ctypes.c_int
         L.zero3_gather.argtypes = [P(zero_plan_t), vp, i64, i64, vp, i32, vp]
         L.zero3_gather.restype = ctypes.c_int
+        L.zero_ckpt_write_host.argtypes = [P(zero_plan_t), vp, vp, vp, vp, i64,
+                                           P(zero_adamw_hparams), ctypes.c_char_p, i32]
+        L.zero_ckpt_write_host.restype = ctypes.c_int
+        L.zero_ckpt_read_host.argtypes = [P(zero_plan_t), ctypes.c_char_p, i32, vp, vp, vp, vp,
+                                          P(i64), P(zero_adamw_hparams)]
+        L.zero_ckpt_read_host.restype = ctypes.c_int
+        L.zero_ckpt_save_async.argtypes = [P(zero_plan_t), vp, vp, vp, vp, i64,
+                                           P(zero_adamw_hparams), ctypes.c_char_p, i32, vp,
+                                           P(vp)]
+        L.zero_ckpt_save_async.restype = ctypes.c_int
+        L.zero_ckpt_job_wait.argtypes = [vp]
+        L.zero_ckpt_job_wait.restype = ctypes.c_int
+        L.zero_ckpt_load.argtypes = [P(zero_plan_t), ctypes.c_char_p, vp, i32, vp, vp, vp, P(i64),
+                                     P(zero_adamw_hparams), vp]
+        L.zero_ckpt_load.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -402,3 +421,75 @@ def zero3_gather(plan: Plan, param_shards, lo: int, hi: int, outs, stream=None) 
     oa = _ptrs([_addr(o) for o in outs])
     _check(lib().zero3_gather(plan.ptr, _addr(param_shards), lo, hi, ctypes.addressof(oa),
                               len(outs), _stream(stream)), "zero3_gather")
+
+
+# -------------------------------------------------------------- checkpoints --
+
+def _np_ptr(a):
+    return a.ctypes.data
+
+
+def zero_ckpt_write_host(plan: Plan, params, master, m, v, step: int, hp: zero_adamw_hparams,
+                         directory: str, n_threads: int = 8) -> None:
+    """Write the checkpoint of host numpy arrays (params uint16 bf16 bits of N,
+    master/m/v float32 with element i at [i])."""
+    _check(lib().zero_ckpt_write_host(plan.ptr, _np_ptr(params), _np_ptr(master), _np_ptr(m),
+                                      _np_ptr(v), step, ctypes.byref(hp),
+                                      os.fsencode(directory), n_threads), "zero_ckpt_write_host")
+
+
+def zero_ckpt_read_host(plan: Plan, directory: str, params, master, m, v, rank: int = -1):
+    """Read a checkpoint (any R) into host numpy arrays in plan's layout;
+    returns (step, hparams)."""
+    step = ctypes.c_int64(0)
+    hp = zero_adamw_hparams()
+    _check(lib().zero_ckpt_read_host(plan.ptr, os.fsencode(directory), rank, _np_ptr(params),
+                                     _np_ptr(master), _np_ptr(m), _np_ptr(v), ctypes.byref(step),
+                                     ctypes.byref(hp)), "zero_ckpt_read_host")
+    return step.value, hp
+
+
+class CkptJob:
+    def __init__(self, handle):
+        self._h = handle
+
+    def wait(self) -> None:
+        if self._h:
+            code = lib().zero_ckpt_job_wait(self._h)
+            self._h = None
+            _check(code, "zero_ckpt_job_wait")
+
+
+def zero_ckpt_save_async(plan: Plan, params, master, m, v, step: int, hp: zero_adamw_hparams,
+                         directory: str, n_threads: int = 8, stream=None) -> CkptJob:
+    c = plan.c
+    _check_tensor(params, "bf16", c.N, "params")
+    for nm, t in (("master", master), ("m", m), ("v", v)):
+        _check_tensor(t, "f32", c.N, nm)
+    job = ctypes.c_void_p()
+    _check(lib().zero_ckpt_save_async(plan.ptr, _addr(params), _addr(master), _addr(m), _addr(v),
+                                      step, ctypes.byref(hp), os.fsencode(directory), n_threads,
+                                      _stream(stream), ctypes.byref(job)), "zero_ckpt_save_async")
+    return CkptJob(job.value)
+
+
+def zero_ckpt_job_wait(job: CkptJob) -> None:
+    job.wait()
+
+
+def zero_ckpt_load(plan: Plan, directory: str, params_list, master, m, v, stream=None):
+    """Load a checkpoint (any R) onto the device in plan's layout; returns
+    (step, hparams)."""
+    c = plan.c
+    for k, p in enumerate(params_list):
+        _check_tensor(p, "bf16", c.N, f"params[{k}]")
+    for nm, t in (("master", master), ("m", m), ("v", v)):
+        _check_tensor(t, "f32", c.N, nm)
+    pa = _ptrs([_addr(p) for p in params_list])
+    step = ctypes.c_int64(0)
+    hp = zero_adamw_hparams()
+    _check(lib().zero_ckpt_load(plan.ptr, os.fsencode(directory), ctypes.addressof(pa),
+                                len(params_list), _addr(master), _addr(m), _addr(v),
+                                ctypes.byref(step), ctypes.byref(hp), _stream(stream)),
+           "zero_ckpt_load")
+    return step.value, hp

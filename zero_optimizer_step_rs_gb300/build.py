@@ -21,7 +21,8 @@ BUILD_DIR = os.path.join(PKG, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
-SOURCES = [os.path.join(CSRC, "zero_step.cu"), os.path.join(CSRC, "plan.cpp")]
+SOURCES = [os.path.join(CSRC, "zero_step.cu"), os.path.join(CSRC, "plan.cpp"),
+           os.path.join(CSRC, "ckpt.cpp")]
 HEADERS = [os.path.join(INCLUDE, "zero_step.h")]
 
 

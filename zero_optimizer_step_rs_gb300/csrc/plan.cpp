@@ -41,6 +41,8 @@ extern "C" const char* zero_status_string(zero_status s)
     case ZERO_ERR_CUDA: return "CUDA launch or copy failed";
     case ZERO_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
     case ZERO_ERR_NONFINITE: return "non-finite gradient";
+    case ZERO_ERR_IO: return "checkpoint file could not be written or read";
+    case ZERO_ERR_CORRUPT: return "checkpoint header or checksum is wrong";
     }
     return "unknown status";
 }
