@@ -119,6 +119,15 @@ def lib():
             L.oracle_zero3_gather.argtypes = [i64, i32, i64, vp, i64, i64, i32, vp,
                                               ctypes.POINTER(ctypes.c_int64)]
             L.oracle_zero3_gather.restype = ctypes.c_int
+            L.oracle_fp16_rne.argtypes = [ctypes.c_float]
+            L.oracle_fp16_rne.restype = ctypes.c_uint16
+            L.oracle_fp16_to_float.argtypes = [ctypes.c_uint16]
+            L.oracle_fp16_to_float.restype = ctypes.c_float
+            L.oracle_compress.argtypes = [i32, vp, i64, vp]
+            L.oracle_compress.restype = None
+            L.oracle_dp_step_compressed.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp,
+                                                    ctypes.POINTER(HParams), i64, i32, vp]
+            L.oracle_dp_step_compressed.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -310,3 +319,43 @@ def zero3_gather(Pshard, n: int, R: int, S: int, lo: int, hi: int, card: int = 0
     if rc != 0:
         raise RuntimeError(f"oracle_zero3_gather failed: {rc}")
     return out[:hi - lo], recv.value
+
+
+COMP_NONE, COMP_FP16, COMP_INT8, COMP_SIGN = 0, 1, 2, 3
+
+
+def fp16_rne(x: float) -> int:
+    return int(lib().oracle_fp16_rne(ctypes.c_float(x)))
+
+
+def fp16_to_float(h: int) -> float:
+    return float(lib().oracle_fp16_to_float(ctypes.c_uint16(h)))
+
+
+def compress(kind: int, x: np.ndarray) -> np.ndarray:
+    _check(x, np.float32, None, "x")
+    d = np.empty(max(1, x.size), np.float32)
+    lib().oracle_compress(kind, _ptr(x), x.size, _ptr(d))
+    return d[:x.size]
+
+
+def dp_step_compressed(G, W, m, v, P, hp: HParams, step: int, R: int, M: int, kind: int,
+                       E=None) -> None:
+    n = W.size
+    for k, g in enumerate(G):
+        _check(g, np.uint16, n, f"G[{k}]")
+    for k, p in enumerate(P):
+        _check(p, np.uint16, n, f"P[{k}]")
+    for nm, a in (("W", W), ("m", m), ("v", v)):
+        _check(a, np.float32, n, nm)
+    ga, pa = _ptr_array(G), _ptr_array(P)
+    ea = None
+    if E is not None:
+        for k, e in enumerate(E):
+            _check(e, np.float32, n, f"E[{k}]")
+        ea = _ptr_array(E)
+    rc = lib().oracle_dp_step_compressed(n, R, M, ctypes.addressof(ga), _ptr(W), _ptr(m), _ptr(v),
+                                         ctypes.addressof(pa), ctypes.byref(hp), step, kind,
+                                         ctypes.addressof(ea) if ea is not None else None)
+    if rc != 0:
+        raise RuntimeError(f"oracle_dp_step_compressed failed: {rc}")

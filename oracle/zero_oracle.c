@@ -486,3 +486,128 @@ int oracle_zero3_gather(int64_t n, int32_t R, int64_t S, const uint16_t* Pshard,
     if (recv) *recv = from_others;
     return 0;
 }
+
+/* ----------------------------------------------------------- compression -- */
+
+uint16_t oracle_fp16_rne(float x)
+{
+    uint32_t u = f2u(x);
+    uint32_t sign = (u >> 16) & 0x8000u;
+    uint32_t a = u & 0x7FFFFFFFu;
+    if (a > 0x7F800000u) return (uint16_t)(sign | 0x7E00u);       /* NaN */
+    if (a >= 0x477FF000u) return (uint16_t)(sign | 0x7C00u);      /* >= 65520: Inf */
+    if (a <= 0x33000000u) return (uint16_t)sign;                  /* <= 2^-25: 0 */
+    int32_t e = (int32_t)(a >> 23) - 127;
+    if (e >= -14) {
+        /* normal: keep 10 of the 23 fraction bits, ties to even; a carry
+         * moves into the exponent; re-bias the exponent from 127 to 15 */
+        uint32_t r = a + 0xFFFu + ((a >> 13) & 1u);
+        r >>= 13;
+        return (uint16_t)(sign | (r - ((127u - 15u) << 10)));
+    }
+    /* subnormal: value / 2^-24 rounded to an integer, ties to even */
+    uint32_t mant = (a & 0x7FFFFFu) | 0x800000u;     /* value = mant * 2^(e-23) */
+    int32_t shift = -e - 1;                          /* 14 .. 24 */
+    uint32_t q = mant >> shift;
+    uint32_t rem = mant & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1);
+    if (rem > half || (rem == half && (q & 1u))) ++q;
+    return (uint16_t)(sign | q);
+}
+
+float oracle_fp16_to_float(uint16_t h)
+{
+    uint32_t sign = (uint32_t)(h & 0x8000u) << 16;
+    uint32_t e = (h >> 10) & 0x1Fu, f = h & 0x3FFu;
+    if (e == 0x1F) return u2f(sign | 0x7F800000u | (f << 13));
+    if (e == 0) {                                    /* zero or subnormal: f * 2^-24 */
+        float v = (float)f * 5.9604644775390625e-08f;
+        return sign ? -v : v;
+    }
+    return u2f(sign | ((e + 127u - 15u) << 23) | (f << 13));
+}
+
+/* pairwise fp32 sum of |x| over one block of up to 128 leaves, zero padded */
+static float abs_tree(const float* x, int64_t count, int64_t lo, int64_t len)
+{
+    if (len == 1) return lo < count ? fabsf(x[lo]) : 0.0f;
+    if (lo >= count) return 0.0f;
+    float a = abs_tree(x, count, lo, len / 2);
+    float b = abs_tree(x, count, lo + len / 2, len / 2);
+    return a + b;
+}
+
+void oracle_compress(int32_t kind, const float* x, int64_t n, float* d)
+{
+    for (int64_t b0 = 0; b0 < n; b0 += ORACLE_COMP_BLOCK) {
+        int64_t cnt = n - b0 < ORACLE_COMP_BLOCK ? n - b0 : ORACLE_COMP_BLOCK;
+        const float* xb = x + b0;
+        float* db = d + b0;
+        if (kind == ORACLE_COMP_FP16) {
+            for (int64_t k = 0; k < cnt; ++k) db[k] = oracle_fp16_to_float(oracle_fp16_rne(xb[k]));
+        } else if (kind == ORACLE_COMP_INT8) {
+            float amax = 0.0f;
+            for (int64_t k = 0; k < cnt; ++k) {
+                float a = fabsf(xb[k]);
+                if (a != a || a > amax) amax = a;   /* a NaN wins, like an unsigned compare */
+                if (amax != amax) break;
+            }
+            float s = amax / 127.0f;
+            for (int64_t k = 0; k < cnt; ++k) {
+                if (s == 0.0f) {
+                    db[k] = 0.0f;
+                } else {
+                    float q = rintf(xb[k] / s);
+                    q = fminf(fmaxf(q, -127.0f), 127.0f);
+                    db[k] = q * s;
+                }
+            }
+        } else if (kind == ORACLE_COMP_SIGN) {
+            float s = abs_tree(xb, cnt, 0, ORACLE_COMP_BLOCK) / (float)cnt;
+            for (int64_t k = 0; k < cnt; ++k) db[k] = xb[k] < 0.0f ? -s : s;
+        } else {
+            for (int64_t k = 0; k < cnt; ++k) db[k] = xb[k];
+        }
+    }
+}
+
+int oracle_dp_step_compressed(int64_t n, int32_t R, int32_t M,
+                              const uint16_t* const* G, float* W, float* m, float* v,
+                              uint16_t* const* P, const oracle_hparams* hp,
+                              int64_t step, int32_t kind, float* const* E)
+{
+    if (check_args(n, R, M, G, W, m, v, P, hp, step)) return -1;
+    if (kind < ORACLE_COMP_NONE || kind > ORACLE_COMP_SIGN) return -1;
+    oracle_scalars s;
+    oracle_make_scalars(hp, step, R, M, &s);
+    size_t nn = (size_t)(n > 0 ? n : 1);
+    float* x = (float*)malloc(sizeof(float) * nn);
+    float* d = (float*)malloc(sizeof(float) * nn);
+    float* acc = (float*)malloc(sizeof(float) * nn);
+    if (!x || !d || !acc) { free(x); free(d); free(acc); return -2; }
+    for (int32_t r = 0; r < R; ++r) {
+        /* rank r: local accumulation of its micro-batches, error feedback */
+        for (int64_t i = 0; i < n; ++i) {
+            float loc = oracle_bf16_to_float(G[(int64_t)r * M][i]);
+            for (int32_t j = 1; j < M; ++j)
+                loc = loc + oracle_bf16_to_float(G[(int64_t)r * M + j][i]);
+            x[i] = E ? loc + E[r][i] : loc;
+        }
+        oracle_compress(kind, x, n, d);
+        for (int64_t i = 0; i < n; ++i) {
+            if (E) E[r][i] = x[i] - d[i];
+            /* the owner adds the decompressed contributions in rank order */
+            acc[i] = (r == 0) ? d[i] : acc[i] + d[i];
+        }
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        float g = acc[i] / s.denom_rm;
+        oracle_adamw_elem(&s, g, &W[i], &m[i], &v[i]);
+        uint16_t p = oracle_bf16_rne(W[i]);
+        for (int32_t r = 0; r < R; ++r) P[r][i] = p;
+    }
+    free(x);
+    free(d);
+    free(acc);
+    return 0;
+}

@@ -229,6 +229,46 @@ int oracle_zero3_gather(int64_t n, int32_t R, int64_t S, const uint16_t* Pshard,
                         int64_t lo, int64_t hi, int32_t card, uint16_t* out,
                         int64_t* recv);
 
+/* ------------------------------------------------------------------------
+ * Compressed gradient reduce-scatter (CS324 Lecture 9 notes, section 7.4:
+ * every card compresses the gradient it sends - fp16, int8, sign - with or
+ * without error feedback, where each card keeps what compression dropped
+ * and adds it back to its next gradient; real systems quantize int8 per
+ * block rather than with one scale for the whole vector).
+ * Reading R14: each rank compresses its locally accumulated gradient x_r
+ * (after error feedback, x_r + e_r) over aligned blocks of 128 elements of
+ * the flat vector (the last block may be short), and the owner sums the
+ * decompressed values in rank order, then divides by R*M:
+ *   fp16: d = (float)fp16_rne(x)                      (2 bytes/param sent)
+ *   int8: a = max|x| over the block; s = a / 127; d = 0 when s == 0, else
+ *         d = clamp(rint(x / s), -127, 127) * s        (1 + 4/128 bytes)
+ *   sign: s = (pairwise fp32 tree sum of |x| over the block, zero padded to
+ *         128) / count; d = (x < 0) ? -s : s          (1/8 + 4/128 bytes)
+ * With error feedback the residual becomes e_r = x_r - d.
+ * ---------------------------------------------------------------------- */
+
+#define ORACLE_COMP_NONE 0
+#define ORACLE_COMP_FP16 1
+#define ORACLE_COMP_INT8 2
+#define ORACLE_COMP_SIGN 3
+#define ORACLE_COMP_BLOCK 128
+
+/* binary16 round to nearest even from the format definition (NaN -> 0x7E00) */
+uint16_t oracle_fp16_rne(float x);
+float    oracle_fp16_to_float(uint16_t h);
+
+/* Compress and decompress x[0..n) (blocks of 128 starting at element 0):
+ * d[k] receives the value the receiver reconstructs. */
+void oracle_compress(int32_t kind, const float* x, int64_t n, float* d);
+
+/* DP step with a compressed reduce-scatter (R14).  E: NULL (no error
+ * feedback) or R pointers to fp32 residuals of n elements, updated in
+ * place.  Returns 0, -1, or -2 on allocation failure. */
+int oracle_dp_step_compressed(int64_t n, int32_t R, int32_t M,
+                              const uint16_t* const* G, float* W, float* m, float* v,
+                              uint16_t* const* P, const oracle_hparams* hp,
+                              int64_t step, int32_t kind, float* const* E);
+
 #ifdef __cplusplus
 }
 #endif

@@ -59,6 +59,14 @@ MUTANTS = {
                                       "if (recv && k / M != r) recv[r] += len;"),
     "zero3_shard_cast_truncates": ("Pshard[lo + k] = oracle_bf16_rne(W[lo + k]);",
                                    "Pshard[lo + k] = (uint16_t)(((union { float f; uint32_t u; }){W[lo + k]}).u >> 16);"),
+    "fp16_truncates": ("uint32_t r = a + 0xFFFu + ((a >> 13) & 1u);", "uint32_t r = a + 0u * ((a >> 13) & 1u);"),
+    "fp16_subnormal_no_round": ("if (rem > half || (rem == half && (q & 1u))) ++q;", "if (rem > half + rem) ++q;"),
+    "int8_scale_128": ("float s = amax / 127.0f;", "float s = amax / 128.0f;"),
+    "int8_truncates": ("float q = rintf(xb[k] / s);", "float q = truncf(xb[k] / s);"),
+    "sign_uses_max": ("float s = abs_tree(xb, cnt, 0, ORACLE_COMP_BLOCK) / (float)cnt;",
+                      "float s = abs_tree(xb, cnt, 0, ORACLE_COMP_BLOCK) / (float)ORACLE_COMP_BLOCK;"),
+    "ef_sign_flipped": ("if (E) E[r][i] = x[i] - d[i];", "if (E) E[r][i] = d[i] - x[i];"),
+    "ef_not_added": ("x[i] = E ? loc + E[r][i] : loc;", "x[i] = E ? loc + 0.0f * E[r][i] : loc;"),
 }
 
 
@@ -76,6 +84,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     env = dict(os.environ, ZERO_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         "tests/test_oracle_pins.py", "tests/test_oracle_collectives.py",
-                        "tests/test_oracle_clip.py", "tests/test_oracle_zero3.py"],
+                        "tests/test_oracle_clip.py", "tests/test_oracle_zero3.py",
+                        "tests/test_oracle_compress.py"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
