@@ -539,6 +539,42 @@ def run_table(args):
         del ds, shards
         torch.cuda.empty_cache()
 
+    # compressed reduce-scatter on the 1B-shaped workload: each codec with and
+    # without error feedback
+    wl = W.llama32_1b()
+    ds = H.DeviceState(wl, staged_scratch=False)
+    ds.fill_state_device()
+    ds.fill_grads_device(wl.step)
+    res = [torch.zeros(wl.N, dtype=torch.float32, device="cuda") for _ in range(wl.R)]
+    wire = {z.ZERO_COMP_FP16: 2.0, z.ZERO_COMP_INT8: 1 + 4 / 128, z.ZERO_COMP_SIGN: 1 / 8 + 4 / 128}
+    names = {z.ZERO_COMP_FP16: "fp16", z.ZERO_COMP_INT8: "int8/128", z.ZERO_COMP_SIGN: "sign/128"}
+    for kind in (z.ZERO_COMP_FP16, z.ZERO_COMP_INT8, z.ZERO_COMP_SIGN):
+        for ef in (False, True):
+            ts, t = [], wl.step
+            for k in range(3 + 10):
+                flush.fill_(k & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                z.zero_step_compressed(ds.plan, ds.grads, ds.W, ds.m, ds.v, ds.params, ds.hp, t,
+                                       kind, res if ef else None)
+                e1.record()
+                torch.cuda.synchronize()
+                t += 1
+                if k >= 3:
+                    ts.append(e0.elapsed_time(e1))
+            ms = float(np.median(ts))
+            b = 2 * wl.R * wl.M + 24 + 2 * wl.R + (8 * wl.R if ef else 0)
+            row = {"workload": "llama-3.2-1b", "R": wl.R, "M": wl.M, "N": wl.N,
+                   "variant": "compressed", "codec": names[kind], "error_feedback": ef,
+                   "wire_bytes_per_param_per_rank": round(wire[kind], 4),
+                   "ms": round(ms, 4), "params_per_s": wl.N / (ms / 1e3), "bytes_per_param": b,
+                   "GB_s": round(b * wl.N / (ms / 1e3) / 1e9, 1),
+                   "frac_of_measured_peak": round(b * wl.N / (ms / 1e3) / 1e9 / peak, 4)}
+            rows.append(row)
+            print(json.dumps(row), flush=True)
+    del ds, res
+    torch.cuda.empty_cache()
+
     for R in (2, 4, 8):
         S = 1024
         while S <= 256 * 1024 * 1024:

@@ -230,6 +230,36 @@ zero_status zero_step_clipped(const zero_plan_t* plan, const uint16_t* const* ra
 /* Scratch bytes zero_step_clipped needs for this plan (-1 for a bad plan). */
 int64_t zero_clip_scratch_bytes(const zero_plan_t* plan);
 
+/* Codecs for zero_step_compressed. */
+#define ZERO_COMP_FP16 1           /* binary16, round to nearest even: 2 bytes sent a param */
+#define ZERO_COMP_INT8 2           /* per 128-element block: 1 byte + a 4-byte scale */
+#define ZERO_COMP_SIGN 3           /* per 128-element block: 1 bit + a 4-byte magnitude */
+
+/*
+ * Step with a compressed gradient reduce-scatter (CS324 Lecture 9 notes,
+ * section 7.4: each card compresses what it sends - fp16, int8 quantised per
+ * block, sign only - optionally with error feedback, each card keeping what
+ * the compression dropped and adding it to its next gradient).  Rank r's
+ * locally accumulated gradient x_r (+ its residual e_r) is compressed over
+ * aligned blocks of 128 elements of the flat vector (the last may be short):
+ *   FP16: d = binary16(x) (round to nearest even)
+ *   INT8: s = max|x| / 127 per block; d = 0 if s == 0, else
+ *         clamp(rint(x / s), -127, 127) * s
+ *   SIGN: s = (pairwise fp32 sum of |x| over the block) / count;
+ *         d = (x < 0) ? -s : s
+ * The owner sums the d_r in rank order, divides by R*M, and AdamW and the
+ * all-gather follow as in zero_step.
+ *   residuals  NULL (no error feedback), or a host array of R device
+ *              pointers, N floats each (16-byte aligned), read and updated
+ *              in place: e_r <- x_r - d_r.  Start them at zero.
+ * Traffic: 2RM + 24 + 2R bytes/param, plus 8R with error feedback (the
+ * compressed message itself lives in registers, never in memory).
+ */
+zero_status zero_step_compressed(const zero_plan_t* plan, const uint16_t* const* rank_grads,
+                                 float* master, float* m, float* v, uint16_t* const* rank_params,
+                                 const zero_adamw_hparams* hp, int64_t step, int32_t kind,
+                                 float* const* residuals, void* stream);
+
 /*
  * ZeRO-3 step (CS25 V6 Lecture 4 notes, "ZeRO-3 / FSDP": the parameters are
  * sharded as well and materialised per unit just before use; CS324 Lecture

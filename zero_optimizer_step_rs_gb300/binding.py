@@ -32,6 +32,9 @@ ZERO_FLAG_CHECK_FINITE = 1
 ZERO_FLAG_SKIP_NONFINITE = 2
 ZERO_VARIANT_FUSED = 0
 ZERO_VARIANT_STAGED = 1
+ZERO_COMP_FP16 = 1
+ZERO_COMP_INT8 = 2
+ZERO_COMP_SIGN = 3
 ZERO_MAX_R = 64
 ZERO_MAX_RM = 256
 ZERO_NOALLOC_MAX_ELEMS = 4 * 1024 * 1024
@@ -41,7 +44,7 @@ EXPORTED = ("zero_abi_version", "zero_status_string", "zero_plan_create", "zero_
             "zero_step_host", "zero_step_staged_noalloc", "zero_step_clipped",
             "zero_clip_scratch_bytes", "zero3_step", "zero3_gather", "zero_ckpt_write_host",
             "zero_ckpt_read_host", "zero_ckpt_save_async", "zero_ckpt_job_wait",
-            "zero_ckpt_load")
+            "zero_ckpt_load", "zero_step_compressed")
 
 
 class ZeroError(RuntimeError):
@@ -128,6 +131,9 @@ def lib():
         L.zero_ckpt_load.argtypes = [P(zero_plan_t), ctypes.c_char_p, vp, i32, vp, vp, vp, P(i64),
                                      P(zero_adamw_hparams), vp]
         L.zero_ckpt_load.restype = ctypes.c_int
+        L.zero_step_compressed.argtypes = [P(zero_plan_t), vp, vp, vp, vp, vp,
+                                           P(zero_adamw_hparams), i64, i32, vp, vp]
+        L.zero_step_compressed.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -493,3 +499,31 @@ def zero_ckpt_load(plan: Plan, directory: str, params_list, master, m, v, stream
                                 ctypes.byref(step), ctypes.byref(hp), _stream(stream)),
            "zero_ckpt_load")
     return step.value, hp
+
+
+def zero_step_compressed(plan: Plan, rank_grads, master, m, v, rank_params,
+                         hp: zero_adamw_hparams, step: int, kind: int, residuals=None,
+                         stream=None) -> None:
+    """Step with a compressed reduce-scatter (kind: ZERO_COMP_FP16 / INT8 /
+    SIGN); residuals: None, or R float32 device tensors of N (error feedback)."""
+    c = plan.c
+    for k, g in enumerate(rank_grads):
+        _check_tensor(g, "bf16", c.N, f"rank_grads[{k}]")
+    for k, p in enumerate(rank_params):
+        _check_tensor(p, "bf16", c.N, f"rank_params[{k}]")
+    for nm, t in (("master", master), ("m", m), ("v", v)):
+        _check_tensor(t, "f32", c.padded, nm)
+    if len(rank_grads) != c.R * c.M or len(rank_params) != c.R:
+        raise ValueError(f"need {c.R * c.M} gradient buffers and {c.R} replicas")
+    ea = None
+    if residuals is not None:
+        if len(residuals) != c.R:
+            raise ValueError(f"need {c.R} residual buffers")
+        for k, e in enumerate(residuals):
+            _check_tensor(e, "f32", c.N, f"residuals[{k}]")
+        ea = _ptrs([_addr(e) for e in residuals])
+    ga, pa = _ptrs([_addr(g) for g in rank_grads]), _ptrs([_addr(p) for p in rank_params])
+    _check(lib().zero_step_compressed(plan.ptr, ctypes.addressof(ga), _addr(master), _addr(m),
+                                      _addr(v), ctypes.addressof(pa), ctypes.byref(hp), step, kind,
+                                      ctypes.addressof(ea) if ea is not None else None,
+                                      _stream(stream)), "zero_step_compressed")

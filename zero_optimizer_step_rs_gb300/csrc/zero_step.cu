@@ -27,6 +27,7 @@
 // give each rank r its own grid row (blockIdx.y = r) and grid-stride over
 // the vectors of shard r, as rank r would on its own GPU.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -1229,6 +1230,231 @@ extern "C" zero_status zero_step_clipped(const zero_plan_t* plan,
     }
     if (err == cudaSuccess) err = launch_adamw_ag(a, st);
     return cuda_status(err);
+}
+
+// ================================================ compressed reduce-scatter ==
+// zero_step_compressed: every rank compresses its locally accumulated
+// gradient (plus its error-feedback residual) over aligned blocks of 128
+// elements of the flat vector before the emulated reduce-scatter, and the
+// owner sums the decompressed values in rank order (the header gives the
+// three codecs).  One warp owns one block: lane l holds elements 4l..4l+3,
+// so the block max is a warp max of |x| and the block's |x| sum is a pairwise
+// tree - the 4 leaves of a lane, then 5 shuffle levels - in element order.
+// The compressed message is never written to memory: on one GPU the wire
+// is a register, and only its decompressed value matters to the owner.
+namespace {
+
+constexpr int kCompBlock = 128;
+
+struct CompArgs {
+    GradPtrs g;
+    ReplicaPtrs P;
+    float* E[ZERO_MAX_R];  // error-feedback residuals (N floats per rank) or unused
+    float* W;
+    float* m;
+    float* v;
+    int64_t n;
+    int32_t R, M;
+    StepScalars s;
+};
+
+template <int KIND>
+__device__ __forceinline__ void codec(float (&x)[4], const bool (&valid)[4], int64_t block_count,
+                                      float (&d)[4])
+{
+    if constexpr (KIND == ZERO_COMP_FP16) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) d[k] = __half2float(__float2half_rn(x[k]));
+    } else if constexpr (KIND == ZERO_COMP_INT8) {
+        uint32_t amax = 0;                        // |x| bits order like the values
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (valid[k]) amax = max(amax, __float_as_uint(x[k]) & 0x7FFFFFFFu);
+        amax = __reduce_max_sync(0xFFFFFFFFu, amax);
+        const float sc = __fdiv_rn(__uint_as_float(amax), 127.0f);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (sc == 0.0f) {
+                d[k] = 0.0f;
+            } else {
+                float q = rintf(__fdiv_rn(x[k], sc));
+                q = fminf(fmaxf(q, -127.0f), 127.0f);
+                d[k] = __fmul_rn(q, sc);
+            }
+        }
+    } else {                                      // ZERO_COMP_SIGN
+        float a[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) a[k] = valid[k] ? fabsf(x[k]) : 0.0f;
+        float t = __fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3]));
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) t = __fadd_rn(t, __shfl_down_sync(0xFFFFFFFFu, t, off));
+        t = __shfl_sync(0xFFFFFFFFu, t, 0);
+        const float sc = __fdiv_rn(t, (float)block_count);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) d[k] = x[k] < 0.0f ? -sc : sc;
+    }
+}
+
+template <int RC, int MC, int KIND, bool EF>
+__global__ void __launch_bounds__(kThreads) k_comp(const __grid_constant__ CompArgs a)
+{
+    const int R = RC > 0 ? RC : a.R;
+    const int M = MC > 0 ? MC : a.M;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
+    const int64_t n = a.n;
+    const int64_t nblk = (n + kCompBlock - 1) / kCompBlock;
+    for (int64_t b = warp; b < nblk; b += nwarps) {       // warp-uniform loop
+        const int64_t e = b * kCompBlock + 4 * lane;
+        const bool full = b * kCompBlock + kCompBlock <= n;
+        const int64_t block_count = full ? kCompBlock : n - b * kCompBlock;
+        bool valid[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) valid[k] = e + k < n;
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int r = 0; r < R; ++r) {
+            float x[4];
+            // rank r's local accumulation of its micro-batches
+            for (int j = 0; j < M; ++j) {
+                float y[4];
+                if (full) {
+                    const uint2 u = ld_stream(a.g.p[r * M + j] + e);
+                    y[0] = bf16_lo(u.x); y[1] = bf16_hi(u.x); y[2] = bf16_lo(u.y); y[3] = bf16_hi(u.y);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) y[k] = valid[k] ? bf16_bits(a.g.p[r * M + j][e + k]) : 0.0f;
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) x[k] = j == 0 ? y[k] : __fadd_rn(x[k], y[k]);
+            }
+            float res[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if constexpr (EF) {
+                if (full) {
+                    const float4 q = ld_stream(a.E[r] + e);
+                    res[0] = q.x; res[1] = q.y; res[2] = q.z; res[3] = q.w;
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) res[k] = valid[k] ? a.E[r][e + k] : 0.0f;
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) x[k] = __fadd_rn(x[k], res[k]);
+            }
+            float d[4];
+            codec<KIND>(x, valid, block_count, d);
+            if constexpr (EF) {
+                float o[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) o[k] = __fsub_rn(x[k], d[k]);
+                if (full) {
+                    st_stream(a.E[r] + e, make_float4(o[0], o[1], o[2], o[3]));
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) if (valid[k]) a.E[r][e + k] = o[k];
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[k] = r == 0 ? d[k] : __fadd_rn(acc[k], d[k]);
+        }
+        // the owner: average, AdamW, all-gather
+        if (full) {
+            float4 w = ld_stream(a.W + e), m = ld_stream(a.m + e), v = ld_stream(a.v + e);
+            float* wp = &w.x;
+            float* mp = &m.x;
+            float* vp = &v.x;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) adamw(a.s, scale_grad(a.s, acc[k]), wp[k], mp[k], vp[k]);
+            st_stream(a.W + e, w);
+            st_stream(a.m + e, m);
+            st_stream(a.v + e, v);
+            const uint2 p = make_uint2(pack_bf16x2(w.x, w.y), pack_bf16x2(w.z, w.w));
+            for (int r = 0; r < R; ++r) st_stream(a.P.p[r] + e, p);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (!valid[k]) continue;
+                const int64_t i = e + k;
+                float w = a.W[i], m = a.m[i], v = a.v[i];
+                adamw(a.s, scale_grad(a.s, acc[k]), w, m, v);
+                a.W[i] = w;
+                a.m[i] = m;
+                a.v[i] = v;
+                const uint16_t p = to_bf16(w);
+                for (int r = 0; r < R; ++r) a.P.p[r][i] = p;
+            }
+        }
+    }
+}
+
+template <int RC, int MC, int KIND, bool EF>
+cudaError_t launch_comp_t(const CompArgs& a, cudaStream_t st)
+{
+    const void* k = reinterpret_cast<const void*>(&k_comp<RC, MC, KIND, EF>);
+    const int64_t blocks = (a.n + kCompBlock - 1) / kCompBlock;   // one warp each
+    const int64_t work = (blocks + kThreads / 32 - 1) / (kThreads / 32);
+    k_comp<RC, MC, KIND, EF><<<grid_for(k, work < 1 ? 1 : work), kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <int KIND, bool EF>
+cudaError_t launch_comp_rm(const CompArgs& a, cudaStream_t st)
+{
+    if (a.R == 8 && a.M == 1) return launch_comp_t<8, 1, KIND, EF>(a, st);
+    if (a.R == 4 && a.M == 1) return launch_comp_t<4, 1, KIND, EF>(a, st);
+    if (a.R == 7 && a.M == 4) return launch_comp_t<7, 4, KIND, EF>(a, st);
+    return launch_comp_t<0, 0, KIND, EF>(a, st);
+}
+
+cudaError_t launch_comp(const CompArgs& a, int kind, bool ef, cudaStream_t st)
+{
+    switch (kind) {
+    case ZERO_COMP_FP16:
+        return ef ? launch_comp_rm<ZERO_COMP_FP16, true>(a, st) : launch_comp_rm<ZERO_COMP_FP16, false>(a, st);
+    case ZERO_COMP_INT8:
+        return ef ? launch_comp_rm<ZERO_COMP_INT8, true>(a, st) : launch_comp_rm<ZERO_COMP_INT8, false>(a, st);
+    default:
+        return ef ? launch_comp_rm<ZERO_COMP_SIGN, true>(a, st) : launch_comp_rm<ZERO_COMP_SIGN, false>(a, st);
+    }
+}
+
+}  // namespace
+
+extern "C" zero_status zero_step_compressed(const zero_plan_t* plan,
+                                            const uint16_t* const* rank_grads, float* master,
+                                            float* m, float* v, uint16_t* const* rank_params,
+                                            const zero_adamw_hparams* hp, int64_t step,
+                                            int32_t kind, float* const* residuals, void* stream)
+{
+    if (zero_status e = check_plan(plan)) return e;
+    if (zero_status e = check_hparams(hp, step)) return e;
+    if (kind != ZERO_COMP_FP16 && kind != ZERO_COMP_INT8 && kind != ZERO_COMP_SIGN)
+        return ZERO_ERR_INVALID_ARG;
+    if (plan->N == 0) return ZERO_OK;
+    Range rs[ZERO_MAX_RM + 2 * ZERO_MAX_R + 4];
+    int nr = 0;
+    if (zero_status e = check_grads(plan, rank_grads, rs, nr)) return e;
+    if (zero_status e = check_replicas(plan, rank_params, rs, nr)) return e;
+    if (zero_status e = check_state(plan, master, m, v, rs, nr)) return e;
+    CompArgs a{};
+    if (residuals) {
+        for (int r = 0; r < plan->R; ++r) {
+            if (zero_status e = check_ptr(residuals[r])) return e;
+            rs[nr++] = rng(residuals[r], 4 * plan->N, true);
+            a.E[r] = residuals[r];
+        }
+    }
+    if (zero_status e = check_overlap(rs, nr)) return e;
+    fill_grad_ptrs(a.g, plan, rank_grads);
+    fill_replica_ptrs(a.P, plan, rank_params);
+    a.W = master;
+    a.m = m;
+    a.v = v;
+    a.n = plan->N;
+    a.R = plan->R;
+    a.M = plan->M;
+    a.s = step_scalars(*hp, step, plan->R, plan->M);
+    return cuda_status(launch_comp(a, kind, residuals != nullptr, static_cast<cudaStream_t>(stream)));
 }
 
 // ================================================================ ZeRO-3 ==
