@@ -267,7 +267,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     wl = W.by_name(args.workload)
-    variant = z.ZERO_VARIANT_STAGED if args.variant == "staged" else z.ZERO_VARIANT_FUSED
+    variant = {"staged": z.ZERO_VARIANT_STAGED, "tma": z.ZERO_VARIANT_FUSED_TMA}.get(
+        args.variant, z.ZERO_VARIANT_FUSED)
     clipped = args.variant == "clipped"
     stream = torch.cuda.current_stream()
 
@@ -323,7 +324,7 @@ def run_ours(args, rank, world, local_rank):
     value = N * args.steps * world / (total_ms / 1e3)
     if clipped:
         bpp = 2 * wl.R * wl.M + 4 + 4 + 24 + 2 * wl.R      # stash written and read back
-    elif variant == z.ZERO_VARIANT_FUSED:
+    elif variant in (z.ZERO_VARIANT_FUSED, z.ZERO_VARIANT_FUSED_TMA):
         bpp = wl.bytes_per_param()
     else:
         bpp = 2 * wl.R * wl.M + 4 + 4 + 24 + 4 + 2 * wl.R
@@ -344,7 +345,7 @@ def run_ours(args, rank, world, local_rank):
                 "unit": "GB/s", "frac": round(achieved_gbs / peak, 4), "traffic": traffic,
                 "peak_source": peak_src,
                 "kernel": ("clipped step (k_rs_norm, k_tree, k_clip_coef, k_adamw_ag)" if clipped
-                           else "k_fused" if variant == 0 else "staged trio"),
+                           else {0: "k_fused", 1: "staged trio", 2: "k_fused_tma"}[variant]),
                 "algorithmic_bytes_per_launch": alg_bytes, "bytes_per_param": bpp}
 
     # -------- end to end through the host-buffer entry point
@@ -389,7 +390,7 @@ def run_ours(args, rank, world, local_rank):
     if clipped:
         launches_per_step = 2 + len(_tree_levels(N))   # rs_norm, tree levels, coef, update
     else:
-        launches_per_step = 1 if variant == z.ZERO_VARIANT_FUSED else 3
+        launches_per_step = 3 if variant == z.ZERO_VARIANT_STAGED else 1
     del ds
     torch.cuda.empty_cache()
 
@@ -635,7 +636,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama-3.2-1b")
-    ap.add_argument("--variant", choices=["fused", "staged", "clipped"], default="fused")
+    ap.add_argument("--variant", choices=["fused", "staged", "clipped", "tma"], default="fused")
     ap.add_argument("--max-norm", type=float, default=1.0,
                     help="global-norm clip threshold for --variant clipped")
     ap.add_argument("--no-e2e", action="store_true")

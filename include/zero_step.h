@@ -86,15 +86,23 @@ typedef enum {
 
 /* Bits OR-ed into the optional device status word. */
 #define ZERO_DEV_NONFINITE 1       /* an averaged gradient (or the norm) was Inf or NaN */
+#define ZERO_DEV_TIMEOUT 2         /* a bounded device wait ran out (TMA variant) */
 #define ZERO_DEV_SKIPPED 4         /* zero_step_clipped skipped the update      */
 
 /* Flags for zero_step / zero_rs_avg. */
 #define ZERO_FLAG_CHECK_FINITE 1   /* set ZERO_DEV_NONFINITE when g is non-finite */
 #define ZERO_FLAG_SKIP_NONFINITE 2 /* zero_step_clipped: skip the update on a non-finite norm */
+/* Test-only, ZERO_VARIANT_FUSED_TMA: every bounded device wait gives up at
+ * once, so the timeout path runs: the kernel drains its copies, sets
+ * ZERO_DEV_TIMEOUT and returns without updating anything it had not
+ * reached.  Needs dev_status. */
+#define ZERO_FLAG_DEBUG_EXPIRE_WAITS (1 << 30)
 
 /* Variants for zero_step. */
 #define ZERO_VARIANT_FUSED 0       /* one pass: rs -> adamw -> ag per element  */
 #define ZERO_VARIANT_STAGED 1      /* rs_avg, adamw_shard, ag_cast, fp32 g in scratch */
+#define ZERO_VARIANT_FUSED_TMA 2   /* one pass, tiles staged by TMA bulk copies (R*M <= 16) */
+#define ZERO_TMA_MAX_RM 16
 
 /*
  * Shard layout of a flat parameter vector (the tensors concatenated in the
@@ -162,14 +170,20 @@ int32_t zero_plan_owner(const zero_plan_t* plan, int64_t i);
  *   hp          AdamW hyper-parameters (0 <= beta1, beta2 < 1; lr, eps,
  *               weight_decay finite; eps >= 0).
  *   step        the step count t >= 1 used for bias correction.
- *   variant     ZERO_VARIANT_FUSED or ZERO_VARIANT_STAGED.
+ *   variant     ZERO_VARIANT_FUSED, ZERO_VARIANT_STAGED, or
+ *               ZERO_VARIANT_FUSED_TMA (the fused pass with each tile's
+ *               gradient and state streams brought into shared memory by
+ *               cp.async.bulk copies completing on an mbarrier, and the
+ *               replicas written back by bulk stores; R*M <= 16; every
+ *               device wait is bounded and reports ZERO_DEV_TIMEOUT).
  *   scratch     device scratch of scratch_bytes bytes; the staged variant
  *               needs plan->scratch_bytes_staged (fp32 reduced gradient of
  *               every shard); ignored (may be NULL) for the fused variant.
- *   flags       0 or ZERO_FLAG_CHECK_FINITE.
+ *   flags       0, ZERO_FLAG_CHECK_FINITE, and for the TMA variant
+ *               ZERO_FLAG_DEBUG_EXPIRE_WAITS (test only).
  *   dev_status  optional device int32 the kernels OR ZERO_DEV_* bits into.
  * Outputs (master, m, v, replicas, scratch) must not overlap one another or
- * any gradient buffer (ZERO_ERR_OVERLAP).  The two variants give identical
+ * any gradient buffer (ZERO_ERR_OVERLAP).  All variants give identical
  * bits.
  */
 zero_status zero_step(const zero_plan_t* plan, const uint16_t* const* rank_grads,
@@ -229,6 +243,21 @@ zero_status zero_step_clipped(const zero_plan_t* plan, const uint16_t* const* ra
 
 /* Scratch bytes zero_step_clipped needs for this plan (-1 for a bad plan). */
 int64_t zero_clip_scratch_bytes(const zero_plan_t* plan);
+
+/*
+ * Replica consistency check, a silent-data-corruption detector (LLM infra
+ * 06, section 15.4: a GPU that flips a bit is found by comparing what two
+ * ranks computed on the same data).  After the all-gather every replica must
+ * hold the same bits; this counts the elements where any replica differs
+ * from rank 0's.
+ *   dev_count  device int64 (8-byte aligned): receives the count (zeroed
+ *              first, on `stream`).
+ *   dev_first  optional device int64: receives the first such index, or
+ *              INT64_MAX when there is none.
+ * Reads 2R bytes per parameter.
+ */
+zero_status zero_check_replicas(const zero_plan_t* plan, uint16_t* const* rank_params,
+                                int64_t* dev_count, int64_t* dev_first, void* stream);
 
 /* Codecs for zero_step_compressed. */
 #define ZERO_COMP_FP16 1           /* binary16, round to nearest even: 2 bytes sent a param */

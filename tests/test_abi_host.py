@@ -109,6 +109,11 @@ BASE = 1 << 40
 
 
 def fake_bufs(plan, gap=1 << 30):
+    # fake addresses are only ever handed to the library where no GPU is
+    # visible: a call that got past validation by mistake then fails with
+    # ZERO_ERR_CUDA instead of touching memory
+    if torch.cuda.is_available():
+        pytest.skip("fake device addresses are used only on machines without a GPU")
     c = plan.c
     addr = [BASE + k * gap for k in range(c.R * c.M + c.R + 5)]
     grads = addr[:c.R * c.M]
@@ -146,7 +151,7 @@ def test_step_null_and_align(plan):
 def test_step_invalid_args(plan):
     g, Wp, mp, vp, P, scr, st = fake_bufs(plan)
     assert call_step(plan, g, Wp, mp, vp, P, step=0) == B.ZERO_ERR_INVALID_ARG
-    assert call_step(plan, g, Wp, mp, vp, P, variant=2) == B.ZERO_ERR_INVALID_ARG
+    assert call_step(plan, g, Wp, mp, vp, P, variant=3) == B.ZERO_ERR_INVALID_ARG
     assert call_step(plan, g, Wp, mp, vp, P, flags=4) == B.ZERO_ERR_INVALID_ARG
     assert call_step(plan, g, Wp, mp, vp, P, flags=1) == B.ZERO_ERR_NULL     # no status word
     for bad in (dict(beta1=1.0), dict(beta2=1.5), dict(beta1=-0.1), dict(eps=-1.0),
@@ -250,3 +255,15 @@ def test_clipped_step_argument_errors():
     assert call(flags=8) == B.ZERO_ERR_INVALID_ARG
     assert call(flags=B.ZERO_FLAG_CHECK_FINITE) == B.ZERO_ERR_NULL
     assert call(sumsq=st + 4) == B.ZERO_ERR_ALIGN
+
+
+def test_tma_variant_argument_errors(plan):
+    g, Wp, mp, vp, P, scr, st = fake_bufs(plan)
+    # debug flag needs the TMA variant and a status word
+    assert call_step(plan, g, Wp, mp, vp, P, variant=0,
+                     flags=B.ZERO_FLAG_DEBUG_EXPIRE_WAITS, status=st) == B.ZERO_ERR_INVALID_ARG
+    assert call_step(plan, g, Wp, mp, vp, P, variant=2,
+                     flags=B.ZERO_FLAG_DEBUG_EXPIRE_WAITS) == B.ZERO_ERR_NULL
+    big = z.Plan([1000], 16, 2, 2)                     # R*M = 32 > 16
+    g2, Wp2, mp2, vp2, P2, _, _ = fake_bufs(big)
+    assert call_step(big, g2, Wp2, mp2, vp2, P2, variant=2) == B.ZERO_ERR_INVALID_ARG

@@ -32,6 +32,9 @@ ZERO_FLAG_CHECK_FINITE = 1
 ZERO_FLAG_SKIP_NONFINITE = 2
 ZERO_VARIANT_FUSED = 0
 ZERO_VARIANT_STAGED = 1
+ZERO_VARIANT_FUSED_TMA = 2
+ZERO_DEV_TIMEOUT = 2
+ZERO_FLAG_DEBUG_EXPIRE_WAITS = 1 << 30
 ZERO_COMP_FP16 = 1
 ZERO_COMP_INT8 = 2
 ZERO_COMP_SIGN = 3
@@ -44,7 +47,7 @@ EXPORTED = ("zero_abi_version", "zero_status_string", "zero_plan_create", "zero_
             "zero_step_host", "zero_step_staged_noalloc", "zero_step_clipped",
             "zero_clip_scratch_bytes", "zero3_step", "zero3_gather", "zero_ckpt_write_host",
             "zero_ckpt_read_host", "zero_ckpt_save_async", "zero_ckpt_job_wait",
-            "zero_ckpt_load", "zero_step_compressed")
+            "zero_ckpt_load", "zero_step_compressed", "zero_check_replicas")
 
 
 class ZeroError(RuntimeError):
@@ -134,6 +137,8 @@ def lib():
         L.zero_step_compressed.argtypes = [P(zero_plan_t), vp, vp, vp, vp, vp,
                                            P(zero_adamw_hparams), i64, i32, vp, vp]
         L.zero_step_compressed.restype = ctypes.c_int
+        L.zero_check_replicas.argtypes = [P(zero_plan_t), vp, vp, vp, vp]
+        L.zero_check_replicas.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -527,3 +532,14 @@ def zero_step_compressed(plan: Plan, rank_grads, master, m, v, rank_params,
                                       _addr(v), ctypes.addressof(pa), ctypes.byref(hp), step, kind,
                                       ctypes.addressof(ea) if ea is not None else None,
                                       _stream(stream)), "zero_step_compressed")
+
+
+def zero_check_replicas(plan: Plan, rank_params, dev_count, dev_first=None, stream=None) -> None:
+    """Count (into dev_count, an int64 device tensor of 1) the elements where
+    any replica differs from replica 0; dev_first receives the first index."""
+    c = plan.c
+    for k, p in enumerate(rank_params):
+        _check_tensor(p, "bf16", c.N, f"rank_params[{k}]")
+    pa = _ptrs([_addr(p) for p in rank_params])
+    _check(lib().zero_check_replicas(plan.ptr, ctypes.addressof(pa), _addr(dev_count),
+                                     _addr(dev_first), _stream(stream)), "zero_check_replicas")

@@ -31,6 +31,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <climits>
 #include <cmath>
 #include <mutex>
 #include <unordered_map>
@@ -638,6 +639,8 @@ zero_status check_state(const zero_plan_t* plan, float* W, float* m, float* v, R
 
 zero_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ZERO_OK : ZERO_ERR_CUDA; }
 
+cudaError_t launch_fused_tma(const FusedArgs& a, bool expire_waits, bool check, cudaStream_t st);
+
 void fill_grad_ptrs(GradPtrs& g, const zero_plan_t* plan, const uint16_t* const* grads)
 {
     for (int q = 0; q < plan->R * plan->M; ++q) g.p[q] = grads[q];
@@ -661,9 +664,16 @@ extern "C" zero_status zero_step(const zero_plan_t* plan, const uint16_t* const*
 {
     if (zero_status e = check_plan(plan)) return e;
     if (zero_status e = check_hparams(hp, step)) return e;
-    if (variant != ZERO_VARIANT_FUSED && variant != ZERO_VARIANT_STAGED) return ZERO_ERR_INVALID_ARG;
-    if (flags & ~ZERO_FLAG_CHECK_FINITE) return ZERO_ERR_INVALID_ARG;
-    if ((flags & ZERO_FLAG_CHECK_FINITE) && !dev_status) return ZERO_ERR_NULL;
+    if (variant != ZERO_VARIANT_FUSED && variant != ZERO_VARIANT_STAGED &&
+        variant != ZERO_VARIANT_FUSED_TMA)
+        return ZERO_ERR_INVALID_ARG;
+    if (variant == ZERO_VARIANT_FUSED_TMA && plan->R * plan->M > ZERO_TMA_MAX_RM)
+        return ZERO_ERR_INVALID_ARG;
+    const int32_t allowed = ZERO_FLAG_CHECK_FINITE |
+                            (variant == ZERO_VARIANT_FUSED_TMA ? ZERO_FLAG_DEBUG_EXPIRE_WAITS : 0);
+    if (flags & ~allowed) return ZERO_ERR_INVALID_ARG;
+    if ((flags & (ZERO_FLAG_CHECK_FINITE | ZERO_FLAG_DEBUG_EXPIRE_WAITS)) && !dev_status)
+        return ZERO_ERR_NULL;
     if (plan->N == 0) return ZERO_OK;
 
     Range rs[ZERO_MAX_RM + ZERO_MAX_R + 5];
@@ -683,7 +693,7 @@ extern "C" zero_status zero_step(const zero_plan_t* plan, const uint16_t* const*
     const bool check = (flags & ZERO_FLAG_CHECK_FINITE) != 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-    if (variant == ZERO_VARIANT_FUSED) {
+    if (variant == ZERO_VARIANT_FUSED || variant == ZERO_VARIANT_FUSED_TMA) {
         FusedArgs a{};
         fill_grad_ptrs(a.g, plan, rank_grads);
         fill_replica_ptrs(a.P, plan, rank_params);
@@ -695,6 +705,9 @@ extern "C" zero_status zero_step(const zero_plan_t* plan, const uint16_t* const*
         a.M = plan->M;
         a.s = s;
         a.status = dev_status;
+        if (variant == ZERO_VARIANT_FUSED_TMA)
+            return cuda_status(launch_fused_tma(a, (flags & ZERO_FLAG_DEBUG_EXPIRE_WAITS) != 0,
+                                                check, st));
         return cuda_status(check ? launch_fused<true>(a, st) : launch_fused<false>(a, st));
     }
 
@@ -1455,6 +1468,320 @@ extern "C" zero_status zero_step_compressed(const zero_plan_t* plan,
     a.M = plan->M;
     a.s = step_scalars(*hp, step, plan->R, plan->M);
     return cuda_status(launch_comp(a, kind, residuals != nullptr, static_cast<cudaStream_t>(stream)));
+}
+
+// ============================================== fused step, TMA bulk staging ==
+// k_fused_tma: the fused step with the R*M gradient tiles and the three
+// state tiles of each 1024-element tile brought into shared memory by
+// cp.async.bulk (one elected thread, completion on an mbarrier, 3 stages
+// in flight per block) and the replica tile written back by R bulk stores
+// from a double-buffered shared tile.  Same arithmetic as k_fused, same bits.
+// On this access pattern it measures a few percent below the register-
+// direct k_fused, which stays the default; it is the selectable variant
+// ZERO_VARIANT_FUSED_TMA.
+//
+// Every mbarrier wait is bounded.  When a wait runs out, the whole block
+// (the decision is block-uniform) stops, thread 0 waits - again bounded -
+// for the stage loads it has issued and not consumed, and for its bulk
+// stores, sets ZERO_DEV_TIMEOUT in the status word and the block returns, so
+// no copy can land in shared memory after the block has left.
+namespace {
+
+constexpr int kTmaTile = 1024;                   // 256 threads x 4 elements
+constexpr int kTmaStages = 3;
+constexpr uint32_t kWaitLimit = 1u << 22;        // tries of mbarrier.try_wait
+constexpr uint32_t kDrainLimit = 1u << 24;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_addr(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, uint32_t limit)
+{
+    for (uint32_t it = 0; it < limit; ++it)
+        if (mbar_try(b, parity)) return true;
+    return false;
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* b)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(b))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_addr(src)), "r"(bytes)
+                 : "memory");
+}
+
+struct TmaLayout {
+    uint32_t stage_bytes, smem_bytes;
+};
+
+TmaLayout tma_layout(int RM)
+{
+    TmaLayout L;
+    L.stage_bytes = (uint32_t)(RM * kTmaTile * 2 + 3 * kTmaTile * 4);
+    L.smem_bytes = 128 + kTmaStages * L.stage_bytes + 2 * kTmaTile * 2;
+    return L;
+}
+
+__global__ void __launch_bounds__(kThreads) k_fused_tma(const __grid_constant__ FusedArgs a,
+                                                        uint32_t wait_limit, int32_t check)
+{
+    const int R = a.R, M = a.M, RM = R * M;
+    constexpr uint32_t GB = kTmaTile * 2, SB = kTmaTile * 4;
+    const uint32_t stage_bytes = (uint32_t)RM * GB + 3 * SB;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint8_t* stages = smem + 128;
+    uint16_t* outbuf = reinterpret_cast<uint16_t*>(stages + kTmaStages * stage_bytes);
+    const int64_t ntiles = a.n / kTmaTile;
+    const int64_t my = ntiles > blockIdx.x ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int tid = threadIdx.x;
+
+    if (tid == 0) {
+        for (int s = 0; s < kTmaStages; ++s) mbar_init(&full[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    auto issue = [&](int64_t k) {
+        const int s = (int)(k % kTmaStages);
+        const int64_t e = (blockIdx.x + k * gridDim.x) * (int64_t)kTmaTile;
+        uint8_t* st = stages + s * stage_bytes;
+        mbar_expect_tx(&full[s], stage_bytes);
+        for (int q = 0; q < RM; ++q) bulk_load(st + q * GB, a.g.p[q] + e, GB, &full[s]);
+        bulk_load(st + RM * GB, a.W + e, SB, &full[s]);
+        bulk_load(st + RM * GB + SB, a.m + e, SB, &full[s]);
+        bulk_load(st + RM * GB + 2 * SB, a.v + e, SB, &full[s]);
+    };
+    if (tid == 0)
+        for (int64_t k = 0; k < kTmaStages && k < my; ++k) issue(k);
+
+    bool timed_out = false, bad = false;
+    int64_t k_fail = 0;
+    for (int64_t k = 0; k < my; ++k) {
+        const int s = (int)(k % kTmaStages);
+        const uint32_t ph = (uint32_t)((k / kTmaStages) & 1);
+        const bool ok = mbar_wait(&full[s], ph, wait_limit);
+        if (__syncthreads_or(!ok)) {
+            timed_out = true;
+            k_fail = k;
+            break;
+        }
+        const uint8_t* st = stages + s * stage_bytes;
+        const int64_t tile0 = (blockIdx.x + k * gridDim.x) * (int64_t)kTmaTile;
+        const int64_t e = tile0 + tid * 4;
+        float loc[4], tot[4];
+        int r = 0, j = 0;
+        for (int q = 0; q < RM; ++q) {
+            const uint2 x = *reinterpret_cast<const uint2*>(st + q * GB + tid * 8);
+            fold4(loc, tot, x, r, j, M);
+            if (++j == M) { j = 0; ++r; }
+        }
+        float4 w = *reinterpret_cast<const float4*>(st + RM * GB + tid * 16);
+        float4 m = *reinterpret_cast<const float4*>(st + RM * GB + SB + tid * 16);
+        float4 v = *reinterpret_cast<const float4*>(st + RM * GB + 2 * SB + tid * 16);
+        float* wp = &w.x;
+        float* mp = &m.x;
+        float* vp = &v.x;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float g = scale_grad(a.s, tot[q]);
+            if (check) bad |= !isfinite(g);
+            adamw(a.s, g, wp[q], mp[q], vp[q]);
+        }
+        st_stream(a.W + e, w);
+        st_stream(a.m + e, m);
+        st_stream(a.v + e, v);
+        uint16_t* ob = outbuf + (k & 1) * kTmaTile;
+        *reinterpret_cast<uint2*>(ob + tid * 4) =
+            make_uint2(pack_bf16x2(w.x, w.y), pack_bf16x2(w.z, w.w));
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();                       // stage s consumed, replica tile written
+        if (tid == 0) {
+            for (int q = 0; q < R; ++q) bulk_store(a.P.p[q] + tile0, ob, GB);
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            if (k + kTmaStages < my) issue(k + kTmaStages);
+            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // tile k-1's stores
+        }
+        __syncthreads();                       // out tile (k+1)&1 free again
+    }
+
+    if (timed_out) {
+        if (tid == 0) {
+            if (a.status) atomicOr(a.status, ZERO_DEV_TIMEOUT);
+            // the loads issued for tiles k_fail .. k_fail+stages-1 must land
+            // before this block's shared memory can be given to another block
+            for (int64_t kk = k_fail; kk < k_fail + kTmaStages && kk < my; ++kk)
+                mbar_wait(&full[kk % kTmaStages], (uint32_t)((kk / kTmaStages) & 1), kDrainLimit);
+        }
+        __syncthreads();
+    }
+    if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+
+    // the last partial tile, element by element, by the block that owns it
+    const int64_t tail0 = ntiles * kTmaTile;
+    if (!timed_out && tail0 < a.n && blockIdx.x == (unsigned)(ntiles % gridDim.x)) {
+        for (int64_t i = tail0 + tid; i < a.n; i += kThreads) {
+            const float g = scale_grad(a.s, grad_sum1(a.g, R, M, i));
+            if (check) bad |= !isfinite(g);
+            float w = a.W[i], m = a.m[i], v = a.v[i];
+            adamw(a.s, g, w, m, v);
+            a.W[i] = w;
+            a.m[i] = m;
+            a.v[i] = v;
+            const uint16_t p = to_bf16(w);
+            for (int q = 0; q < R; ++q) a.P.p[q][i] = p;
+        }
+    }
+    if (check && __any_sync(0xFFFFFFFFu, bad) && (tid & 31) == 0 && a.status)
+        atomicOr(a.status, ZERO_DEV_NONFINITE);
+}
+
+cudaError_t launch_fused_tma(const FusedArgs& a, bool expire_waits, bool check, cudaStream_t st)
+{
+    const TmaLayout L = tma_layout(a.R * a.M);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static std::mutex mu;
+    static uint32_t configured[64] = {};         // largest dynamic smem set per device
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (configured[dev & 63] < L.smem_bytes) {
+            cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&k_fused_tma),
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)L.smem_bytes);
+            if (e != cudaSuccess) return e;
+            configured[dev & 63] = L.smem_bytes;
+        }
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reinterpret_cast<const void*>(&k_fused_tma),
+                                                      kThreads, L.smem_bytes) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const int64_t tiles = a.n / kTmaTile;
+    int64_t grid = (int64_t)device_sms(dev) * per_sm;
+    if (grid > tiles) grid = tiles;
+    if (grid < 1) grid = 1;
+    k_fused_tma<<<(unsigned)grid, kThreads, L.smem_bytes, st>>>(a, expire_waits ? 0u : kWaitLimit,
+                                                               check ? 1 : 0);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// ====================================================== replica consistency ==
+// zero_check_replicas: count the elements where any rank's replica differs
+// from rank 0's, and the first such index - a silent-data-corruption check
+// (every replica must hold the same bits after the all-gather).
+namespace {
+
+struct CheckArgs {
+    ReplicaPtrs P;
+    int64_t n;
+    int32_t R;
+    unsigned long long* count;
+    long long* first;
+};
+
+__global__ void __launch_bounds__(kThreads) k_check(const __grid_constant__ CheckArgs a)
+{
+    const int64_t nvec = a.n / 8;
+    unsigned long long bad = 0;
+    long long first = LLONG_MAX;
+    for (int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x; q < nvec;
+         q += (int64_t)gridDim.x * kThreads) {
+        const int64_t e = q * 8;
+        const uint4 r0 = __ldcs(reinterpret_cast<const uint4*>(a.P.p[0] + e));
+        uint32_t diff[4] = {0, 0, 0, 0};
+        for (int r = 1; r < a.R; ++r) {
+            const uint4 x = __ldcs(reinterpret_cast<const uint4*>(a.P.p[r] + e));
+            diff[0] |= x.x ^ r0.x;
+            diff[1] |= x.y ^ r0.y;
+            diff[2] |= x.z ^ r0.z;
+            diff[3] |= x.w ^ r0.w;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (diff[k] & 0xFFFFu) { ++bad; first = min(first, (long long)(e + 2 * k)); }
+            if (diff[k] >> 16) { ++bad; first = min(first, (long long)(e + 2 * k + 1)); }
+        }
+    }
+    if (blockIdx.x == 0) {
+        for (int64_t i = nvec * 8 + threadIdx.x; i < a.n; i += kThreads) {
+            bool d = false;
+            for (int r = 1; r < a.R; ++r) d |= a.P.p[r][i] != a.P.p[0][i];
+            if (d) { ++bad; first = min(first, (long long)i); }
+        }
+    }
+    // warp-aggregated: one atomic per warp that saw a mismatch
+    for (int off = 16; off > 0; off >>= 1) {
+        bad += __shfl_down_sync(0xFFFFFFFFu, bad, off);
+        first = min(first, __shfl_down_sync(0xFFFFFFFFu, first, off));
+    }
+    if ((threadIdx.x & 31) == 0 && bad) {
+        atomicAdd(a.count, bad);
+        if (a.first) atomicMin(a.first, first);
+    }
+}
+
+}  // namespace
+
+extern "C" zero_status zero_check_replicas(const zero_plan_t* plan, uint16_t* const* rank_params,
+                                           int64_t* dev_count, int64_t* dev_first, void* stream)
+{
+    if (zero_status e = check_plan(plan)) return e;
+    if (!dev_count) return ZERO_ERR_NULL;
+    if (((uintptr_t)dev_count & 7u) || ((uintptr_t)dev_first & 7u)) return ZERO_ERR_ALIGN;
+    Range rs[ZERO_MAX_R + 2];
+    int nr = 0;
+    if (plan->N > 0)
+        if (zero_status e = check_replicas(plan, rank_params, rs, nr)) return e;
+    for (int k = 0; k < nr; ++k) rs[k].out = false;             // read only here
+    rs[nr++] = rng(dev_count, 8, true);
+    if (dev_first) rs[nr++] = rng(dev_first, 8, true);
+    if (zero_status e = check_overlap(rs, nr)) return e;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const long long none = LLONG_MAX;
+    if (cudaMemsetAsync(dev_count, 0, 8, st) != cudaSuccess) return ZERO_ERR_CUDA;
+    if (dev_first && cudaMemcpyAsync(dev_first, &none, 8, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return ZERO_ERR_CUDA;
+    if (plan->N == 0 || plan->R == 1) return ZERO_OK;
+    CheckArgs a{};
+    fill_replica_ptrs(a.P, plan, rank_params);
+    a.n = plan->N;
+    a.R = plan->R;
+    a.count = reinterpret_cast<unsigned long long*>(dev_count);
+    a.first = reinterpret_cast<long long*>(dev_first);
+    const void* k = reinterpret_cast<const void*>(&k_check);
+    const int64_t work = (a.n / 8 + kThreads - 1) / kThreads;
+    k_check<<<grid_for(k, work < 1 ? 1 : work), kThreads, 0, st>>>(a);
+    return cuda_status(cudaGetLastError());
 }
 
 // ================================================================ ZeRO-3 ==
