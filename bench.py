@@ -232,14 +232,14 @@ def max_over_ranks(x: float, device=None) -> float:
 # ------------------------------------------------------------ our arm --
 
 KERNEL_SRC = os.path.join(ROOT, "zero_optimizer_step_rs_gb300", "csrc", "zero_step.cu")
-NOALLOC_MARKER = "// ================================================ staged step, no allocation =="
+FUSED_PATH_END = "// ================================================== end of the fused path =="
 
 
 def kernel_source_hash() -> str:
-    """Hash of the kernel source the fused path is compiled from: zero_step.cu
-    up to its allocation-free section (which holds no code of k_fused)."""
+    """Hash of the source the fused path is compiled from: zero_step.cu up to
+    its end-of-fused-path marker (helpers, k_fused and its launch)."""
     with open(KERNEL_SRC) as f:
-        body = f.read().split(NOALLOC_MARKER)[0].rstrip()
+        body = f.read().split(FUSED_PATH_END)[0].rstrip()
     return hashlib.sha256(body.encode()).hexdigest()[:16]
 
 

@@ -240,6 +240,48 @@ __device__ __forceinline__ void report_nonfinite(bool bad, int32_t* status)
     }
 }
 
+// ------------------------------------------------------ launch helpers --
+
+struct DevInfo {
+    int sms = 0;
+    std::unordered_map<const void*, int> occ;
+};
+
+std::mutex g_mu;
+DevInfo g_dev[64];
+
+int device_sms(int dev)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevInfo& d = g_dev[dev & 63];
+    if (d.sms == 0) cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    return d.sms > 0 ? d.sms : 1;
+}
+
+int blocks_per_sm(int dev, const void* kernel)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevInfo& d = g_dev[dev & 63];
+    auto it = d.occ.find(kernel);
+    if (it != d.occ.end()) return it->second;
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, 0) != cudaSuccess ||
+        nb < 1)
+        nb = 1;
+    d.occ[kernel] = nb;
+    return nb;
+}
+
+// persistent grid: every SM gets its resident blocks, capped by the work
+unsigned grid_for(const void* kernel, int64_t work_blocks)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int64_t cap = (int64_t)device_sms(dev) * blocks_per_sm(dev, kernel);
+    int64_t g = work_blocks < cap ? work_blocks : cap;
+    return (unsigned)(g < 1 ? 1 : g);
+}
+
 // ---------------------------------------------------------- fused step --
 
 // OUT selects where the bf16 result goes, as a template switch so the plain
@@ -321,6 +363,43 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ Fuse
     }
     report_nonfinite<CHECK>(bad, a.status);
 }
+
+// ----------------------------------------------------- fused dispatch --
+
+template <int RC, int MC, bool CHECK, int OUT = 0>
+cudaError_t launch_fused_t(const FusedArgs& a, cudaStream_t st)
+{
+    constexpr int U = 2;
+    const void* k = reinterpret_cast<const void*>(&k_fused<RC, MC, U, CHECK, OUT>);
+    const int64_t tiles = (a.n + kUnit * U - 1) / (kUnit * U);
+    k_fused<RC, MC, U, CHECK, OUT><<<grid_for(k, tiles), kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <bool CHECK, int OUT>
+cudaError_t launch_fused_table(const FusedArgs& a, cudaStream_t st)
+{
+    const int R = a.R, M = a.M;
+#define ZERO_CASE(r_, m_) \
+    if (R == r_ && M == m_) return launch_fused_t<r_, m_, CHECK, OUT>(a, st);
+    ZERO_CASE(8, 1) ZERO_CASE(4, 1) ZERO_CASE(2, 1) ZERO_CASE(1, 1) ZERO_CASE(16, 1)
+    ZERO_CASE(4, 2) ZERO_CASE(7, 4) ZERO_CASE(8, 2) ZERO_CASE(4, 4) ZERO_CASE(2, 2)
+#undef ZERO_CASE
+    return launch_fused_t<0, 0, CHECK, OUT>(a, st);
+}
+
+template <bool CHECK>
+cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st)
+{
+    // the zero-copy host path is bound by the host link, not by HBM: one
+    // run-time (R, M) instantiation serves it
+    if (a.extra_rep) return launch_fused_t<0, 0, CHECK, 1>(a, st);
+    if (a.zero3) return launch_fused_table<CHECK, 2>(a, st);
+    return launch_fused_table<CHECK, 0>(a, st);
+}
+
+// ================================================== end of the fused path ==
+// (everything above is what k_fused and its launch are compiled from)
 
 // ------------------------------------------------------- staged steps --
 // Shard r = blockIdx.y covers [r*S, r*S + len), len = min(S, n - r*S).
@@ -419,82 +498,6 @@ __global__ void __launch_bounds__(kThreads) k_ag_cast(const __grid_constant__ St
             for (int k = 0; k < R; ++k) a.P.p[k][i] = p;
         }
     }
-}
-
-// ------------------------------------------------------ launch helpers --
-
-struct DevInfo {
-    int sms = 0;
-    std::unordered_map<const void*, int> occ;
-};
-
-std::mutex g_mu;
-DevInfo g_dev[64];
-
-int device_sms(int dev)
-{
-    std::lock_guard<std::mutex> lk(g_mu);
-    DevInfo& d = g_dev[dev & 63];
-    if (d.sms == 0) cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-    return d.sms > 0 ? d.sms : 1;
-}
-
-int blocks_per_sm(int dev, const void* kernel)
-{
-    std::lock_guard<std::mutex> lk(g_mu);
-    DevInfo& d = g_dev[dev & 63];
-    auto it = d.occ.find(kernel);
-    if (it != d.occ.end()) return it->second;
-    int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, 0) != cudaSuccess ||
-        nb < 1)
-        nb = 1;
-    d.occ[kernel] = nb;
-    return nb;
-}
-
-// persistent grid: every SM gets its resident blocks, capped by the work
-unsigned grid_for(const void* kernel, int64_t work_blocks)
-{
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const int64_t cap = (int64_t)device_sms(dev) * blocks_per_sm(dev, kernel);
-    int64_t g = work_blocks < cap ? work_blocks : cap;
-    return (unsigned)(g < 1 ? 1 : g);
-}
-
-// ----------------------------------------------------- fused dispatch --
-
-template <int RC, int MC, bool CHECK, int OUT = 0>
-cudaError_t launch_fused_t(const FusedArgs& a, cudaStream_t st)
-{
-    constexpr int U = 2;
-    const void* k = reinterpret_cast<const void*>(&k_fused<RC, MC, U, CHECK, OUT>);
-    const int64_t tiles = (a.n + kUnit * U - 1) / (kUnit * U);
-    k_fused<RC, MC, U, CHECK, OUT><<<grid_for(k, tiles), kThreads, 0, st>>>(a);
-    return cudaGetLastError();
-}
-
-template <bool CHECK, int OUT>
-cudaError_t launch_fused_table(const FusedArgs& a, cudaStream_t st)
-{
-    const int R = a.R, M = a.M;
-#define ZERO_CASE(r_, m_) \
-    if (R == r_ && M == m_) return launch_fused_t<r_, m_, CHECK, OUT>(a, st);
-    ZERO_CASE(8, 1) ZERO_CASE(4, 1) ZERO_CASE(2, 1) ZERO_CASE(1, 1) ZERO_CASE(16, 1)
-    ZERO_CASE(4, 2) ZERO_CASE(7, 4) ZERO_CASE(8, 2) ZERO_CASE(4, 4) ZERO_CASE(2, 2)
-#undef ZERO_CASE
-    return launch_fused_t<0, 0, CHECK, OUT>(a, st);
-}
-
-template <bool CHECK>
-cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st)
-{
-    // the zero-copy host path is bound by the host link, not by HBM: one
-    // run-time (R, M) instantiation serves it
-    if (a.extra_rep) return launch_fused_t<0, 0, CHECK, 1>(a, st);
-    if (a.zero3) return launch_fused_table<CHECK, 2>(a, st);
-    return launch_fused_table<CHECK, 0>(a, st);
 }
 
 template <bool CHECK>
