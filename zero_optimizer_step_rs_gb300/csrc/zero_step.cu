@@ -1312,6 +1312,56 @@ __device__ __forceinline__ void codec(float (&x)[4], const bool (&valid)[4], int
     }
 }
 
+template <int KIND, bool EF>
+__device__ __forceinline__ void comp_ranks_generic(const CompArgs& a, int R, int M, int64_t e,
+                                                   bool full, const bool (&valid)[4],
+                                                   int64_t block_count, float (&acc)[4])
+{
+    for (int r = 0; r < R; ++r) {
+        float x[4];
+        // rank r's local accumulation of its micro-batches
+        for (int j = 0; j < M; ++j) {
+            float y[4];
+            if (full) {
+                const uint2 u = ld_stream(a.g.p[r * M + j] + e);
+                y[0] = bf16_lo(u.x); y[1] = bf16_hi(u.x); y[2] = bf16_lo(u.y); y[3] = bf16_hi(u.y);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) y[k] = valid[k] ? bf16_bits(a.g.p[r * M + j][e + k]) : 0.0f;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x[k] = j == 0 ? y[k] : __fadd_rn(x[k], y[k]);
+        }
+        float res[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if constexpr (EF) {
+            if (full) {
+                const float4 q = ld_stream(a.E[r] + e);
+                res[0] = q.x; res[1] = q.y; res[2] = q.z; res[3] = q.w;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) res[k] = valid[k] ? a.E[r][e + k] : 0.0f;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x[k] = __fadd_rn(x[k], res[k]);
+        }
+        float d[4];
+        codec<KIND>(x, valid, block_count, d);
+        if constexpr (EF) {
+            float o[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o[k] = __fsub_rn(x[k], d[k]);
+            if (full) {
+                st_stream(a.E[r] + e, make_float4(o[0], o[1], o[2], o[3]));
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) if (valid[k]) a.E[r][e + k] = o[k];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] = r == 0 ? d[k] : __fadd_rn(acc[k], d[k]);
+    }
+}
+
 template <int RC, int MC, int KIND, bool EF>
 __global__ void __launch_bounds__(kThreads) k_comp(const __grid_constant__ CompArgs a)
 {
@@ -1330,48 +1380,49 @@ __global__ void __launch_bounds__(kThreads) k_comp(const __grid_constant__ CompA
 #pragma unroll
         for (int k = 0; k < 4; ++k) valid[k] = e + k < n;
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int r = 0; r < R; ++r) {
-            float x[4];
-            // rank r's local accumulation of its micro-batches
-            for (int j = 0; j < M; ++j) {
-                float y[4];
-                if (full) {
-                    const uint2 u = ld_stream(a.g.p[r * M + j] + e);
-                    y[0] = bf16_lo(u.x); y[1] = bf16_hi(u.x); y[2] = bf16_lo(u.y); y[3] = bf16_hi(u.y);
-                } else {
+        // every rank's loads first, then the codecs and their warp reductions,
+        // so the loads are all in flight before the first sync; fp16 without
+        // error feedback has no sync and runs faster in the rank-by-rank form
+        // (fewer registers, more blocks per SM)
+        if constexpr (RC > 0 && MC > 0 && (KIND != ZERO_COMP_FP16 || EF)) {
+            if (full) {
+                uint2 gx[RC * MC];
+                float4 ex[EF ? RC : 1];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) y[k] = valid[k] ? bf16_bits(a.g.p[r * M + j][e + k]) : 0.0f;
+                for (int q = 0; q < RC * MC; ++q) gx[q] = ld_stream(a.g.p[q] + e);
+                if constexpr (EF) {
+#pragma unroll
+                    for (int r = 0; r < RC; ++r) ex[r] = ld_stream(a.E[r] + e);
                 }
 #pragma unroll
-                for (int k = 0; k < 4; ++k) x[k] = j == 0 ? y[k] : __fadd_rn(x[k], y[k]);
-            }
-            float res[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if constexpr (EF) {
-                if (full) {
-                    const float4 q = ld_stream(a.E[r] + e);
-                    res[0] = q.x; res[1] = q.y; res[2] = q.z; res[3] = q.w;
-                } else {
+                for (int r = 0; r < RC; ++r) {
+                    float x[4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) res[k] = valid[k] ? a.E[r][e + k] : 0.0f;
+                    for (int j = 0; j < MC; ++j) {
+                        const uint2 u = gx[r * MC + j];
+                        const float y[4] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y)};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) x[k] = j == 0 ? y[k] : __fadd_rn(x[k], y[k]);
+                    }
+                    if constexpr (EF) {
+                        x[0] = __fadd_rn(x[0], ex[r].x);
+                        x[1] = __fadd_rn(x[1], ex[r].y);
+                        x[2] = __fadd_rn(x[2], ex[r].z);
+                        x[3] = __fadd_rn(x[3], ex[r].w);
+                    }
+                    float d[4];
+                    codec<KIND>(x, valid, block_count, d);
+                    if constexpr (EF)
+                        st_stream(a.E[r] + e, make_float4(__fsub_rn(x[0], d[0]), __fsub_rn(x[1], d[1]),
+                                                          __fsub_rn(x[2], d[2]), __fsub_rn(x[3], d[3])));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) acc[k] = r == 0 ? d[k] : __fadd_rn(acc[k], d[k]);
                 }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) x[k] = __fadd_rn(x[k], res[k]);
+            } else {
+                comp_ranks_generic<KIND, EF>(a, R, M, e, full, valid, block_count, acc);
             }
-            float d[4];
-            codec<KIND>(x, valid, block_count, d);
-            if constexpr (EF) {
-                float o[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) o[k] = __fsub_rn(x[k], d[k]);
-                if (full) {
-                    st_stream(a.E[r] + e, make_float4(o[0], o[1], o[2], o[3]));
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) if (valid[k]) a.E[r][e + k] = o[k];
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) acc[k] = r == 0 ? d[k] : __fadd_rn(acc[k], d[k]);
+        } else {
+            comp_ranks_generic<KIND, EF>(a, R, M, e, full, valid, block_count, acc);
         }
         // the owner: average, AdamW, all-gather
         if (full) {
