@@ -270,11 +270,25 @@ def run_ours(args, rank, world, local_rank):
     variant = {"staged": z.ZERO_VARIANT_STAGED, "tma": z.ZERO_VARIANT_FUSED_TMA}.get(
         args.variant, z.ZERO_VARIANT_FUSED)
     clipped = args.variant == "clipped"
+    zero3 = args.variant == "zero3"
+    compressed = args.variant == "compressed"
     stream = torch.cuda.current_stream()
 
     ds = H.DeviceState(wl, str(dev), staged_scratch=(variant == z.ZERO_VARIANT_STAGED))
     if clipped:
         ds.step = lambda t, variant=0, flags=0: ds.step_clipped(t, args.max_norm, flags=flags)
+    elif zero3:
+        shards = torch.empty(ds.padded, dtype=torch.bfloat16, device=dev)
+        ds.step = lambda t, variant=0, flags=0: z.zero3_step(
+            ds.plan, ds.grads, ds.W, ds.m, ds.v, shards, ds.hp, t, flags=flags,
+            dev_status=ds.status)
+    elif compressed:
+        codec = {"fp16": z.ZERO_COMP_FP16, "int8": z.ZERO_COMP_INT8, "sign": z.ZERO_COMP_SIGN}[
+            args.codec]
+        resid = ([torch.zeros(wl.N, dtype=torch.float32, device=dev) for _ in range(wl.R)]
+                 if args.ef else None)
+        ds.step = lambda t, variant=0, flags=0: z.zero_step_compressed(
+            ds.plan, ds.grads, ds.W, ds.m, ds.v, ds.params, ds.hp, t, codec, resid)
     ds.fill_state_device()
     t = wl.first_step()
     while t < wl.step:                     # prior steps build the moments
@@ -324,6 +338,10 @@ def run_ours(args, rank, world, local_rank):
     value = N * args.steps * world / (total_ms / 1e3)
     if clipped:
         bpp = 2 * wl.R * wl.M + 4 + 4 + 24 + 2 * wl.R      # stash written and read back
+    elif zero3:
+        bpp = 2 * wl.R * wl.M + 24 + 2
+    elif compressed:
+        bpp = wl.bytes_per_param() + (8 * wl.R if args.ef else 0)
     elif variant in (z.ZERO_VARIANT_FUSED, z.ZERO_VARIANT_FUSED_TMA):
         bpp = wl.bytes_per_param()
     else:
@@ -338,19 +356,21 @@ def run_ours(args, rank, world, local_rank):
         peak, peak_src = 6800.0, "fallback"
     rec, _ = traffic_per_param()
     traffic = None
-    if (rec and variant == z.ZERO_VARIANT_FUSED and not clipped and rec.get("R") == wl.R
-            and rec.get("M") == wl.M):
+    if (rec and args.variant == "fused" and rec.get("R") == wl.R and rec.get("M") == wl.M):
         traffic = round(rec["dram_bytes_per_param"] * N)
     roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved_gbs / peak, 4), "traffic": traffic,
                 "peak_source": peak_src,
                 "kernel": ("clipped step (k_rs_norm, k_tree, k_clip_coef, k_adamw_ag)" if clipped
+                           else "k_fused (ZeRO-3 output)" if zero3
+                           else f"k_comp ({args.codec}{', error feedback' if args.ef else ''})"
+                           if compressed
                            else {0: "k_fused", 1: "staged trio", 2: "k_fused_tma"}[variant]),
                 "algorithmic_bytes_per_launch": alg_bytes, "bytes_per_param": bpp}
 
     # -------- end to end through the host-buffer entry point
     e2e = None
-    if not args.no_e2e and variant == z.ZERO_VARIANT_FUSED and not clipped:
+    if not args.no_e2e and args.variant == "fused":
         host_g = [torch.empty(N, dtype=torch.bfloat16, pin_memory=True) for _ in ds.grads]
         for h, d in zip(host_g, ds.grads):
             h.copy_(d[:N])
@@ -409,6 +429,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": wl.name, "N": N, "R": wl.R, "M": wl.M, "stage": wl.stage,
                    "step": wl.step, "variant": args.variant,
                    **({"max_norm": args.max_norm} if clipped else {}),
+                   **({"codec": args.codec, "error_feedback": args.ef} if compressed else {}),
                    "l2": "inputs (%.1f GB/step) far larger than the 129 MB L2; no flush"
                          % (alg_bytes / 1e9),
                    "parallelism": f"{world} independent replica(s) of an R={wl.R} "
@@ -636,7 +657,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama-3.2-1b")
-    ap.add_argument("--variant", choices=["fused", "staged", "clipped", "tma"], default="fused")
+    ap.add_argument("--variant", choices=["fused", "staged", "clipped", "tma", "zero3",
+                                          "compressed"], default="fused")
+    ap.add_argument("--codec", choices=["fp16", "int8", "sign"], default="int8",
+                    help="codec for --variant compressed")
+    ap.add_argument("--ef", action="store_true", help="error feedback for --variant compressed")
     ap.add_argument("--max-norm", type=float, default=1.0,
                     help="global-norm clip threshold for --variant clipped")
     ap.add_argument("--no-e2e", action="store_true")
