@@ -209,8 +209,9 @@ def oracle_sample_rate(wl, target_s=12.0, sample_elems=1 << 24, threads=None):
 
 
 def _tree_levels(N: int):
-    """Partial counts of the clipped step's norm tree (2048 leaves a block)."""
-    lv = [max(1, -(-N // 2048))]
+    """Partial counts of the clipped step's norm tree (256 leaves a warp in
+    the streaming pass, then 2048 partials a block)."""
+    lv = [max(1, -(-N // 256))]
     while lv[-1] > 1:
         lv.append(-(-lv[-1] // 2048))
     return lv

@@ -224,11 +224,11 @@ def test_binding_rejects_host_tensors_for_device_arguments():
 
 def test_clip_scratch_bytes_layout():
     # fp32 gradient stash (4 * padded) + one 256-byte-rounded segment per tree
-    # level (ceil(N/2048) partials, then ceil(./2048) ... down to 1) + control
+    # level (ceil(N/256) warp partials, then ceil(./2048) ... down to 1) + control
     p = z.Plan([65536], 4, 2, 1)
-    assert z.zero_clip_scratch_bytes(p) == 4 * 65536 + 256 + 256 + 256
-    p = z.Plan([1_235_814_400], 8, 1, 2)             # 603,425 -> 295 -> 1 partials
-    levels = [603_425, 295, 1]
+    assert z.zero_clip_scratch_bytes(p) == 4 * 65536 + 1024 + 256 + 256
+    p = z.Plan([1_235_814_400], 8, 1, 2)             # 4,827,400 -> 2,358 -> 2 -> 1 partials
+    levels = [4_827_400, 2_358, 2, 1]
     want = 4 * p.padded + sum(-(-4 * n // 256) * 256 for n in levels) + 256
     assert z.zero_clip_scratch_bytes(p) == want
 

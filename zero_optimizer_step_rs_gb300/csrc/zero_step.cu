@@ -924,15 +924,18 @@ extern "C" zero_status zero_step_host(const zero_plan_t* plan, const uint16_t* c
 // skip decision for a non-finite norm), and a last pass applies it with the
 // AdamW update and the R-way bf16 all-gather.
 //
-// Tree decomposition: a block reduces 2048 consecutive leaves (256 threads x
-// 8 leaves: a 3-level tree in registers, 5 levels of warp shuffles, 3 levels
-// across the 8 warps), which is exactly an aligned subtree of the global
-// tree; the next level does the same to 2048 partials at a time.  Adding a
-// zero (padding) changes no value, so the result equals the tree over the
-// leaves padded to the next power of two for any N and any grid.
+// Tree decomposition: in the streaming pass each warp reduces 256
+// consecutive leaves (32 lanes x 8 leaves: a 3-level tree in registers, then
+// 5 levels of shuffles) - exactly an aligned subtree of the global tree - and
+// writes one partial, with no block-wide barrier; each further level is a
+// block reducing 2048 partials (8 leaves per thread, the warp levels, then 3
+// levels across the 8 warps), again an aligned subtree.  Adding a zero
+// (padding) changes no value, so the result equals the tree over the leaves
+// padded to the next power of two for any N and any grid.
 namespace {
 
-constexpr int kTreeLeaves = 2048;                 // leaves per block (256 x 8)
+constexpr int kTreeLeaves = 2048;                 // leaves per tree block (256 x 8)
+constexpr int kWarpLeaves = 256;                  // leaves per warp in the streaming pass
 
 struct ClipCtl {
     double sumsq;          // squared norm (the fp32 tree value, widened)
@@ -955,7 +958,7 @@ ClipLayout clip_layout(const zero_plan_t* plan)
     ClipLayout L{};
     L.g_off = 0;
     int64_t off = round256(4 * plan->padded);
-    int64_t len = (plan->N + kTreeLeaves - 1) / kTreeLeaves;
+    int64_t len = (plan->N + kWarpLeaves - 1) / kWarpLeaves;
     if (len < 1) len = 1;
     L.levels = 0;
     while (true) {
@@ -977,6 +980,16 @@ __device__ __forceinline__ float tree8(const float (&x)[8])
 {
     return __fadd_rn(__fadd_rn(__fadd_rn(x[0], x[1]), __fadd_rn(x[2], x[3])),
                      __fadd_rn(__fadd_rn(x[4], x[5]), __fadd_rn(x[6], x[7])));
+}
+
+__device__ __forceinline__ float warp_tree(float v)
+{
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_down_sync(0xFFFFFFFFu, v, off);
+        v = __fadd_rn(v, o);           // meaningful in lanes that are multiples of 2*off
+    }
+    return v;                          // lane 0 holds the warp's subtree
 }
 
 __device__ __forceinline__ float block_tree(float v)
@@ -1004,7 +1017,7 @@ struct ClipArgs {
     GradPtrs g;
     ReplicaPtrs P;
     float* gs;             // averaged gradients (padded floats; [0, N) used)
-    float* lvl0;           // first tree level: one partial per 2048-element tile
+    float* lvl0;           // first tree level: one partial per 256 elements (per warp)
     float* W;
     float* m;
     float* v;
@@ -1050,8 +1063,9 @@ __global__ void __launch_bounds__(kThreads) k_rs_norm(const __grid_constant__ Cl
         float sq[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) sq[k] = __fmul_rn(g[k], g[k]);   // padding leaves are +0
-        const float part = block_tree(tree8(sq));
-        if (threadIdx.x == 0) a.lvl0[tile] = part;
+        const float part = warp_tree(tree8(sq));
+        const int64_t wpart = tile * (kTreeLeaves / kWarpLeaves) + (threadIdx.x >> 5);
+        if ((threadIdx.x & 31) == 0 && wpart * kWarpLeaves < n) a.lvl0[wpart] = part;
     }
 }
 
@@ -1091,43 +1105,57 @@ __global__ void k_clip_coef(const float* __restrict__ root, ClipCtl* ctl, float 
     if (sumsq_out) *sumsq_out = c.sumsq;
 }
 
-// pass 2: g' = g * coef (when clipping), AdamW, bf16 all-gather
+// pass 2: g' = g * coef (when clipping), AdamW, bf16 all-gather; tiles of
+// 256 threads x 4 elements x 2 units with every load of a tile issued first,
+// as in k_fused
 template <int RC>
 __global__ void __launch_bounds__(kThreads) k_adamw_ag(const __grid_constant__ ClipArgs a)
 {
     const ClipCtl c = *a.ctl;
     if (c.skip) return;
     const int R = RC > 0 ? RC : a.R;
+    constexpr int U = 2;
+    constexpr int T = kUnit * U;
     const int64_t n = a.n;
-    const int64_t nvec = n / kVec;
-    for (int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x; q < nvec;
-         q += (int64_t)gridDim.x * kThreads) {
-        const int64_t e = q * kVec;
-        float4 g = ld_stream(a.gs + e);
-        float4 w = ld_stream(a.W + e), m = ld_stream(a.m + e), v = ld_stream(a.v + e);
-        if (c.clip) {
-            g.x = __fmul_rn(g.x, c.coef);
-            g.y = __fmul_rn(g.y, c.coef);
-            g.z = __fmul_rn(g.z, c.coef);
-            g.w = __fmul_rn(g.w, c.coef);
-        }
-        adamw(a.s, g.x, w.x, m.x, v.x);
-        adamw(a.s, g.y, w.y, m.y, v.y);
-        adamw(a.s, g.z, w.z, m.z, v.z);
-        adamw(a.s, g.w, w.w, m.w, v.w);
-        st_stream(a.W + e, w);
-        st_stream(a.m + e, m);
-        st_stream(a.v + e, v);
-        const uint2 p = make_uint2(pack_bf16x2(w.x, w.y), pack_bf16x2(w.z, w.w));
-        if constexpr (RC > 0) {
+    const int64_t full_tiles = n / T;
+    for (int64_t tile = blockIdx.x; tile < full_tiles; tile += gridDim.x) {
+        const int64_t e0 = tile * T + (int64_t)threadIdx.x * kVec;
+        float4 g[U], w[U], m[U], v[U];
 #pragma unroll
-            for (int r = 0; r < RC; ++r) st_stream(a.P.p[r] + e, p);
-        } else {
-            for (int r = 0; r < R; ++r) st_stream(a.P.p[r] + e, p);
+        for (int u = 0; u < U; ++u) {
+            const int64_t e = e0 + (int64_t)u * kUnit;
+            g[u] = ld_stream(a.gs + e);
+            w[u] = ld_stream(a.W + e);
+            m[u] = ld_stream(a.m + e);
+            v[u] = ld_stream(a.v + e);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t e = e0 + (int64_t)u * kUnit;
+            float* gp = &g[u].x;
+            float* wp = &w[u].x;
+            float* mp = &m[u].x;
+            float* vp = &v[u].x;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float gk = c.clip ? __fmul_rn(gp[k], c.coef) : gp[k];
+                adamw(a.s, gk, wp[k], mp[k], vp[k]);
+            }
+            st_stream(a.W + e, w[u]);
+            st_stream(a.m + e, m[u]);
+            st_stream(a.v + e, v[u]);
+            const uint2 p = make_uint2(pack_bf16x2(w[u].x, w[u].y), pack_bf16x2(w[u].z, w[u].w));
+            if constexpr (RC > 0) {
+#pragma unroll
+                for (int r = 0; r < RC; ++r) st_stream(a.P.p[r] + e, p);
+            } else {
+                for (int r = 0; r < R; ++r) st_stream(a.P.p[r] + e, p);
+            }
         }
     }
-    if (blockIdx.x == 0) {
-        for (int64_t i = nvec * kVec + threadIdx.x; i < n; i += kThreads) {
+    const int64_t tail0 = full_tiles * T;
+    if (tail0 < n && blockIdx.x == (unsigned)(full_tiles % gridDim.x)) {
+        for (int64_t i = tail0 + threadIdx.x; i < n; i += kThreads) {
             float g = a.gs[i];
             if (c.clip) g = __fmul_rn(g, c.coef);
             float w = a.W[i], m = a.m[i], v = a.v[i];
@@ -1162,7 +1190,7 @@ cudaError_t launch_rs_norm(const ClipArgs& a, cudaStream_t st)
 
 cudaError_t launch_adamw_ag(const ClipArgs& a, cudaStream_t st)
 {
-    const int64_t work = (a.n / kVec + kThreads - 1) / kThreads;
+    const int64_t work = (a.n + 2 * kUnit - 1) / (2 * kUnit);     // tiles of 2 units
     auto go = [&](const void* k, auto kern) {
         kern<<<grid_for(k, work < 1 ? 1 : work), kThreads, 0, st>>>(a);
         return cudaGetLastError();
