@@ -25,7 +25,10 @@
 // 256 threads x 4 elements x U units per block (grid-stride over tiles);
 // the last partial tile is done element by element.  The staged kernels
 // give each rank r its own grid row (blockIdx.y = r) and grid-stride over
-// the vectors of shard r, as rank r would on its own GPU.
+// shard r, as rank r would on its own GPU: k_rs_avg over tiles of one or two
+// units from the shard start, k_adamw over 4-vectors, k_ag_cast over
+// 8-element vectors that start on the shard's first multiple of 8 (one
+// 16-byte store per replica), with the head and tail done element by element.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -419,23 +422,32 @@ __global__ void __launch_bounds__(kThreads) k_rs_avg(const __grid_constant__ Sta
     const int M = MC > 0 ? MC : a.M;
     const int r = blockIdx.y;
     const int64_t lo = (int64_t)r * a.S, len = shard_len(a.n, a.S, r);
-    const int64_t nvec = len / kVec;
+    // two units per tile while R*M is small; with many source buffers one
+    // unit already keeps R*M loads in flight per thread
+    constexpr int U = (RC > 0 && RC * MC <= 16) ? 2 : 1;
+    constexpr int T = kUnit * U;              // tiles of U*1024 elements from the shard start
+    const int64_t full_tiles = len / T;
     bool bad = false;
-    for (int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x; q < nvec;
-         q += (int64_t)gridDim.x * kThreads) {
-        const int64_t e = lo + q * kVec;
-        float acc[4];
-        grad_sum4<RC, MC>(a.g, R, M, e, acc);
-        float4 o;
-        o.x = scale_grad(a.s, acc[0]);
-        o.y = scale_grad(a.s, acc[1]);
-        o.z = scale_grad(a.s, acc[2]);
-        o.w = scale_grad(a.s, acc[3]);
-        if (CHECK) bad |= !(isfinite(o.x) && isfinite(o.y) && isfinite(o.z) && isfinite(o.w));
-        st_stream(a.gs_out + e, o);
+    for (int64_t tile = blockIdx.x; tile < full_tiles; tile += gridDim.x) {
+        const int64_t e0 = lo + tile * T + (int64_t)threadIdx.x * kVec;
+        float acc[U][4];
+#pragma unroll
+        for (int u = 0; u < U; ++u) grad_sum4<RC, MC>(a.g, R, M, e0 + (int64_t)u * kUnit, acc[u]);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float4 o;
+            o.x = scale_grad(a.s, acc[u][0]);
+            o.y = scale_grad(a.s, acc[u][1]);
+            o.z = scale_grad(a.s, acc[u][2]);
+            o.w = scale_grad(a.s, acc[u][3]);
+            if (CHECK) bad |= !(isfinite(o.x) && isfinite(o.y) && isfinite(o.z) && isfinite(o.w));
+            st_stream(a.gs_out + e0 + (int64_t)u * kUnit, o);
+        }
     }
-    if (blockIdx.x == 0) {
-        for (int64_t i = lo + nvec * kVec + threadIdx.x; i < lo + len; i += kThreads) {
+    // the shard's last partial tile, element by element, by the block that owns it
+    const int64_t tail0 = lo + full_tiles * T;
+    if (tail0 < lo + len && blockIdx.x == (unsigned)(full_tiles % gridDim.x)) {
+        for (int64_t i = tail0 + threadIdx.x; i < lo + len; i += kThreads) {
             const float g = scale_grad(a.s, grad_sum1(a.g, R, M, i));
             if (CHECK) bad |= !isfinite(g);
             a.gs_out[i] = g;
@@ -476,35 +488,48 @@ __global__ void __launch_bounds__(kThreads) k_adamw(const __grid_constant__ Stag
 template <int RC>
 __global__ void __launch_bounds__(kThreads) k_ag_cast(const __grid_constant__ StagedArgs a)
 {
+    // 8 elements per thread: two float4 loads of W, one 16-byte store per
+    // replica.  A shard starts on a multiple of 4 elements only, so the vector
+    // loop starts at the shard's first multiple of 8; the head before it and
+    // the tail after the last full vector are done element by element.
     const int R = RC > 0 ? RC : a.R;
     const int r = blockIdx.y;
     const int64_t lo = (int64_t)r * a.S, len = shard_len(a.n, a.S, r);
-    const int64_t nvec = len / kVec;
-    for (int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x; q < nvec;
+    const int64_t hi = lo + len;
+    const int64_t v0 = (lo + 7) / 8 * 8;                  // first 8-aligned element
+    const int64_t n8 = hi > v0 ? (hi - v0) / 8 : 0;
+    for (int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x; q < n8;
          q += (int64_t)gridDim.x * kThreads) {
-        const int64_t e = lo + q * kVec;
-        const float4 w = ld_stream(a.W + e);
-        const uint2 p = make_uint2(pack_bf16x2(w.x, w.y), pack_bf16x2(w.z, w.w));
+        const int64_t e = v0 + q * 8;
+        const float4 w0 = ld_stream(a.W + e), w1 = ld_stream(a.W + e + 4);
+        const uint4 p = make_uint4(pack_bf16x2(w0.x, w0.y), pack_bf16x2(w0.z, w0.w),
+                                   pack_bf16x2(w1.x, w1.y), pack_bf16x2(w1.z, w1.w));
         if constexpr (RC > 0) {
 #pragma unroll
-            for (int k = 0; k < RC; ++k) st_stream(a.P.p[k] + e, p);
+            for (int k = 0; k < RC; ++k) __stcs(reinterpret_cast<uint4*>(a.P.p[k] + e), p);
         } else {
-            for (int k = 0; k < R; ++k) st_stream(a.P.p[k] + e, p);
+            for (int k = 0; k < R; ++k) __stcs(reinterpret_cast<uint4*>(a.P.p[k] + e), p);
         }
     }
     if (blockIdx.x == 0) {
-        for (int64_t i = lo + nvec * kVec + threadIdx.x; i < lo + len; i += kThreads) {
+        const int64_t head_end = v0 < hi ? v0 : hi;
+        for (int64_t i = lo + threadIdx.x; i < head_end; i += kThreads) {
+            const uint16_t p = to_bf16(a.W[i]);
+            for (int k = 0; k < R; ++k) a.P.p[k][i] = p;
+        }
+        for (int64_t i = v0 + n8 * 8 + threadIdx.x; i < hi; i += kThreads) {
             const uint16_t p = to_bf16(a.W[i]);
             for (int k = 0; k < R; ++k) a.P.p[k][i] = p;
         }
     }
 }
 
+
 template <bool CHECK>
 cudaError_t launch_rs(const StagedArgs& a, cudaStream_t st)
 {
     const int R = a.R, M = a.M;
-    const int64_t work = (a.S / kVec + kThreads - 1) / kThreads;
+    const int64_t work = (a.S + kUnit - 1) / kUnit;      // at most one block per unit of a shard
     auto go = [&](const void* k, auto kern) {
         const int64_t per_rank = ((int64_t)grid_for(k, work * a.R) + a.R - 1) / a.R;
         dim3 grid((unsigned)(per_rank < 1 ? 1 : per_rank), (unsigned)a.R);
@@ -533,7 +558,7 @@ cudaError_t launch_adamw(const StagedArgs& a, cudaStream_t st)
 
 cudaError_t launch_ag(const StagedArgs& a, cudaStream_t st)
 {
-    const int64_t work = (a.S / kVec + kThreads - 1) / kThreads;
+    const int64_t work = (a.S / 8 + kThreads - 1) / kThreads;
     auto go = [&](const void* k, auto kern) {
         const int64_t per_rank = ((int64_t)grid_for(k, work * a.R) + a.R - 1) / a.R;
         dim3 grid((unsigned)(per_rank < 1 ? 1 : per_rank), (unsigned)a.R);
