@@ -9,7 +9,7 @@ it; the seeded input generator ``zgen`` is the only module both sides use.
 The arithmetic lives in ``zero_oracle.c`` (plain C11, one float operation at
 a time, no FMA contraction); this file only builds it with gcc and marshals
 numpy arrays.  See ``zero_oracle.h`` for the passages each function follows
-and for the readings R1-R9 taken where the pages leave a step open.
+and for the readings R1-R15 taken where the pages leave a step open.
 """
 from __future__ import annotations
 
@@ -128,6 +128,9 @@ def lib():
             L.oracle_dp_step_compressed.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp,
                                                     ctypes.POINTER(HParams), i64, i32, vp]
             L.oracle_dp_step_compressed.restype = ctypes.c_int
+            L.oracle_onebit_step.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp,
+                                             ctypes.POINTER(HParams), i64, i64, vp, vp]
+            L.oracle_onebit_step.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -359,3 +362,24 @@ def dp_step_compressed(G, W, m, v, P, hp: HParams, step: int, R: int, M: int, ki
                                          ctypes.addressof(ea) if ea is not None else None)
     if rc != 0:
         raise RuntimeError(f"oracle_dp_step_compressed failed: {rc}")
+
+
+def onebit_step(G, W, m, v, P, hp: HParams, step: int, freeze_step: int, R: int, M: int,
+                S: int, E, Es) -> None:
+    """1-bit Adam step (reading R15) on numpy arrays of n elements each;
+    E (R arrays) and Es are updated in place after the warm-up."""
+    n = W.size
+    for k, g in enumerate(G):
+        _check(g, np.uint16, n, f"G[{k}]")
+    for k, p in enumerate(P):
+        _check(p, np.uint16, n, f"P[{k}]")
+    for nm, a in (("W", W), ("m", m), ("v", v), ("Es", Es)):
+        _check(a, np.float32, n, nm)
+    for k, e in enumerate(E):
+        _check(e, np.float32, n, f"E[{k}]")
+    ga, pa, ea = _ptr_array(G), _ptr_array(P), _ptr_array(E)
+    rc = lib().oracle_onebit_step(n, S, R, M, ctypes.addressof(ga), _ptr(W), _ptr(m), _ptr(v),
+                                  ctypes.addressof(pa), ctypes.byref(hp), step, freeze_step,
+                                  ctypes.addressof(ea), _ptr(Es))
+    if rc != 0:
+        raise RuntimeError(f"oracle_onebit_step failed: {rc}")

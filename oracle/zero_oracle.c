@@ -2,7 +2,7 @@
  * zero_oracle.c - CPU oracle for the ZeRO-1/2 mixed-precision AdamW step.
  *
  * TEST INFRASTRUCTURE, NOT PRODUCT CODE (see zero_oracle.h for who may load
- * it, the passages each function follows and the readings R1-R9).
+ * it, the passages each function follows and the readings R1-R15).
  *
  * Build: gcc -std=c11 -O2 -ffp-contract=off -fno-fast-math -fPIC -shared
  * (-ffp-contract=off keeps every float * and + separately rounded, which is
@@ -27,6 +27,12 @@
  *   oracle_zero_bytes      the pages' exercises (7B/8 ranks, 7.5B/64 ranks,
  *                          p=8 per-card units)
  *   oracle_shard_len       hand-computed layouts (uneven 100,000,007 / 7)
+ *   oracle_onebit_step     (tests/test_oracle_onebit.py) warm-up == the
+ *                          plain step; a hand-worked two-rank example; the
+ *                          plain step whenever the sign codec is lossless
+ *                          and beta2 = 0; a closed form for the frozen
+ *                          preconditioner; codec and error-feedback
+ *                          invariants on random inputs
  */
 #define _POSIX_C_SOURCE 200809L
 #include "zero_oracle.h"
@@ -609,5 +615,80 @@ int oracle_dp_step_compressed(int64_t n, int32_t R, int32_t M,
     free(x);
     free(d);
     free(acc);
+    return 0;
+}
+
+/* ------------------------------------------------------------ 1-bit Adam -- */
+
+/* Reading R15 (zero_oracle.h).  The warm-up is the plain step; afterwards
+ * the ranks' local momenta are sign-compressed with error feedback, the
+ * owner averages them and compresses its shard again with its own error
+ * feedback, and the update divides by the frozen preconditioner.  Names
+ * follow R15: xr/dr a worker's input and decompressed message, y/ds the
+ * server's. */
+int oracle_onebit_step(int64_t n, int64_t S, int32_t R, int32_t M,
+                       const uint16_t* const* G, float* W, float* m, float* v,
+                       uint16_t* const* P, const oracle_hparams* hp, int64_t step,
+                       int64_t freeze_step, float* const* E, float* Es)
+{
+    if (freeze_step < 1 || S < 1 || !E || !Es) return -1;
+    if (n > 0 && S * (int64_t)R < n) return -1;
+    if (step <= freeze_step)
+        return oracle_dp_step(n, R, M, G, W, m, v, P, hp, step);
+    if (check_args(n, R, M, G, W, m, v, P, hp, step)) return -1;
+    oracle_scalars s;            /* beta1 and lr's bias correction at t */
+    oracle_scalars sf;           /* the frozen bias correction of v, at T_w */
+    oracle_make_scalars(hp, step, R, M, &s);
+    oracle_make_scalars(hp, freeze_step, R, M, &sf);
+    size_t nn = (size_t)(n > 0 ? n : 1);
+    float* xr = (float*)malloc(sizeof(float) * nn);
+    float* dr = (float*)malloc(sizeof(float) * nn);
+    float* dsum = (float*)malloc(sizeof(float) * nn);
+    if (!xr || !dr || !dsum) { free(xr); free(dr); free(dsum); return -2; }
+    float denom_m = (float)M, denom_r = (float)R;
+    for (int32_t r = 0; r < R; ++r) {
+        /* worker r: local momentum, error feedback, 1-bit compression */
+        for (int64_t i = 0; i < n; ++i) {
+            float loc = oracle_bf16_to_float(G[(int64_t)r * M][i]);
+            for (int32_t j = 1; j < M; ++j)
+                loc = loc + oracle_bf16_to_float(G[(int64_t)r * M + j][i]);
+            float gl = loc / denom_m;
+            float ml = s.beta1 * m[i] + s.one_minus_beta1 * gl;
+            xr[i] = ml + E[r][i];
+        }
+        oracle_compress(ORACLE_COMP_SIGN, xr, n, dr);
+        for (int64_t i = 0; i < n; ++i) {
+            E[r][i] = xr[i] - dr[i];
+            dsum[i] = (r == 0) ? dr[i] : dsum[i] + dr[i];
+        }
+    }
+    /* server: the owner of each shard averages, adds its residual and
+     * compresses again, blocks counted from the shard's start */
+    float* y = xr;
+    float* ds = dr;
+    for (int64_t i = 0; i < n; ++i) y[i] = dsum[i] / denom_r + Es[i];
+    for (int32_t r = 0; r < R; ++r) {
+        int64_t lo = (int64_t)r * S;
+        if (lo >= n) break;
+        int64_t len = n - lo < S ? n - lo : S;
+        oracle_compress(ORACLE_COMP_SIGN, y + lo, len, ds + lo);
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        Es[i] = y[i] - ds[i];
+        float mi = ds[i];
+        float wd = W[i] * s.decay;
+        float root = sqrtf(v[i]);
+        float q = root / sf.bc2_sqrt;
+        float den = q + s.eps;
+        float ratio = mi / den;
+        float upd = s.step_size * ratio;
+        W[i] = wd - upd;
+        m[i] = mi;
+        uint16_t p = oracle_bf16_rne(W[i]);
+        for (int32_t r = 0; r < R; ++r) P[r][i] = p;
+    }
+    free(xr);
+    free(dr);
+    free(dsum);
     return 0;
 }

@@ -269,6 +269,47 @@ int oracle_dp_step_compressed(int64_t n, int32_t R, int32_t M,
                               uint16_t* const* P, const oracle_hparams* hp,
                               int64_t step, int32_t kind, float* const* E);
 
+/* ------------------------------------------------------------------------
+ * 1-bit Adam (CS324 Lecture 9 notes, section 7.4: error feedback alone
+ * does not carry over to Adam, because Adam is a non-linear function of the
+ * gradient; the remedy is to warm up with plain Adam, then freeze the
+ * variance into a fixed preconditioner and compress the communication to
+ * 1 bit).
+ * Reading R15 (the pages give the idea, not the formulas):
+ *   - steps t <= T_w (the warm-up) are the plain step of oracle_dp_step,
+ *     v is updated there, and the residuals are not touched;
+ *   - at t > T_w, for each rank r and element i:
+ *       gl_r = (sum_j G[r][j][i]) / (float)M       local average, j ascending
+ *       ml_r = beta1*m[i] + (1-beta1)*gl_r          local momentum
+ *       x_r  = ml_r + E[r][i]                       worker error feedback
+ *       d_r  = sign codec of x_r over aligned 128-element blocks of the flat
+ *              vector (R14's sign codec); E[r][i] = x_r - d_r
+ *     and the owner of element i (rank i / S):
+ *       a    = (((d_0 + d_1) + ...) + d_{R-1}) / (float)R
+ *       y    = a + Es[i]                            server error feedback
+ *       ds   = sign codec of y over blocks of 128 elements counted from the
+ *              start of the owner's shard (the last block of a shard may be
+ *              short); Es[i] = y - ds
+ *       m[i] = ds                                   the momentum every rank
+ *                                                   decompresses
+ *       W[i] = W[i]*(1-lr*wd) - (lr/(1-beta1^t)) * (ds / den),
+ *       den  = sqrt(v[i]) / sqrt(1-beta2^T_w) + eps
+ *     v is not written: the frozen preconditioner is v and its bias
+ *     correction as they stood at the end of the warm-up.  Every float
+ *     operation is rounded on its own (R2); the replicas receive bf16(W).
+ * ---------------------------------------------------------------------- */
+
+/* One step of 1-bit Adam in the ZeRO layout.  S: shard length (the owner's
+ * blocks start at multiples of S).  E: R pointers to n fp32 worker
+ * residuals; Es: n fp32 server residuals (index i for element i); both are
+ * updated in place at t > freeze_step and start at zero.  freeze_step >= 1.
+ * v is updated in the warm-up only.
+ * Returns 0, -1 (bad arguments) or -2 (allocation failure). */
+int oracle_onebit_step(int64_t n, int64_t S, int32_t R, int32_t M,
+                       const uint16_t* const* G, float* W, float* m, float* v,
+                       uint16_t* const* P, const oracle_hparams* hp, int64_t step,
+                       int64_t freeze_step, float* const* E, float* Es);
+
 #ifdef __cplusplus
 }
 #endif

@@ -67,6 +67,17 @@ MUTANTS = {
                       "float s = abs_tree(xb, cnt, 0, ORACLE_COMP_BLOCK) / (float)ORACLE_COMP_BLOCK;"),
     "ef_sign_flipped": ("if (E) E[r][i] = x[i] - d[i];", "if (E) E[r][i] = d[i] - x[i];"),
     "ef_not_added": ("x[i] = E ? loc + E[r][i] : loc;", "x[i] = E ? loc + 0.0f * E[r][i] : loc;"),
+    "onebit_warmup_off_by_one": ("if (step <= freeze_step)", "if (step < freeze_step)"),
+    "onebit_local_mean_not_divided": ("float gl = loc / denom_m;", "float gl = loc + 0.0f * denom_m;"),
+    "onebit_momentum_from_grad_only": ("float ml = s.beta1 * m[i] + s.one_minus_beta1 * gl;",
+                                       "float ml = 0.0f * m[i] + s.one_minus_beta1 * gl;"),
+    "onebit_worker_ef_sign": ("E[r][i] = xr[i] - dr[i];", "E[r][i] = dr[i] - xr[i];"),
+    "onebit_no_server_ef": ("y[i] = dsum[i] / denom_r + Es[i];", "y[i] = dsum[i] / denom_r + 0.0f * Es[i];"),
+    "onebit_server_ef_sign": ("Es[i] = y[i] - ds[i];", "Es[i] = ds[i] - y[i];"),
+    "onebit_global_server_blocks": ("oracle_compress(ORACLE_COMP_SIGN, y + lo, len, ds + lo);",
+                                    "if (r == 0) oracle_compress(ORACLE_COMP_SIGN, y, n + 0 * len, ds);"),
+    "onebit_update_skips_server_codec": ("float mi = ds[i];", "float mi = dsum[i] / denom_r;"),
+    "onebit_bias_correction_at_t": ("float q = root / sf.bc2_sqrt;", "float q = root / s.bc2_sqrt;"),
 }
 
 
@@ -85,6 +96,6 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         "tests/test_oracle_pins.py", "tests/test_oracle_collectives.py",
                         "tests/test_oracle_clip.py", "tests/test_oracle_zero3.py",
-                        "tests/test_oracle_compress.py"],
+                        "tests/test_oracle_compress.py", "tests/test_oracle_onebit.py"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
