@@ -273,6 +273,10 @@ def run_ours(args, rank, world, local_rank):
     clipped = args.variant == "clipped"
     zero3 = args.variant == "zero3"
     compressed = args.variant == "compressed"
+    onebit = args.variant == "onebit"
+    if onebit:                             # 1-bit Adam wants shards on the 128-element block grid
+        import dataclasses
+        wl = dataclasses.replace(wl, align=128)
     stream = torch.cuda.current_stream()
 
     ds = H.DeviceState(wl, str(dev), staged_scratch=(variant == z.ZERO_VARIANT_STAGED))
@@ -290,6 +294,14 @@ def run_ours(args, rank, world, local_rank):
                  if args.ef else None)
         ds.step = lambda t, variant=0, flags=0: z.zero_step_compressed(
             ds.plan, ds.grads, ds.W, ds.m, ds.v, ds.params, ds.hp, t, codec, resid)
+    elif onebit:
+        # freeze before the measured step, so every warm-up and timed step is
+        # a compressed one
+        freeze = max(1, wl.step - 1)
+        w_res = [torch.zeros(wl.N, dtype=torch.float32, device=dev) for _ in range(wl.R)]
+        s_res = torch.zeros(ds.padded, dtype=torch.float32, device=dev)
+        ds.step = lambda t, variant=0, flags=0: z.zero_step_onebit(
+            ds.plan, ds.grads, ds.W, ds.m, ds.v, ds.params, ds.hp, t, freeze, w_res, s_res)
     ds.fill_state_device()
     t = wl.first_step()
     while t < wl.step:                     # prior steps build the moments
@@ -343,6 +355,8 @@ def run_ours(args, rank, world, local_rank):
         bpp = 2 * wl.R * wl.M + 24 + 2
     elif compressed:
         bpp = wl.bytes_per_param() + (8 * wl.R if args.ef else 0)
+    elif onebit:
+        bpp = 2 * wl.R * wl.M + 10 * wl.R + 28
     elif variant in (z.ZERO_VARIANT_FUSED, z.ZERO_VARIANT_FUSED_TMA):
         bpp = wl.bytes_per_param()
     else:
@@ -366,6 +380,7 @@ def run_ours(args, rank, world, local_rank):
                            else "k_fused (ZeRO-3 output)" if zero3
                            else f"k_comp ({args.codec}{', error feedback' if args.ef else ''})"
                            if compressed
+                           else "k_onebit (1-bit Adam, frozen variance)" if onebit
                            else {0: "k_fused", 1: "staged trio", 2: "k_fused_tma"}[variant]),
                 "algorithmic_bytes_per_launch": alg_bytes, "bytes_per_param": bpp}
 
@@ -431,6 +446,7 @@ def run_ours(args, rank, world, local_rank):
                    "step": wl.step, "variant": args.variant,
                    **({"max_norm": args.max_norm} if clipped else {}),
                    **({"codec": args.codec, "error_feedback": args.ef} if compressed else {}),
+                   **({"freeze_step": max(1, wl.step - 1), "align": 128} if onebit else {}),
                    "l2": "inputs (%.1f GB/step) far larger than the 129 MB L2; no flush"
                          % (alg_bytes / 1e9),
                    "parallelism": f"{world} independent replica(s) of an R={wl.R} "
@@ -598,6 +614,39 @@ def run_table(args):
     del ds, res
     torch.cuda.empty_cache()
 
+    # 1-bit Adam after its warm-up on the 1B-shaped workload (shards on the
+    # 128-element block grid)
+    import dataclasses
+    wl = dataclasses.replace(W.llama32_1b(), align=128)
+    ds = H.DeviceState(wl, staged_scratch=False)
+    ds.fill_state_device()
+    ds.fill_grads_device(wl.step)
+    w_res = [torch.zeros(wl.N, dtype=torch.float32, device="cuda") for _ in range(wl.R)]
+    s_res = torch.zeros(ds.padded, dtype=torch.float32, device="cuda")
+    ts, t = [], wl.step
+    for k in range(3 + 10):
+        flush.fill_(k & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        z.zero_step_onebit(ds.plan, ds.grads, ds.W, ds.m, ds.v, ds.params, ds.hp, t, wl.step - 1,
+                           w_res, s_res)
+        e1.record()
+        torch.cuda.synchronize()
+        t += 1
+        if k >= 3:
+            ts.append(e0.elapsed_time(e1))
+    ms = float(np.median(ts))
+    b = 2 * wl.R * wl.M + 10 * wl.R + 28
+    row = {"workload": "llama-3.2-1b", "R": wl.R, "M": wl.M, "N": wl.N, "variant": "onebit",
+           "wire_bytes_per_param_per_rank": round(2 * (1 / 8 + 4 / 128), 4),
+           "ms": round(ms, 4), "params_per_s": wl.N / (ms / 1e3), "bytes_per_param": b,
+           "GB_s": round(b * wl.N / (ms / 1e3) / 1e9, 1),
+           "frac_of_measured_peak": round(b * wl.N / (ms / 1e3) / 1e9 / peak, 4)}
+    rows.append(row)
+    print(json.dumps(row), flush=True)
+    del ds, w_res, s_res
+    torch.cuda.empty_cache()
+
     for R in (2, 4, 8):
         S = 1024
         while S <= 256 * 1024 * 1024:
@@ -659,7 +708,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama-3.2-1b")
     ap.add_argument("--variant", choices=["fused", "staged", "clipped", "tma", "zero3",
-                                          "compressed"], default="fused")
+                                          "compressed", "onebit"], default="fused")
     ap.add_argument("--codec", choices=["fp16", "int8", "sign"], default="int8",
                     help="codec for --variant compressed")
     ap.add_argument("--ef", action="store_true", help="error feedback for --variant compressed")

@@ -290,6 +290,40 @@ zero_status zero_step_compressed(const zero_plan_t* plan, const uint16_t* const*
                                  float* const* residuals, void* stream);
 
 /*
+ * 1-bit Adam step (CS324 Lecture 9 notes, section 7.4: error feedback alone
+ * does not carry over to Adam, so warm up with plain Adam, then freeze the
+ * variance into a fixed preconditioner and send 1 bit per value).
+ *   step <= freeze_step (the warm-up): exactly zero_step's fused step; v is
+ *     updated and the residuals are not touched.
+ *   step > freeze_step, for every element i and rank r:
+ *     gl_r = (sum_j G[r][j][i]) / M;  x_r = beta1*m[i] + (1-beta1)*gl_r + E_r[i]
+ *     d_r  = sign codec of x_r (ZERO_COMP_SIGN, 128-element blocks of the
+ *            flat vector);  E_r[i] = x_r - d_r
+ *     y    = (d_0 + ... + d_{R-1}) / R + Es[i]   (ranks ascending)
+ *     ds   = sign codec of y over the same blocks, which lie inside one
+ *            owner's shard;  Es[i] = y - ds;  m[i] = ds
+ *     W[i] = W[i]*(1-lr*wd) - lr/(1-beta1^t) * ds / (sqrt(v[i]) /
+ *            sqrt(1-beta2^freeze_step) + eps);  v is read, not written;
+ *     every replica receives bf16(W[i]).
+ *   Each float operation is rounded on its own.
+ *   freeze_step  >= 1, else ZERO_ERR_INVALID_ARG.
+ *   plan->S      must be a multiple of 128 (make the plan with align_elems
+ *                a multiple of 128) so that every owner's compression block
+ *                is a block of the flat vector; else ZERO_ERR_INVALID_ARG.
+ *   worker_residuals  host array of R device pointers, N floats each
+ *                (16-byte aligned), read and updated in place; start at 0.
+ *   server_residual   device, plan->padded floats in the state layout
+ *                (element i at index i, the pad never touched); start at 0.
+ * Traffic after the warm-up: 2RM + 10R + 28 bytes/param (grads 2RM, worker
+ * residuals 8R, replicas 2R, W/m/Es read and written 24, v read 4).
+ */
+zero_status zero_step_onebit(const zero_plan_t* plan, const uint16_t* const* rank_grads,
+                             float* master, float* m, float* v, uint16_t* const* rank_params,
+                             const zero_adamw_hparams* hp, int64_t step, int64_t freeze_step,
+                             float* const* worker_residuals, float* server_residual,
+                             void* stream);
+
+/*
  * ZeRO-3 step (CS25 V6 Lecture 4 notes, "ZeRO-3 / FSDP": the parameters are
  * sharded as well and materialised per unit just before use; CS324 Lecture
  * 9 notes, section 3.4: bit-identical to plain DP).  The reduce-scatter,

@@ -267,3 +267,35 @@ def test_tma_variant_argument_errors(plan):
     big = z.Plan([1000], 16, 2, 2)                     # R*M = 32 > 16
     g2, Wp2, mp2, vp2, P2, _, _ = fake_bufs(big)
     assert call_step(big, g2, Wp2, mp2, vp2, P2, variant=2) == B.ZERO_ERR_INVALID_ARG
+
+
+def test_onebit_argument_errors():
+    import ctypes
+    plan = z.Plan([100_000], 4, 2, 2, 128)
+    g, Wp, mp, vp, P, scr, st = fake_bufs(plan)
+    E = [BASE + (1 << 36) + k * (1 << 30) for k in range(plan.R)]
+    L = B.lib()
+
+    def call(pl=plan, step=3, freeze=2, worker=E, server=scr, hp=None):
+        ga, pa = B._ptrs(g), B._ptrs(P)
+        ea = B._ptrs(worker) if worker is not None else None
+        hp = hp if hp is not None else z.hparams()
+        return L.zero_step_onebit(pl.ptr, ctypes.addressof(ga), Wp, mp, vp,
+                                  ctypes.addressof(pa), ctypes.byref(hp), step, freeze,
+                                  ctypes.addressof(ea) if ea is not None else None, server, None)
+    assert call(freeze=0) == B.ZERO_ERR_INVALID_ARG
+    assert call(step=0) == B.ZERO_ERR_INVALID_ARG
+    assert call(hp=z.hparams(beta2=1.0)) == B.ZERO_ERR_INVALID_ARG
+    # S = 25,024 with the default 64-element alignment: not a multiple of 128
+    assert plan.S % 128 == 0
+    assert call(pl=z.Plan([100_000], 4, 2, 2)) == B.ZERO_ERR_INVALID_ARG
+    assert call(worker=None) == B.ZERO_ERR_NULL
+    assert call(server=None) == B.ZERO_ERR_NULL
+    assert call(server=scr + 8) == B.ZERO_ERR_ALIGN
+    assert call(worker=E[:-1] + [0]) == B.ZERO_ERR_NULL
+    assert call(worker=[E[0] + 4] + E[1:]) == B.ZERO_ERR_ALIGN
+    # overlaps are checked before the first launch
+    assert call(server=Wp) == B.ZERO_ERR_OVERLAP
+    assert call(worker=[g[0]] + E[1:]) == B.ZERO_ERR_OVERLAP
+    assert call(worker=[E[0], E[0]] + E[2:]) == B.ZERO_ERR_OVERLAP
+    assert call(worker=[P[1]] + E[1:]) == B.ZERO_ERR_OVERLAP

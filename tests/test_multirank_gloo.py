@@ -45,7 +45,7 @@ def _worker(rank, world, port, out):
 def test_two_gloo_ranks_max_and_single_printer():
     world = 2
     port = _free_port()
-    manager = mp.Manager()
+    manager = mp.get_context("spawn").Manager()      # no fork of a threaded process
     out = manager.dict()
     mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
     assert out[0][0] == out[1][0] == 13.5

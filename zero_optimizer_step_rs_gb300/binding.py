@@ -47,7 +47,7 @@ EXPORTED = ("zero_abi_version", "zero_status_string", "zero_plan_create", "zero_
             "zero_step_host", "zero_step_staged_noalloc", "zero_step_clipped",
             "zero_clip_scratch_bytes", "zero3_step", "zero3_gather", "zero_ckpt_write_host",
             "zero_ckpt_read_host", "zero_ckpt_save_async", "zero_ckpt_job_wait",
-            "zero_ckpt_load", "zero_step_compressed", "zero_check_replicas")
+            "zero_ckpt_load", "zero_step_compressed", "zero_check_replicas", "zero_step_onebit")
 
 
 class ZeroError(RuntimeError):
@@ -139,6 +139,9 @@ def lib():
         L.zero_step_compressed.restype = ctypes.c_int
         L.zero_check_replicas.argtypes = [P(zero_plan_t), vp, vp, vp, vp]
         L.zero_check_replicas.restype = ctypes.c_int
+        L.zero_step_onebit.argtypes = [P(zero_plan_t), vp, vp, vp, vp, vp,
+                                       P(zero_adamw_hparams), i64, i64, vp, vp, vp]
+        L.zero_step_onebit.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -543,3 +546,32 @@ def zero_check_replicas(plan: Plan, rank_params, dev_count, dev_first=None, stre
     pa = _ptrs([_addr(p) for p in rank_params])
     _check(lib().zero_check_replicas(plan.ptr, ctypes.addressof(pa), _addr(dev_count),
                                      _addr(dev_first), _stream(stream)), "zero_check_replicas")
+
+
+def zero_step_onebit(plan: Plan, rank_grads, master, m, v, rank_params,
+                     hp: zero_adamw_hparams, step: int, freeze_step: int, worker_residuals,
+                     server_residual, stream=None) -> None:
+    """1-bit Adam: the plain step while step <= freeze_step, then the
+    sign-compressed momentum exchange with worker and owner error feedback
+    and a frozen variance.  worker_residuals: R float32 device tensors of N;
+    server_residual: a float32 device tensor of plan.padded.  The plan's
+    shard length must be a multiple of 128 (align_elems a multiple of 128)."""
+    c = plan.c
+    for k, g in enumerate(rank_grads):
+        _check_tensor(g, "bf16", c.N, f"rank_grads[{k}]")
+    for k, p in enumerate(rank_params):
+        _check_tensor(p, "bf16", c.N, f"rank_params[{k}]")
+    for nm, t in (("master", master), ("m", m), ("v", v), ("server_residual", server_residual)):
+        _check_tensor(t, "f32", c.padded, nm)
+    if len(rank_grads) != c.R * c.M or len(rank_params) != c.R:
+        raise ValueError(f"need {c.R * c.M} gradient buffers and {c.R} replicas")
+    if len(worker_residuals) != c.R:
+        raise ValueError(f"need {c.R} worker residual buffers")
+    for k, e in enumerate(worker_residuals):
+        _check_tensor(e, "f32", c.N, f"worker_residuals[{k}]")
+    ga, pa = _ptrs([_addr(g) for g in rank_grads]), _ptrs([_addr(p) for p in rank_params])
+    ea = _ptrs([_addr(e) for e in worker_residuals])
+    _check(lib().zero_step_onebit(plan.ptr, ctypes.addressof(ga), _addr(master), _addr(m),
+                                  _addr(v), ctypes.addressof(pa), ctypes.byref(hp), step,
+                                  freeze_step, ctypes.addressof(ea), _addr(server_residual),
+                                  _stream(stream)), "zero_step_onebit")
