@@ -647,6 +647,35 @@ def run_table(args):
     del ds, w_res, s_res
     torch.cuda.empty_cache()
 
+    # the step with global-norm clipping on the 1B-shaped workload (clipping
+    # active: max_norm far below the gradient norm)
+    wl = W.llama32_1b()
+    ds = H.DeviceState(wl, staged_scratch=False)
+    ds.fill_state_device()
+    ds.fill_grads_device(wl.step)
+    ts, t = [], wl.step
+    for k in range(3 + 10):
+        flush.fill_(k & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        ds.step_clipped(t, 1e-3)
+        e1.record()
+        torch.cuda.synchronize()
+        t += 1
+        if k >= 3:
+            ts.append(e0.elapsed_time(e1))
+    ms = float(np.median(ts))
+    b = 2 * wl.R * wl.M + 4 + 4 + 24 + 2 * wl.R
+    row = {"workload": "llama-3.2-1b", "R": wl.R, "M": wl.M, "N": wl.N, "variant": "clipped",
+           "launches": 2 + len(_tree_levels(wl.N)), "ms": round(ms, 4),
+           "params_per_s": wl.N / (ms / 1e3), "bytes_per_param": b,
+           "GB_s": round(b * wl.N / (ms / 1e3) / 1e9, 1),
+           "frac_of_measured_peak": round(b * wl.N / (ms / 1e3) / 1e9 / peak, 4)}
+    rows.append(row)
+    print(json.dumps(row), flush=True)
+    del ds
+    torch.cuda.empty_cache()
+
     for R in (2, 4, 8):
         S = 1024
         while S <= 256 * 1024 * 1024:

@@ -54,6 +54,19 @@ def test_clipped_matches_oracle(n, R, M):
         assert int(ds.status.item()) == 0
 
 
+@pytest.mark.parametrize("n", [1, 2049, 100_003])
+@pytest.mark.parametrize("R,M", [(64, 4), (64, 1), (1, 256)])
+def test_clipped_largest_rank_and_microbatch_counts(n, R, M):
+    """The library's limits: 64 ranks, 256 gradient buffers."""
+    wl = W.flat(R, M, n, seed=n % 997 + R, step=3)
+    G, W0, m0, v0 = H.host_inputs(wl, 3)
+    want, ss, _ = _oracle_clipped(wl, G, W0, m0, v0, 3, 1e-4)
+    ds, got, gss = _gpu_clipped(wl, G, W0, m0, v0, 3, 1e-4)
+    assert gss == ss, (gss, ss)
+    res = H.compare(got, want)
+    assert not {k: v for k, v in res.items() if v}, res
+
+
 def test_no_clipping_is_bit_identical_to_zero_step():
     wl = W.llama32_1b().scaled(300_000)
     G, W0, m0, v0 = H.host_inputs(wl, wl.step)

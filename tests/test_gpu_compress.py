@@ -50,7 +50,7 @@ def test_compressed_step_matches_oracle(kind, ef, n):
 
 
 @pytest.mark.parametrize("kind", KINDS)
-@pytest.mark.parametrize("R,M", [(8, 1), (7, 4), (3, 2)])
+@pytest.mark.parametrize("R,M", [(8, 1), (7, 4), (3, 2), (64, 4), (1, 256)])
 def test_compressed_rank_microbatch_pairs(kind, R, M):
     _run(W.flat(R, M, 20_011, seed=R + M, step=1, state="synthetic"), kind, True, [1, 2])
 

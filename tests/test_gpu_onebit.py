@@ -72,7 +72,8 @@ def test_onebit_matches_oracle(n):
     _run(wl, [1, 2, 3, 4, 5], freeze=2)
 
 
-@pytest.mark.parametrize("R,M", [(8, 1), (4, 1), (7, 4), (3, 2), (2, 2), (1, 1)])
+@pytest.mark.parametrize("R,M", [(8, 1), (4, 1), (7, 4), (3, 2), (2, 2), (1, 1), (64, 4),
+                                 (64, 1), (1, 256)])
 def test_onebit_rank_microbatch_pairs(R, M):
     wl = _with_align(W.flat(R, M, 20_011, seed=R + M, step=1, state="synthetic"))
     _run(wl, [1, 2, 3, 4], freeze=1)

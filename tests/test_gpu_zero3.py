@@ -60,9 +60,10 @@ def test_zero3_step_matches_oracle(name, target):
     assert int(ds.status.item()) == 0
 
 
-@pytest.mark.parametrize("n,R", [(1, 2), (7, 4), (2049, 3), (4096 * 8, 8), (100_003, 7)])
-def test_zero3_step_ragged(n, R):
-    wl = W.flat(R, 1, n, seed=n, step=2)
+@pytest.mark.parametrize("n,R,M", [(1, 2, 1), (7, 4, 1), (2049, 3, 1), (4096 * 8, 8, 1),
+                                   (100_003, 7, 1), (100_003, 64, 4), (2049, 1, 256)])
+def test_zero3_step_ragged(n, R, M):
+    wl = W.flat(R, M, n, seed=n, step=2)
     plan, ds, shards, (Wz, mz, vz, Ps) = _zero3_run(wl, [2])
     assert np.array_equal(H.u16_from_bf16(shards), Ps)
 
