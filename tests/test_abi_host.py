@@ -299,3 +299,15 @@ def test_onebit_argument_errors():
     assert call(worker=[g[0]] + E[1:]) == B.ZERO_ERR_OVERLAP
     assert call(worker=[E[0], E[0]] + E[2:]) == B.ZERO_ERR_OVERLAP
     assert call(worker=[P[1]] + E[1:]) == B.ZERO_ERR_OVERLAP
+
+
+def test_committed_fused_traffic_matches_the_fused_source():
+    """profiles/traffic.json holds the ncu DRAM bytes of k_fused; it is only
+    valid for the source it was captured on (zero_step.cu up to the end of
+    the fused path).  Any edit there needs a new capture."""
+    import json
+    import os
+    import bench
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    rec = json.load(open(os.path.join(root, "profiles", "traffic.json")))
+    assert rec["source_sha256_16"] == bench.kernel_source_hash()

@@ -57,3 +57,70 @@ def test_compressed_rank_microbatch_pairs(kind, R, M):
 
 def test_compressed_uneven_workload_scaled():
     _run(W.uneven().scaled(200_000), KINDS[1], True, [1, 2])
+
+
+def _split3(x):
+    """bf16 bit patterns (hi, mid, lo) whose fp32 sum ((hi + mid) + lo) is x
+    exactly, or None when three pieces do not carry x's bits."""
+    x = np.float32(x)
+    pieces, rest = [], x
+    for _ in range(3):
+        b = oracle.bf16_rne(float(rest))
+        f = np.float32(oracle.bf16_to_float(b))
+        pieces.append(b)
+        rest = np.float32(rest - f)
+    f = [np.float32(oracle.bf16_to_float(b)) for b in pieces]
+    return pieces if np.float32(np.float32(f[0] + f[1]) + f[2]) == x else None
+
+
+def test_int8_codes_at_half_integer_quotients():
+    """Without error feedback a rank's x is the fp32 sum of its M bf16
+    micro-batch values, so with M = 3 any fp32 x can be built exactly.  Each
+    block holds its max A and values within a few ulps of (j +- 1/2) * s,
+    s = A / 127: the quotients x / s land on and around the half-integers
+    where the rounded code changes.  Some blocks have scales outside the
+    reciprocal path's range (2^-100 .. 2^100), one block is all zero."""
+    R, M = 2, 3
+    rng = np.random.default_rng(2024)
+    scales = [float(2.0 ** e * rng.uniform(1, 2)) for e in rng.integers(-60, 40, 90)]
+    scales += [2.0 ** -118 * 1.3, 2.0 ** -105, 2.0 ** 108 * 1.7, 2.0 ** 110]   # fallback path
+    scales += [2.0 ** -93 * 1.01, 2.0 ** 106 * 1.9]           # s just inside the range
+    xs = [[] for _ in range(R)]
+    for A in scales + [0.0]:
+        A = np.float32(oracle.bf16_to_float(oracle.bf16_rne(A)))     # one bf16 piece
+        s = np.float32(A / np.float32(127.0))
+        for r in range(R):
+            blk = [A if r == 0 else -A]
+            while len(blk) < 128:
+                if A == 0:
+                    blk.append(np.float32(0.0))
+                    continue
+                j = int(rng.integers(-127, 127))
+                t = np.float32((j + 0.5) * np.float64(s))
+                t = (np.array([t], np.float32).view(np.int32) + int(rng.integers(-3, 4))).view(np.float32)[0]
+                if abs(t) <= A and _split3(t) is not None:
+                    blk.append(t)
+            xs[r].extend(blk)
+    n = len(xs[0])
+    G = [np.zeros(n, np.uint16) for _ in range(R * M)]
+    for r in range(R):
+        for i, x in enumerate(xs[r]):
+            p = _split3(x)
+            assert p is not None
+            for j in range(M):
+                G[r * M + j][i] = p[j]
+    wl = W.flat(R, M, n, seed=1, step=1, state="zero")
+    W0 = np.zeros(n, np.float32)
+    m0, v0 = np.zeros(n, np.float32), np.zeros(n, np.float32)
+    Wc, mc, vc = W0.copy(), m0.copy(), v0.copy()
+    Pc = [np.zeros(n, np.uint16) for _ in range(R)]
+    hp = oracle.hparams(**wl.hparams())
+    oracle.dp_step_compressed(G, Wc, mc, vc, Pc, hp, 1, R, M, oracle.COMP_INT8, None)
+    ds = H.DeviceState(wl, staged_scratch=False)
+    ds.upload_state(W0, m0, v0)
+    ds.upload_grads(G)
+    z.zero_step_compressed(ds.plan, ds.grads, ds.W, ds.m, ds.v, ds.params, ds.hp, 1,
+                           z.ZERO_COMP_INT8, None)
+    torch.cuda.synchronize()
+    res = H.compare(ds.result(), (Wc, mc, vc, Pc))
+    assert not {k: v for k, v in res.items() if v}, res

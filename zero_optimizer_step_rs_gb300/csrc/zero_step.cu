@@ -25,10 +25,7 @@
 // 256 threads x 4 elements x U units per block (grid-stride over tiles);
 // the last partial tile is done element by element.  The staged kernels
 // give each rank r its own grid row (blockIdx.y = r) and grid-stride over
-// shard r, as rank r would on its own GPU: k_rs_avg over tiles of one or two
-// units from the shard start, k_adamw over 4-vectors, k_ag_cast over
-// 8-element vectors that start on the shard's first multiple of 8 (one
-// 16-byte store per replica), with the head and tail done element by element.
+// the vectors of shard r, as rank r would on its own GPU.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -407,6 +404,10 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st)
 // ------------------------------------------------------- staged steps --
 // Shard r = blockIdx.y covers [r*S, r*S + len), len = min(S, n - r*S).
 // S is a multiple of 4, so every shard starts on a vector boundary.
+// k_rs_avg walks tiles of one or two units from the shard start, k_adamw
+// 4-vectors, and k_ag_cast 8-element vectors that start on the shard's first
+// multiple of 8 (one 16-byte store per replica), with the head and tail done
+// element by element.
 
 __device__ __forceinline__ int64_t shard_len(int64_t n, int64_t S, int r)
 {
@@ -1327,7 +1328,28 @@ struct CompArgs {
     StepScalars s;
 };
 
-template <int KIND>
+// x / b rounded to nearest even from r = RN(1/b): a first FMA correction
+// makes the product x*r a faithful quotient, and a second one with the
+// correctly rounded reciprocal gives the correctly rounded quotient
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990: the residual of a
+// faithful quotient is exact under FMA, and one more correction rounds it
+// correctly).  The argument needs the residuals to stay normal: it is used
+// for 2^-100 <= b <= 2^100 and |x / b| <= 128, where any quotient below 0.5 in
+// magnitude may come out a few ulps off but still rounds to the same
+// integer (a signed zero), which is all the int8 codec takes from it.
+__device__ __forceinline__ float quot_by_recip(float x, float b, float r)
+{
+    const float y0 = __fmul_rn(x, r);
+    const float y1 = __fmaf_rn(__fmaf_rn(-y0, b, x), r, y0);
+    return __fmaf_rn(__fmaf_rn(-y1, b, x), r, y1);
+}
+
+// RECIP: int8 quotients through quot_by_recip (faster where the kernel is
+// bound by issue, i.e. without error feedback; with error feedback, where
+// the residual traffic hides the division, the plain division measures
+// faster).  Both give the same bits.
+template <int KIND, bool RECIP = false>
 __device__ __forceinline__ void codec(float (&x)[4], const bool (&valid)[4], int64_t block_count,
                                       float (&d)[4])
 {
@@ -1341,14 +1363,41 @@ __device__ __forceinline__ void codec(float (&x)[4], const bool (&valid)[4], int
             if (valid[k]) amax = max(amax, __float_as_uint(x[k]) & 0x7FFFFFFFu);
         amax = __reduce_max_sync(0xFFFFFFFFu, amax);
         const float sc = __fdiv_rn(__uint_as_float(amax), 127.0f);
+        if constexpr (RECIP) {
+            // x / sc correctly rounded: the block shares sc, so while sc is
+            // a normal number well inside the exponent range (warp-uniform
+            // test) every quotient comes from one reciprocal and FMA
+            // corrections (quot_by_recip); otherwise the IEEE division
+            const bool fast = sc >= 0x1p-100f && sc <= 0x1p100f;
+            float t[4];
+            if (fast) {
+                const float rc = __frcp_rn(sc);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            if (sc == 0.0f) {
-                d[k] = 0.0f;
+                for (int k = 0; k < 4; ++k) t[k] = quot_by_recip(x[k], sc, rc);
             } else {
-                float q = rintf(__fdiv_rn(x[k], sc));
-                q = fminf(fmaxf(q, -127.0f), 127.0f);
-                d[k] = __fmul_rn(q, sc);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) t[k] = __fdiv_rn(x[k], sc);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (sc == 0.0f) {
+                    d[k] = 0.0f;
+                } else {
+                    float q = rintf(t[k]);
+                    q = fminf(fmaxf(q, -127.0f), 127.0f);
+                    d[k] = __fmul_rn(q, sc);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (sc == 0.0f) {
+                    d[k] = 0.0f;
+                } else {
+                    float q = rintf(__fdiv_rn(x[k], sc));
+                    q = fminf(fmaxf(q, -127.0f), 127.0f);
+                    d[k] = __fmul_rn(q, sc);
+                }
             }
         }
     } else {                                      // ZERO_COMP_SIGN
@@ -1398,7 +1447,7 @@ __device__ __forceinline__ void comp_ranks_generic(const CompArgs& a, int R, int
             for (int k = 0; k < 4; ++k) x[k] = __fadd_rn(x[k], res[k]);
         }
         float d[4];
-        codec<KIND>(x, valid, block_count, d);
+        codec<KIND, !EF>(x, valid, block_count, d);
         if constexpr (EF) {
             float o[4];
 #pragma unroll
@@ -1433,10 +1482,12 @@ __global__ void __launch_bounds__(kThreads) k_comp(const __grid_constant__ CompA
 #pragma unroll
         for (int k = 0; k < 4; ++k) valid[k] = e + k < n;
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        // every rank's loads first, then the codecs and their warp reductions,
-        // so the loads are all in flight before the first sync; fp16 without
-        // error feedback has no sync and runs faster in the rank-by-rank form
-        // (fewer registers, more blocks per SM)
+        float4 w4, m4, v4;                        // the owner's state of a full block
+        bool have_state = false;
+        // every rank's loads first - and the owner's state - then the codecs
+        // and their warp reductions, so the loads are all in flight before the
+        // first sync; fp16 without error feedback has no sync and runs faster
+        // in the rank-by-rank form (fewer registers, more blocks per SM)
         if constexpr (RC > 0 && MC > 0 && (KIND != ZERO_COMP_FP16 || EF)) {
             if (full) {
                 uint2 gx[RC * MC];
@@ -1447,6 +1498,7 @@ __global__ void __launch_bounds__(kThreads) k_comp(const __grid_constant__ CompA
 #pragma unroll
                     for (int r = 0; r < RC; ++r) ex[r] = ld_stream(a.E[r] + e);
                 }
+                have_state = false;
 #pragma unroll
                 for (int r = 0; r < RC; ++r) {
                     float x[4];
@@ -1464,7 +1516,7 @@ __global__ void __launch_bounds__(kThreads) k_comp(const __grid_constant__ CompA
                         x[3] = __fadd_rn(x[3], ex[r].w);
                     }
                     float d[4];
-                    codec<KIND>(x, valid, block_count, d);
+                    codec<KIND, !EF>(x, valid, block_count, d);
                     if constexpr (EF)
                         st_stream(a.E[r] + e, make_float4(__fsub_rn(x[0], d[0]), __fsub_rn(x[1], d[1]),
                                                           __fsub_rn(x[2], d[2]), __fsub_rn(x[3], d[3])));
@@ -1479,7 +1531,12 @@ __global__ void __launch_bounds__(kThreads) k_comp(const __grid_constant__ CompA
         }
         // the owner: average, AdamW, all-gather
         if (full) {
-            float4 w = ld_stream(a.W + e), m = ld_stream(a.m + e), v = ld_stream(a.v + e);
+            if (!have_state) {
+                w4 = ld_stream(a.W + e);
+                m4 = ld_stream(a.m + e);
+                v4 = ld_stream(a.v + e);
+            }
+            float4 w = w4, m = m4, v = v4;
             float* wp = &w.x;
             float* mp = &m.x;
             float* vp = &v.x;
