@@ -1345,11 +1345,14 @@ __device__ __forceinline__ float quot_by_recip(float x, float b, float r)
     return __fmaf_rn(__fmaf_rn(-y1, b, x), r, y1);
 }
 
-// RECIP: int8 quotients through quot_by_recip (faster where the kernel is
-// bound by issue, i.e. without error feedback; with error feedback, where
-// the residual traffic hides the division, the plain division measures
-// faster).  Both give the same bits.
-template <int KIND, bool RECIP = false>
+// Two ways to the same bits, chosen per kernel by measurement (the codec's
+// arithmetic cost is hidden or not depending on what else the kernel moves):
+//   RECIP  int8 quotients through quot_by_recip instead of one IEEE division
+//          each (taken without error feedback, where the kernel is bound by
+//          instruction issue);
+//   POW2   a full sign block's |x| sum scaled by the exact 2^-7 instead of
+//          divided by 128 (taken with error feedback).
+template <int KIND, bool RECIP = false, bool POW2 = false>
 __device__ __forceinline__ void codec(float (&x)[4], const bool (&valid)[4], int64_t block_count,
                                       float (&d)[4])
 {
@@ -1408,7 +1411,10 @@ __device__ __forceinline__ void codec(float (&x)[4], const bool (&valid)[4], int
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) t = __fadd_rn(t, __shfl_down_sync(0xFFFFFFFFu, t, off));
         t = __shfl_sync(0xFFFFFFFFu, t, 0);
-        const float sc = __fdiv_rn(t, (float)block_count);
+        // a full block divides by 128: scaling by the exact 2^-7 rounds the
+        // same quotient
+        const float sc = POW2 && block_count == kCompBlock ? __fmul_rn(t, 1.0f / kCompBlock)
+                                                           : __fdiv_rn(t, (float)block_count);
 #pragma unroll
         for (int k = 0; k < 4; ++k) d[k] = x[k] < 0.0f ? -sc : sc;
     }
@@ -1447,7 +1453,7 @@ __device__ __forceinline__ void comp_ranks_generic(const CompArgs& a, int R, int
             for (int k = 0; k < 4; ++k) x[k] = __fadd_rn(x[k], res[k]);
         }
         float d[4];
-        codec<KIND, !EF>(x, valid, block_count, d);
+        codec<KIND, !EF, EF>(x, valid, block_count, d);
         if constexpr (EF) {
             float o[4];
 #pragma unroll
@@ -1516,7 +1522,7 @@ __global__ void __launch_bounds__(kThreads) k_comp(const __grid_constant__ CompA
                         x[3] = __fadd_rn(x[3], ex[r].w);
                     }
                     float d[4];
-                    codec<KIND, !EF>(x, valid, block_count, d);
+                    codec<KIND, !EF, EF>(x, valid, block_count, d);
                     if constexpr (EF)
                         st_stream(a.E[r] + e, make_float4(__fsub_rn(x[0], d[0]), __fsub_rn(x[1], d[1]),
                                                           __fsub_rn(x[2], d[2]), __fsub_rn(x[3], d[3])));
