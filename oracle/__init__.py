@@ -131,6 +131,11 @@ def lib():
             L.oracle_onebit_step.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp,
                                              ctypes.POINTER(HParams), i64, i64, vp, vp]
             L.oracle_onebit_step.restype = ctypes.c_int
+            L.oracle_zero3_rs_unit.argtypes = [i64, i32, i32, i64, vp, i64, i64, vp, vp]
+            L.oracle_zero3_rs_unit.restype = ctypes.c_int
+            L.oracle_zero3_update.argtypes = [i64, i32, i32, i64, vp, vp, vp, vp, vp,
+                                              ctypes.POINTER(HParams), i64]
+            L.oracle_zero3_update.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -383,3 +388,32 @@ def onebit_step(G, W, m, v, P, hp: HParams, step: int, freeze_step: int, R: int,
                                   ctypes.addressof(ea), _ptr(Es))
     if rc != 0:
         raise RuntimeError(f"oracle_onebit_step failed: {rc}")
+
+
+def zero3_rs_unit(Gu, n: int, R: int, M: int, S: int, lo: int, hi: int, gshard: np.ndarray):
+    """Reduce-scatter of the unit [lo, hi) (reading R16) into gshard (n or
+    more floats, element i at index i); returns the per-card receive counts."""
+    for k, g in enumerate(Gu):
+        _check(g, np.uint16, hi - lo, f"Gu[{k}]")
+    _check(gshard, np.float32, None, "gshard")
+    if gshard.size < n:
+        raise ValueError("gshard too small")
+    ga = _ptr_array(Gu) if Gu else None
+    recv = np.zeros(R, np.int64)
+    rc = lib().oracle_zero3_rs_unit(n, R, M, S, ctypes.addressof(ga) if ga is not None else None,
+                                    lo, hi, _ptr(gshard), _ptr(recv))
+    if rc != 0:
+        raise RuntimeError(f"oracle_zero3_rs_unit failed: {rc}")
+    return recv
+
+
+def zero3_update(gshard, W, m, v, Pshard, hp: HParams, step: int, n: int, R: int, M: int,
+                 S: int) -> None:
+    """Shard update from reduce-scattered gradients (reading R16)."""
+    for nm, a in (("gshard", gshard), ("W", W), ("m", m), ("v", v)):
+        _check(a, np.float32, None, nm)
+    _check(Pshard, np.uint16, None, "Pshard")
+    rc = lib().oracle_zero3_update(n, R, M, S, _ptr(gshard), _ptr(W), _ptr(m), _ptr(v),
+                                   _ptr(Pshard), ctypes.byref(hp), step)
+    if rc != 0:
+        raise RuntimeError(f"oracle_zero3_update failed: {rc}")

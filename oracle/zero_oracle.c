@@ -27,6 +27,11 @@
  *   oracle_zero_bytes      the pages' exercises (7B/8 ranks, 7.5B/64 ranks,
  *                          p=8 per-card units)
  *   oracle_shard_len       hand-computed layouts (uneven 100,000,007 / 7)
+ *   oracle_zero3_rs_unit / oracle_zero3_update  (tests/test_oracle_zero3.py)
+ *                          composed over random unit partitions in random
+ *                          order == oracle_zero3_step bit for bit; the
+ *                          worked 4-rank reduce-scatter example as one unit;
+ *                          per-card receive counts add up to the step's
  *   oracle_onebit_step     (tests/test_oracle_onebit.py) warm-up == the
  *                          plain step; a hand-worked two-rank example; the
  *                          plain step whenever the sign codec is lossless
@@ -490,6 +495,53 @@ int oracle_zero3_gather(int64_t n, int32_t R, int64_t S, const uint16_t* Pshard,
         if (owner != card) ++from_others;
     }
     if (recv) *recv = from_others;
+    return 0;
+}
+
+/* Reading R16 (zero_oracle.h): the unit's reduce-scatter, card by card. */
+int oracle_zero3_rs_unit(int64_t n, int32_t R, int32_t M, int64_t S,
+                         const uint16_t* const* Gu, int64_t lo, int64_t hi,
+                         float* gshard, int64_t* recv)
+{
+    if (n < 0 || R < 1 || M < 1 || S < 0 || S * R < n) return -1;
+    if (lo < 0 || hi < lo || hi > n) return -1;
+    if (hi > lo && (!Gu || !gshard)) return -1;
+    float denom_rm = (float)((double)R * (double)M);
+    int32_t RM = R * M;
+    const uint16_t** ptr = (const uint16_t**)malloc(sizeof(void*) * (size_t)RM);
+    if (!ptr) return -1;
+    for (int32_t r = 0; r < R; ++r) {                   /* card r */
+        int64_t own_lo = (int64_t)r * S, own_hi = own_lo + S;
+        if (own_hi > n) own_hi = n;
+        int64_t a = lo > own_lo ? lo : own_lo;          /* the unit's part card r owns */
+        int64_t b = hi < own_hi ? hi : own_hi;
+        if (recv) recv[r] = 0;
+        if (b <= a) continue;
+        /* every rank's gradient values for [a, b): rank q's buffers hold
+         * element i at index i - lo */
+        for (int32_t k = 0; k < RM; ++k) {
+            ptr[k] = Gu[k] + (a - lo);
+            if (recv && k % M == 0 && k / M != r) recv[r] += b - a;
+        }
+        for (int64_t i = a; i < b; ++i)
+            gshard[i] = oracle_avg_grad((const uint16_t* const*)ptr, R, M, i - a, denom_rm);
+    }
+    free(ptr);
+    return 0;
+}
+
+int oracle_zero3_update(int64_t n, int32_t R, int32_t M, int64_t S, const float* gshard,
+                        float* W, float* m, float* v, uint16_t* Pshard,
+                        const oracle_hparams* hp, int64_t step)
+{
+    if (n < 0 || R < 1 || M < 1 || S < 0 || S * R < n || !hp || step < 1) return -1;
+    if (n > 0 && (!gshard || !W || !m || !v || !Pshard)) return -1;
+    oracle_scalars s;
+    oracle_make_scalars(hp, step, R, M, &s);
+    for (int64_t i = 0; i < n; ++i) {        /* each card updates the elements it owns */
+        oracle_adamw_elem(&s, gshard[i], &W[i], &m[i], &v[i]);
+        Pshard[i] = oracle_bf16_rne(W[i]);
+    }
     return 0;
 }
 

@@ -229,6 +229,34 @@ int oracle_zero3_gather(int64_t n, int32_t R, int64_t S, const uint16_t* Pshard,
                         int64_t lo, int64_t hi, int32_t card, uint16_t* out,
                         int64_t* recv);
 
+/* ZeRO-3 backward, unit by unit (CS25 V6 Lecture 4 notes, "ZeRO-3 / FSDP":
+ * the backward materialises each unit's parameters again and reduce-
+ * scatters the unit's gradient; LLM infra 06, section 3.1: all-gather,
+ * reduce-scatter and all-gather again, about 1.5 times DP's traffic).
+ * Reading R16: right after a unit [lo, hi)'s backward, every rank holds the
+ * unit's gradient for each of its micro-batches: Gu[r*M + j] holds hi - lo
+ * bf16 values, element i at index i - lo.  Each card r receives, for the
+ * elements of the unit it owns, the other ranks' local sums, and writes
+ *   gshard[i] = (ordered sum as in oracle_avg_grad) / (R*M)
+ * into its fp32 gradient shard (padded layout, element i at index i).
+ * The step then updates every owned element from gshard and casts it into
+ * the card's bf16 parameter shard (oracle_zero3_update).  Over any set of
+ * units that covers [0, n) once, in any order, the result is that of
+ * oracle_zero3_step.
+ * recv (may be NULL, R entries) receives per card the count of numbers it
+ * got from other cards for this unit: one per other rank and owned element.
+ * Returns 0 or -1 (bad argument; 0 <= lo <= hi <= n). */
+int oracle_zero3_rs_unit(int64_t n, int32_t R, int32_t M, int64_t S,
+                         const uint16_t* const* Gu, int64_t lo, int64_t hi,
+                         float* gshard, int64_t* recv);
+
+/* ZeRO-3 shard update from reduce-scattered gradients: AdamW of every
+ * element i < n from gshard[i], then Pshard[i] = bf16(W[i]).  Returns 0 or
+ * -1. */
+int oracle_zero3_update(int64_t n, int32_t R, int32_t M, int64_t S, const float* gshard,
+                        float* W, float* m, float* v, uint16_t* Pshard,
+                        const oracle_hparams* hp, int64_t step);
+
 /* ------------------------------------------------------------------------
  * Compressed gradient reduce-scatter (CS324 Lecture 9 notes, section 7.4:
  * every card compresses the gradient it sends - fp16, int8, sign - with or

@@ -67,6 +67,15 @@ MUTANTS = {
                       "float s = abs_tree(xb, cnt, 0, ORACLE_COMP_BLOCK) / (float)ORACLE_COMP_BLOCK;"),
     "ef_sign_flipped": ("if (E) E[r][i] = x[i] - d[i];", "if (E) E[r][i] = d[i] - x[i];"),
     "ef_not_added": ("x[i] = E ? loc + E[r][i] : loc;", "x[i] = E ? loc + 0.0f * E[r][i] : loc;"),
+    "zero3_unit_source_offset": ("ptr[k] = Gu[k] + (a - lo);", "ptr[k] = Gu[k] + (a - lo) * 0;"),
+    "zero3_unit_owned_range_clipped_low": ("int64_t a = lo > own_lo ? lo : own_lo;",
+                                           "int64_t a = own_lo;"),
+    "zero3_unit_counts_own_rank": ("if (recv && k % M == 0 && k / M != r) recv[r] += b - a;",
+                                   "if (recv && k % M == 0) recv[r] += b - a;"),
+    "zero3_unit_divides_by_R": ("float denom_rm = (float)((double)R * (double)M);",
+                                "float denom_rm = (float)((double)R * (double)1);"),
+    "zero3_update_casts_before_update": ("oracle_adamw_elem(&s, gshard[i], &W[i], &m[i], &v[i]);\n        Pshard[i] = oracle_bf16_rne(W[i]);",
+                                         "Pshard[i] = oracle_bf16_rne(W[i]);\n        oracle_adamw_elem(&s, gshard[i], &W[i], &m[i], &v[i]);"),
     "onebit_warmup_off_by_one": ("if (step <= freeze_step)", "if (step < freeze_step)"),
     "onebit_local_mean_not_divided": ("float gl = loc / denom_m;", "float gl = loc + 0.0f * denom_m;"),
     "onebit_momentum_from_grad_only": ("float ml = s.beta1 * m[i] + s.one_minus_beta1 * gl;",

@@ -90,3 +90,78 @@ def test_reduce_scatter_traffic_independent_of_microbatches(M):
     recv = oracle.zero3_step(G, W0.copy(), m0.copy(), v0.copy(), np.zeros(n, np.uint16),
                              oracle.hparams(), 1, p, M, n, S)
     assert list(recv) == [(p - 1) * S] * p
+
+
+# ------------------------------------------------- per-unit reduce-scatter --
+# Reading R16: each unit's gradient is reduce-scattered right after its
+# backward into the owners' fp32 gradient shards; the step then updates the
+# shards from them.
+
+
+def _unit_grads(G, lo, hi):
+    return [np.ascontiguousarray(g[lo:hi]) for g in G]
+
+
+def _partition(n, rng, pieces):
+    cuts = np.sort(rng.choice(np.arange(1, n), size=min(pieces, n - 1), replace=False))
+    b = [0] + cuts.tolist() + [n]
+    units = [(b[k], b[k + 1]) for k in range(len(b) - 1)]
+    rng.shuffle(units)                       # any order: the backward runs last unit first
+    return units
+
+
+@pytest.mark.parametrize("n,R,M,align,pieces", [(1000, 4, 2, 64, 7), (4099, 7, 4, 64, 30),
+                                                (5, 4, 1, 64, 3), (8192, 8, 1, 64, 1),
+                                                (130, 3, 3, 4, 129), (10_007, 2, 2, 8, 11)])
+def test_unit_reduce_scatter_then_update_is_the_zero3_step(n, R, M, align, pieces):
+    G, W0, m0, v0 = _inputs(n, R, M, n + 5 * R)
+    S = oracle.shard_len(n, R, align)
+    hp = oracle.hparams()
+    # the whole-step oracle (itself pinned to plain DP above)
+    Wz = np.zeros(R * S, np.float32)
+    mz, vz = Wz.copy(), Wz.copy()
+    Wz[:n], mz[:n], vz[:n] = W0, m0, v0
+    Ps = np.full(R * S, 0xBEEF, np.uint16)
+    recv_step = oracle.zero3_step(G, Wz, mz, vz, Ps, hp, 4, R, M, n, S)
+    # unit by unit, in a shuffled order
+    rng = np.random.default_rng(n)
+    gshard = np.full(R * S, np.nan, np.float32)
+    recv = np.zeros(R, np.int64)
+    for lo, hi in _partition(n, rng, pieces):
+        recv += oracle.zero3_rs_unit(_unit_grads(G, lo, hi), n, R, M, S, lo, hi, gshard)
+    assert not np.isnan(gshard[:n]).any()              # every element reduced once
+    assert np.isnan(gshard[n:]).all()                  # the pad never written
+    Wu = np.zeros(R * S, np.float32)
+    mu, vu = Wu.copy(), Wu.copy()
+    Wu[:n], mu[:n], vu[:n] = W0, m0, v0
+    Pu = np.full(R * S, 0xBEEF, np.uint16)
+    oracle.zero3_update(gshard, Wu, mu, vu, Pu, hp, 4, n, R, M, S)
+    for a, b in ((Wu, Wz), (mu, mz), (vu, vz)):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    assert np.array_equal(Pu, Ps)
+    assert np.array_equal(recv, recv_step)
+
+
+def test_unit_reduce_scatter_worked_example():
+    # the pages' 4-rank example as one unit of 4 elements, one per rank
+    gd = load_golden("rs_worked_example.txt")
+    G = [np.array([oracle.bf16_rne(x) for x in gd[f"rank{r}"]], np.uint16) for r in range(4)]
+    g = np.zeros(4, np.float32)
+    recv = oracle.zero3_rs_unit(G, 4, 4, 1, 1, 0, 4, g)
+    assert g.tolist() == gd["rs_avg"]
+    assert recv.tolist() == [3, 3, 3, 3]                # one number from each other rank
+
+
+def test_unit_receive_counts_and_untouched_elements():
+    n, R, M, S = 300, 3, 2, 128                         # shards [0,128) [128,256) [256,300)
+    G, _, _, _ = _inputs(n, R, M, 9)
+    g = np.full(n, -1.0, np.float32)
+    lo, hi = 100, 270
+    recv = oracle.zero3_rs_unit(_unit_grads(G, lo, hi), n, R, M, S, lo, hi, g)
+    # card 0 owns 100..127 (28), card 1 128..255 (128), card 2 256..269 (14);
+    # each receives one number per element from each of the other 2 ranks
+    assert recv.tolist() == [2 * 28, 2 * 128, 2 * 14]
+    assert np.all(g[:lo] == -1.0) and np.all(g[hi:] == -1.0)
+    assert np.all(g[lo:hi] != -1.0)
+    with pytest.raises(RuntimeError):                   # hi beyond n
+        oracle.zero3_rs_unit([np.zeros(296, np.uint16)] * (R * M), n, R, M, S, 5, 301, g)
