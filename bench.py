@@ -575,6 +575,39 @@ def run_table(args):
                 rows.append(row)
                 print(json.dumps(row), flush=True)
             del full
+            # FSDP's backward: each layer's gradient reduce-scattered by its
+            # own launch (last layer first), then one update of the shards
+            gs = torch.empty(ds.padded, dtype=torch.float32, device="cuda")
+            units = list(zip(layers[:-1], layers[1:]))[::-1]
+            t_rs, t_up = [], []
+            for k in range(3 + 10):
+                flush.fill_(k & 0xFF)
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                ev[0].record()
+                for lo, hi in units:
+                    z.zero3_rs_unit(ds.plan, [g[lo:hi] for g in ds.grads], lo, hi, gs)
+                ev[1].record()
+                z.zero3_update(ds.plan, gs, ds.W, ds.m, ds.v, shards, ds.hp, t)
+                ev[2].record()
+                torch.cuda.synchronize()
+                t += 1
+                if k >= 3:
+                    t_rs.append(ev[0].elapsed_time(ev[1]))
+                    t_up.append(ev[1].elapsed_time(ev[2]))
+            for label, ms, b, n_l in (
+                    ("zero3_rs_unit, unit = layer (18 units)", float(np.median(t_rs)),
+                     2 * wl.R * wl.M + 4, len(units)),
+                    ("zero3_update", float(np.median(t_up)), 30, 1),
+                    ("unit reduce-scatter + update", float(np.median(t_rs)) + float(np.median(t_up)),
+                     2 * wl.R * wl.M + 34, len(units) + 1)):
+                row = {"workload": name, "R": wl.R, "M": wl.M, "N": wl.N,
+                       "variant": "zero3_units", "part": label, "launches": n_l,
+                       "ms": round(ms, 4), "params_per_s": wl.N / (ms / 1e3), "bytes_per_param": b,
+                       "GB_s": round(b * wl.N / (ms / 1e3) / 1e9, 1),
+                       "frac_of_measured_peak": round(b * wl.N / (ms / 1e3) / 1e9 / peak, 4)}
+                rows.append(row)
+                print(json.dumps(row), flush=True)
+            del gs
         del ds, shards
         torch.cuda.empty_cache()
 

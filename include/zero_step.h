@@ -353,6 +353,40 @@ zero_status zero3_gather(const zero_plan_t* plan, const uint16_t* param_shards, 
                          int64_t hi, uint16_t* const* outs, int32_t n_out, void* stream);
 
 /*
+ * ZeRO-3 gradient reduce-scatter of one unit, right after that unit's
+ * backward (CS25 V6 Lecture 4 notes, "ZeRO-3 / FSDP": the backward
+ * materialises each unit's parameters again and reduce-scatters its
+ * gradient; LLM infra 06, section 3.1).  For every element i in [lo, hi):
+ *   grad_shards[i] = (ordered fp32 sum over r, j of unit_grads[r*M + j][i - lo])
+ *                    / (R*M)
+ * with the sum order and the division of zero_step, written into the owner's
+ * gradient shard.  Elements outside [lo, hi) are not touched.
+ *   unit_grads   host array of R*M device pointers, each hi - lo bf16 (the
+ *                unit's gradient of rank r, micro-batch j), 16-byte aligned.
+ *   grad_shards  device, plan->padded floats in the state layout (element i
+ *                at index i, pad never written); must not overlap the inputs.
+ *   0 <= lo <= hi <= N, any lo.  flags: 0 or ZERO_FLAG_CHECK_FINITE (then
+ *   dev_status is required, as in zero_step).
+ * Traffic: 2RM + 4 bytes per element of the unit.
+ */
+zero_status zero3_rs_unit(const zero_plan_t* plan, const uint16_t* const* unit_grads, int64_t lo,
+                          int64_t hi, float* grad_shards, int32_t flags, int32_t* dev_status,
+                          void* stream);
+
+/*
+ * ZeRO-3 shard update from reduce-scattered gradients: AdamW of every
+ * element i < N from grad_shards[i], then param_shards[i] = bf16(master[i]),
+ * the rank's own parameter shard.  After zero3_rs_unit over units that cover
+ * [0, N) once, in any order, the result is zero3_step's, bit for bit.
+ *   grad_shards  device, plan->padded floats (read only).  Other arguments
+ *                as zero3_step.
+ * Traffic: 4 + 24 + 2 bytes per element.
+ */
+zero_status zero3_update(const zero_plan_t* plan, const float* grad_shards, float* master,
+                         float* m, float* v, uint16_t* param_shards,
+                         const zero_adamw_hparams* hp, int64_t step, void* stream);
+
+/*
  * End-to-end step from host memory.  host_grads: R*M host pointers to the
  * gradient buffers (N bf16 each); host_params_out: host, N bf16, receives
  * replica 0 (every replica holds the same bits).  Two modes:

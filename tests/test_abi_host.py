@@ -311,3 +311,36 @@ def test_committed_fused_traffic_matches_the_fused_source():
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     rec = json.load(open(os.path.join(root, "profiles", "traffic.json")))
     assert rec["source_sha256_16"] == bench.kernel_source_hash()
+
+
+def test_zero3_unit_entry_argument_errors():
+    import ctypes
+    plan = z.Plan([100_000], 4, 2, 2)
+    g, Wp, mp, vp, P, scr, st = fake_bufs(plan)
+    L = B.lib()
+    hp = z.hparams()
+
+    def rs(lo=10, hi=5000, grads=g, gs=scr, flags=0, status=None):
+        ga = B._ptrs(grads) if grads is not None else None
+        return L.zero3_rs_unit(plan.ptr, ctypes.addressof(ga) if ga is not None else None, lo, hi,
+                               gs, flags, status, None)
+    assert rs(lo=-1) == B.ZERO_ERR_INVALID_ARG
+    assert rs(lo=6000, hi=5000) == B.ZERO_ERR_INVALID_ARG
+    assert rs(hi=100_001) == B.ZERO_ERR_INVALID_ARG
+    assert rs(flags=2) == B.ZERO_ERR_INVALID_ARG
+    assert rs(flags=B.ZERO_FLAG_CHECK_FINITE) == B.ZERO_ERR_NULL
+    assert rs(lo=7, hi=7, grads=None, gs=None) == B.ZERO_OK          # empty unit: nothing to do
+    assert rs(grads=None) == B.ZERO_ERR_NULL
+    assert rs(grads=g[:-1] + [0]) == B.ZERO_ERR_NULL
+    assert rs(grads=[g[0] + 2] + g[1:]) == B.ZERO_ERR_ALIGN
+    assert rs(gs=scr + 4) == B.ZERO_ERR_ALIGN
+    assert rs(gs=g[3]) == B.ZERO_ERR_OVERLAP
+    assert rs(status=scr + 64) == B.ZERO_ERR_OVERLAP
+
+    def upd(gs=scr, W=Wp, m=mp, v=vp, ps=P[0], step=1):
+        return L.zero3_update(plan.ptr, gs, W, m, v, ps, ctypes.byref(hp), step, None)
+    assert upd(step=0) == B.ZERO_ERR_INVALID_ARG
+    assert upd(gs=None) == B.ZERO_ERR_NULL
+    assert upd(gs=Wp) == B.ZERO_ERR_OVERLAP
+    assert upd(ps=mp) == B.ZERO_ERR_OVERLAP
+    assert upd(ps=P[0] + 2) == B.ZERO_ERR_ALIGN

@@ -133,3 +133,117 @@ def test_full_size_zero3_llama():
     z.zero3_gather(ds.plan, shards, 0, ds.N, [full])
     torch.cuda.synchronize()
     assert torch.equal(full.view(torch.int16), shards[:ds.N].view(torch.int16))
+
+
+# ----------------------------------------- per-unit reduce-scatter (FSDP) --
+
+def _random_units(n, rng, pieces):
+    if n == 1:
+        return [(0, 1)]
+    cuts = np.sort(rng.choice(np.arange(1, n), size=min(pieces, n - 1), replace=False))
+    b = [0] + cuts.tolist() + [n]
+    units = [(b[k], b[k + 1]) for k in range(len(b) - 1)]
+    rng.shuffle(units)
+    return units
+
+
+@pytest.mark.parametrize("n,R,M,pieces", [(1, 2, 1, 1), (1000, 4, 2, 7), (4099, 7, 4, 30),
+                                          (8192, 8, 1, 3), (20_011, 3, 2, 64), (100_003, 8, 1, 9),
+                                          (5003, 64, 4, 5), (2049, 1, 256, 4)])
+def test_unit_reduce_scatter_then_update_matches_oracle(n, R, M, pieces):
+    """Random units (any start, so the fp32 shard stores take both the
+    vector and the scalar path) in shuffled order, each unit's gradient in
+    buffers of its own; then the update.  Gradient shards, state and
+    parameter shards bit for bit against the oracle, and against zero3_step."""
+    wl = W.flat(R, M, n, seed=n + R, step=3)
+    G, W0, m0, v0 = H.host_inputs(wl, 3)
+    plan = z.Plan(wl.numels, R, M, wl.stage, wl.align)
+    S, padded = plan.S, plan.padded
+    hp = oracle.hparams(**wl.hparams())
+    rng = np.random.default_rng(n)
+    units = _random_units(n, rng, pieces)
+    # oracle
+    g_or = np.full(padded, np.nan, np.float32)
+    for lo, hi in units:
+        oracle.zero3_rs_unit([np.ascontiguousarray(g[lo:hi]) for g in G], n, R, M, S, lo, hi, g_or)
+    Wz = np.zeros(padded, np.float32)
+    mz, vz = Wz.copy(), Wz.copy()
+    Wz[:n], mz[:n], vz[:n] = W0, m0, v0
+    Ps = np.full(padded, CANARY, np.uint16)
+    oracle.zero3_update(g_or, Wz, mz, vz, Ps, hp, 3, n, R, M, S)
+    # GPU, unit by unit
+    ds = H.DeviceState(wl, staged_scratch=False)
+    ds.upload_state(W0, m0, v0)
+    gs = torch.full((padded,), float("nan"), dtype=torch.float32, device="cuda")
+    for lo, hi in units:
+        ug = [H.bf16_from_u16(np.ascontiguousarray(g[lo:hi]), "cuda") for g in G]
+        z.zero3_rs_unit(ds.plan, ug, lo, hi, gs, flags=z.ZERO_FLAG_CHECK_FINITE,
+                        dev_status=ds.status)
+    shards = torch.full((padded,), CANARY, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    z.zero3_update(ds.plan, gs, ds.W, ds.m, ds.v, shards, ds.hp, 3)
+    torch.cuda.synchronize()
+    g_gpu = gs.cpu().numpy()
+    assert np.array_equal(np.isnan(g_gpu), np.isnan(g_or))          # pad untouched
+    fin = ~np.isnan(g_or)
+    assert np.array_equal(g_gpu[fin].view(np.uint32), g_or[fin].view(np.uint32))
+    for t, a in ((ds.W, Wz), (ds.m, mz), (ds.v, vz)):
+        assert np.array_equal(t.cpu().numpy().view(np.uint32)[:n], a.view(np.uint32)[:n])
+    assert np.array_equal(H.u16_from_bf16(shards), Ps)              # pad included
+    assert int(ds.status.item()) == 0
+    # the whole-step kernel gives the same bits
+    ds2 = H.DeviceState(wl, staged_scratch=False)
+    ds2.upload_state(W0, m0, v0)
+    ds2.upload_grads(G)
+    shards2 = torch.full((padded,), CANARY, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    z.zero3_step(ds2.plan, ds2.grads, ds2.W, ds2.m, ds2.v, shards2, ds2.hp, 3)
+    torch.cuda.synchronize()
+    assert torch.equal(shards2.view(torch.int16), shards.view(torch.int16))
+    assert torch.equal(ds2.W.view(torch.int32), ds.W.view(torch.int32))
+
+
+def test_unit_reduce_scatter_reports_non_finite():
+    wl = W.flat(4, 1, 3000, seed=5, step=1)
+    G, W0, m0, v0 = H.host_inputs(wl, 1)
+    G[2][1234] = 0x7F80                                      # +Inf in rank 2's gradient
+    ds = H.DeviceState(wl, staged_scratch=False)
+    gs = torch.zeros(ds.padded, dtype=torch.float32, device="cuda")
+    lo, hi = 1001, 2999
+    ug = [H.bf16_from_u16(np.ascontiguousarray(g[lo:hi]), "cuda") for g in G]
+    z.zero3_rs_unit(ds.plan, ug, lo, hi, gs, flags=z.ZERO_FLAG_CHECK_FINITE, dev_status=ds.status)
+    torch.cuda.synchronize()
+    assert int(ds.status.item()) & z.ZERO_DEV_NONFINITE
+    assert torch.isinf(gs[1234]).item()
+
+
+def test_full_size_unit_reduce_scatter_llama_layers():
+    """The 1B-shaped workload with one unit per transformer layer (plus the
+    embedding and the final norm), the backward's order (last unit first),
+    each unit's gradient read in place from the full gradient buffers; the
+    result equals zero3_step everywhere."""
+    wl = W.llama32_1b()
+    ds = H.DeviceState(wl, staged_scratch=False)
+    ds.fill_state_device()
+    ds.fill_grads_device(wl.step)
+    offs = [int(o) for o in wl.offsets]
+    # embedding, 16 layers of 9 tensors, final norm
+    bounds = [offs[0], offs[1]] + [offs[1 + 9 * k] for k in range(1, 17)] + [offs[-1]]
+    bounds = sorted(set(bounds))
+    units = list(zip(bounds[:-1], bounds[1:]))[::-1]
+    assert units[-1][0] == 0 and max(h for _, h in units) == ds.N
+    gs = torch.empty(ds.padded, dtype=torch.float32, device="cuda")
+    for lo, hi in units:
+        assert lo % 8 == 0                                   # slices stay 16-byte aligned
+        z.zero3_rs_unit(ds.plan, [g[lo:hi] for g in ds.grads], lo, hi, gs,
+                        flags=z.ZERO_FLAG_CHECK_FINITE, dev_status=ds.status)
+    shards = torch.empty(ds.padded, dtype=torch.bfloat16, device="cuda")
+    W1 = ds.W.clone()
+    m1, v1 = ds.m.clone(), ds.v.clone()
+    z.zero3_update(ds.plan, gs, W1, m1, v1, shards, ds.hp, wl.step)
+    shards_ref = torch.empty(ds.padded, dtype=torch.bfloat16, device="cuda")
+    z.zero3_step(ds.plan, ds.grads, ds.W, ds.m, ds.v, shards_ref, ds.hp, wl.step)
+    torch.cuda.synchronize()
+    N = ds.N
+    assert torch.equal(shards[:N].view(torch.int16), shards_ref[:N].view(torch.int16))
+    for a, b in ((W1, ds.W), (m1, ds.m), (v1, ds.v)):
+        assert torch.equal(a[:N].view(torch.int32), b[:N].view(torch.int32))
+    assert int(ds.status.item()) == 0

@@ -47,7 +47,8 @@ EXPORTED = ("zero_abi_version", "zero_status_string", "zero_plan_create", "zero_
             "zero_step_host", "zero_step_staged_noalloc", "zero_step_clipped",
             "zero_clip_scratch_bytes", "zero3_step", "zero3_gather", "zero_ckpt_write_host",
             "zero_ckpt_read_host", "zero_ckpt_save_async", "zero_ckpt_job_wait",
-            "zero_ckpt_load", "zero_step_compressed", "zero_check_replicas", "zero_step_onebit")
+            "zero_ckpt_load", "zero_step_compressed", "zero_check_replicas", "zero_step_onebit",
+            "zero3_rs_unit", "zero3_update")
 
 
 class ZeroError(RuntimeError):
@@ -142,6 +143,11 @@ def lib():
         L.zero_step_onebit.argtypes = [P(zero_plan_t), vp, vp, vp, vp, vp,
                                        P(zero_adamw_hparams), i64, i64, vp, vp, vp]
         L.zero_step_onebit.restype = ctypes.c_int
+        L.zero3_rs_unit.argtypes = [P(zero_plan_t), vp, i64, i64, vp, i32, vp, vp]
+        L.zero3_rs_unit.restype = ctypes.c_int
+        L.zero3_update.argtypes = [P(zero_plan_t), vp, vp, vp, vp, vp, P(zero_adamw_hparams), i64,
+                                   vp]
+        L.zero3_update.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -575,3 +581,31 @@ def zero_step_onebit(plan: Plan, rank_grads, master, m, v, rank_params,
                                   _addr(v), ctypes.addressof(pa), ctypes.byref(hp), step,
                                   freeze_step, ctypes.addressof(ea), _addr(server_residual),
                                   _stream(stream)), "zero_step_onebit")
+
+
+def zero3_rs_unit(plan: Plan, unit_grads, lo: int, hi: int, grad_shards, flags: int = 0,
+                  dev_status=None, stream=None) -> None:
+    """Reduce-scatter one unit's gradients (R*M bf16 device tensors of
+    hi - lo each) into the owners' fp32 gradient shards (plan.padded floats)."""
+    c = plan.c
+    if len(unit_grads) != c.R * c.M:
+        raise ValueError(f"need {c.R * c.M} unit gradient buffers")
+    for k, g in enumerate(unit_grads):
+        _check_tensor(g, "bf16", hi - lo, f"unit_grads[{k}]")
+    _check_tensor(grad_shards, "f32", c.padded, "grad_shards")
+    ga = _ptrs([_addr(g) for g in unit_grads])
+    _check(lib().zero3_rs_unit(plan.ptr, ctypes.addressof(ga), lo, hi, _addr(grad_shards), flags,
+                               _addr(dev_status), _stream(stream)), "zero3_rs_unit")
+
+
+def zero3_update(plan: Plan, grad_shards, master, m, v, param_shards, hp: zero_adamw_hparams,
+                 step: int, stream=None) -> None:
+    """AdamW of every owned element from the reduce-scattered fp32 gradient
+    shards, then the bf16 cast into each rank's own parameter shard."""
+    c = plan.c
+    for nm, t in (("grad_shards", grad_shards), ("master", master), ("m", m), ("v", v)):
+        _check_tensor(t, "f32", c.padded, nm)
+    _check_tensor(param_shards, "bf16", c.padded, "param_shards")
+    _check(lib().zero3_update(plan.ptr, _addr(grad_shards), _addr(master), _addr(m), _addr(v),
+                              _addr(param_shards), ctypes.byref(hp), step, _stream(stream)),
+           "zero3_update")
