@@ -607,7 +607,64 @@ def run_table(args):
                        "frac_of_measured_peak": round(b * wl.N / (ms / 1e3) / 1e9 / peak, 4)}
                 rows.append(row)
                 print(json.dumps(row), flush=True)
-            del gs
+            # the same backward with each layer's parameters all-gathered
+            # again before its reduce-scatter (FSDP materialises a unit for
+            # its backward) into one of two transient buffers: all on one
+            # stream, then with the next layer's gather prefetched on a second
+            # stream (it waits only for its buffer to be released)
+            umax = max(hi - lo for lo, hi in units)
+            bufs = [torch.empty(umax, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+            main, side = torch.cuda.current_stream(), torch.cuda.Stream()
+            unit_grads = [[g[lo:hi] for g in ds.grads] for lo, hi in units]
+
+            def serial():
+                for k, (lo, hi) in enumerate(units):
+                    z.zero3_gather(ds.plan, shards, lo, hi, [bufs[k % 2][:hi - lo]])
+                    z.zero3_rs_unit(ds.plan, unit_grads[k], lo, hi, gs)
+
+            def prefetched():
+                gathered = [torch.cuda.Event() for _ in units]
+                released = [torch.cuda.Event() for _ in units]
+                side.wait_stream(main)
+
+                def issue(k):
+                    lo, hi = units[k]
+                    if k >= 2:
+                        side.wait_event(released[k - 2])
+                    z.zero3_gather(ds.plan, shards, lo, hi, [bufs[k % 2][:hi - lo]], stream=side)
+                    gathered[k].record(side)
+
+                issue(0)
+                for k, (lo, hi) in enumerate(units):
+                    if k + 1 < len(units):
+                        issue(k + 1)
+                    main.wait_event(gathered[k])
+                    z.zero3_rs_unit(ds.plan, unit_grads[k], lo, hi, gs)
+                    released[k].record(main)
+
+            b = 4 + 2 * wl.R * wl.M + 4
+            for label, fn in (("gather + reduce-scatter per layer, one stream", serial),
+                              ("gather + reduce-scatter per layer, next gather prefetched "
+                               "on a second stream", prefetched)):
+                ts = []
+                for k in range(3 + 10):
+                    flush.fill_(k & 0xFF)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    fn()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    if k >= 3:
+                        ts.append(e0.elapsed_time(e1))
+                ms = float(np.median(ts))
+                row = {"workload": name, "R": wl.R, "M": wl.M, "N": wl.N,
+                       "variant": "zero3_backward", "part": label, "launches": 2 * len(units),
+                       "ms": round(ms, 4), "params_per_s": wl.N / (ms / 1e3), "bytes_per_param": b,
+                       "GB_s": round(b * wl.N / (ms / 1e3) / 1e9, 1),
+                       "frac_of_measured_peak": round(b * wl.N / (ms / 1e3) / 1e9 / peak, 4)}
+                rows.append(row)
+                print(json.dumps(row), flush=True)
+            del gs, bufs, unit_grads
         del ds, shards
         torch.cuda.empty_cache()
 

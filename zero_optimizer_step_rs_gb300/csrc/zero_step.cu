@@ -532,7 +532,7 @@ cudaError_t launch_rs(const StagedArgs& a, cudaStream_t st)
     const int R = a.R, M = a.M;
     const int64_t work = (a.S + kUnit - 1) / kUnit;      // at most one block per unit of a shard
     auto go = [&](const void* k, auto kern) {
-        const int64_t per_rank = ((int64_t)grid_for(k, work * a.R) + a.R - 1) / a.R;
+        const int64_t per_rank = (int64_t)grid_for(k, work * a.R) / a.R;    // never past one wave
         dim3 grid((unsigned)(per_rank < 1 ? 1 : per_rank), (unsigned)a.R);
         kern<<<grid, kThreads, 0, st>>>(a);
         return cudaGetLastError();
@@ -551,7 +551,7 @@ cudaError_t launch_adamw(const StagedArgs& a, cudaStream_t st)
 {
     const void* k = reinterpret_cast<const void*>(&k_adamw);
     const int64_t work = (a.S / kVec + kThreads - 1) / kThreads;
-    const int64_t per_rank = ((int64_t)grid_for(k, work * a.R) + a.R - 1) / a.R;
+    const int64_t per_rank = (int64_t)grid_for(k, work * a.R) / a.R;    // never past one wave
     dim3 grid((unsigned)(per_rank < 1 ? 1 : per_rank), (unsigned)a.R);
     k_adamw<<<grid, kThreads, 0, st>>>(a);
     return cudaGetLastError();
@@ -561,7 +561,7 @@ cudaError_t launch_ag(const StagedArgs& a, cudaStream_t st)
 {
     const int64_t work = (a.S / 8 + kThreads - 1) / kThreads;
     auto go = [&](const void* k, auto kern) {
-        const int64_t per_rank = ((int64_t)grid_for(k, work * a.R) + a.R - 1) / a.R;
+        const int64_t per_rank = (int64_t)grid_for(k, work * a.R) / a.R;    // never past one wave
         dim3 grid((unsigned)(per_rank < 1 ? 1 : per_rank), (unsigned)a.R);
         kern<<<grid, kThreads, 0, st>>>(a);
         return cudaGetLastError();
