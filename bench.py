@@ -480,6 +480,9 @@ def run_table(args):
     peak = float(peaks.get("hbm_gbs", 6800.0))
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
     rows = []
+    sampler = ClockSampler(gpu_uuid(0))          # SM clocks over the GPU part
+    sampler.start()
+    sampler.mark_start()
 
     def timed(ds, variant, reps):
         ts = []
@@ -552,17 +555,30 @@ def run_table(args):
             layers = [0, offs[1]] + [offs[1 + 9 * (l + 1)] for l in range(16)] + [offs[-1]]
             layers = sorted(set(layers))
             full = torch.empty(wl.N, dtype=torch.bfloat16, device="cuda")
-            for label, cuts in (("unit = tensor (146 units)", offs),
-                                ("unit = layer (18 units)", layers),
-                                ("unit = whole model (1 unit)", [0, wl.N])):
+            for label, cuts, graph in (("unit = tensor (146 units)", offs, False),
+                                       ("unit = tensor (146 units), one CUDA graph", offs, True),
+                                       ("unit = layer (18 units)", layers, False),
+                                       ("unit = layer (18 units), one CUDA graph", layers, True),
+                                       ("unit = whole model (1 unit)", [0, wl.N], False)):
+                def gather_all():
+                    for lo, hi in zip(cuts[:-1], cuts[1:]):
+                        z.zero3_gather(ds.plan, shards, lo, hi, [full[:hi - lo]])
+                run = gather_all
+                if graph:
+                    # the same launches captured once and replayed: no host
+                    # work between them (the eager rows above have already
+                    # run every kernel once)
+                    cg = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(cg):
+                        gather_all()
+                    run = cg.replay
                 ts = []
                 for k in range(3 + 10):
                     flush.fill_(k & 0xFF)
                     e0 = torch.cuda.Event(enable_timing=True)
                     e1 = torch.cuda.Event(enable_timing=True)
                     e0.record()
-                    for lo, hi in zip(cuts[:-1], cuts[1:]):
-                        z.zero3_gather(ds.plan, shards, lo, hi, [full[:hi - lo]])
+                    run()
                     e1.record()
                     torch.cuda.synchronize()
                     if k >= 3:
@@ -771,6 +787,11 @@ def run_table(args):
         while S <= 256 * 1024 * 1024:
             measure(W.sweep_point(R, S), f"sweep R={R} S={S}", reps=20, variants=(0,))
             S *= 4
+
+    sampler.mark_stop()
+    row = {"clocks": sampler.stop(), "scope": "every GPU row of the table"}
+    rows.append(row)
+    print(json.dumps(row), flush=True)
 
     # oracle on 1 core and on all cores, per workload, first 2^22 params
     for name in ("tiny", "gpt2-small", "llama-3.2-1b", "uneven", "large"):

@@ -50,9 +50,10 @@ def test_compressed_step_matches_oracle(kind, ef, n):
 
 
 @pytest.mark.parametrize("kind", KINDS)
-@pytest.mark.parametrize("R,M", [(8, 1), (7, 4), (3, 2), (64, 4), (1, 256)])
-def test_compressed_rank_microbatch_pairs(kind, R, M):
-    _run(W.flat(R, M, 20_011, seed=R + M, step=1, state="synthetic"), kind, True, [1, 2])
+@pytest.mark.parametrize("R,M", [(8, 1), (4, 1), (7, 4), (3, 2), (64, 4), (1, 256)])
+@pytest.mark.parametrize("ef", [False, True])
+def test_compressed_rank_microbatch_pairs(kind, R, M, ef):
+    _run(W.flat(R, M, 20_011, seed=R + M, step=1, state="synthetic"), kind, ef, [1, 2])
 
 
 def test_compressed_uneven_workload_scaled():
@@ -124,3 +125,75 @@ def test_int8_codes_at_half_integer_quotients():
     torch.cuda.synchronize()
     res = H.compare(ds.result(), (Wc, mc, vc, Pc))
     assert not {k: v for k, v in res.items() if v}, res
+
+
+def _regime_block(rng, regime):
+    """128 bf16 bit patterns of one block in one magnitude regime."""
+    sign = rng.integers(0, 2, 128).astype(np.uint32) << 31
+    if regime == "zero":
+        f = np.zeros(128, np.float32)
+    elif regime == "single":
+        f = np.zeros(128, np.float32)
+        f[rng.integers(0, 128)] = np.float32(2.0 ** int(rng.integers(-20, 20)))
+    elif regime == "subnormal":                    # bf16 subnormals, 2^-133 .. 2^-127
+        f = (rng.uniform(1, 2, 128) * 2.0 ** rng.integers(-133, -127, 128)).astype(np.float32)
+    elif regime == "tiny":                         # block scale below 2^-100
+        f = (rng.uniform(1, 2, 128) * 2.0 ** int(rng.integers(-126, -108))).astype(np.float32)
+    elif regime == "huge":                         # block scale around and above 2^100
+        f = (rng.uniform(1, 2, 128) * 2.0 ** int(rng.integers(100, 114))).astype(np.float32)
+    elif regime == "halfint":                      # quotients near j + 1/2 (as bf16 allows)
+        A = np.float32(rng.uniform(1, 2) * 2.0 ** int(rng.integers(-40, 40)))
+        s = np.float64(A) / 127.0
+        j = rng.integers(-127, 127, 128)
+        f = np.minimum(np.abs(((j + 0.5) * s).astype(np.float32)), A)
+        f[0] = A
+    else:                                          # "normal": mixed magnitudes
+        f = (rng.standard_normal(128) * 10.0 ** int(rng.integers(-6, 1))).astype(np.float32)
+    bits = (np.abs(f).view(np.uint32) | sign) >> 16
+    return bits.astype(np.uint16)
+
+
+@pytest.mark.parametrize("kind", KINDS[1:])
+@pytest.mark.parametrize("R,M", [(8, 1), (4, 1), (7, 4), (2, 3)])
+@pytest.mark.parametrize("ef", [False, True])
+def test_codecs_on_extreme_blocks(kind, R, M, ef):
+    """int8 and sign codecs on blocks of zeros, a single value, bf16
+    subnormals, scales far below and above the reciprocal path's range,
+    quotients near half-integers and mixed magnitudes, for the compile-time
+    (R, M) cases (8, 1), (4, 1), (7, 4) and a run-time one, with a ragged last
+    block; two steps, so the error-feedback residuals are used."""
+    gk, ok = kind
+    rng = np.random.default_rng(R * 100 + M + (7 if ef else 0) + gk)
+    regimes = ["zero", "single", "subnormal", "tiny", "huge", "halfint", "normal"]
+    nblk = 3 * len(regimes)
+    n = nblk * 128 + 37
+    idx = np.arange(n, dtype=np.int64)
+    wl = W.flat(R, M, n, seed=R + M, step=1, state="synthetic")
+    _, W0, m0, v0 = H.host_inputs(wl, 1)
+    Wc, mc, vc = W0.copy(), m0.copy(), v0.copy()
+    Pc = [np.zeros(n, np.uint16) for _ in range(R)]
+    Ec = [np.zeros(n, np.float32) for _ in range(R)] if ef else None
+    ds = H.DeviceState(wl, staged_scratch=False)
+    ds.upload_state(W0, m0, v0)
+    Ed = [torch.zeros(n, dtype=torch.float32, device="cuda") for _ in range(R)] if ef else None
+    hp = oracle.hparams(**wl.hparams())
+    for t in (1, 2):
+        G = []
+        for q in range(R * M):
+            g = np.empty(n, np.uint16)
+            for b in range(nblk + 1):
+                blk = _regime_block(rng, regimes[int(rng.integers(0, len(regimes)))])
+                g[b * 128:min(n, b * 128 + 128)] = blk[:min(128, n - b * 128)]
+            G.append(g)
+        oracle.dp_step_compressed(G, Wc, mc, vc, Pc, hp, t, R, M, ok, Ec)
+        ds.upload_grads(G)
+        z.zero_step_compressed(ds.plan, ds.grads, ds.W, ds.m, ds.v, ds.params, ds.hp, t, gk, Ed)
+    torch.cuda.synchronize()
+    res = H.compare(ds.result(), (Wc, mc, vc, Pc))
+    assert not {k: v for k, v in res.items() if v}, res
+    if ef:
+        for e_d, e_c in zip(Ed, Ec):
+            got, want = e_d.cpu().numpy(), e_c
+            nan = np.isnan(want)
+            assert np.array_equal(np.isnan(got), nan)
+            assert np.array_equal(got.view(np.uint32)[~nan], want.view(np.uint32)[~nan])

@@ -1140,7 +1140,7 @@ __global__ void __launch_bounds__(kThreads) k_adamw_ag(const __grid_constant__ C
     const ClipCtl c = *a.ctl;
     if (c.skip) return;
     const int R = RC > 0 ? RC : a.R;
-    constexpr int U = 2;
+    constexpr int U = 4;
     constexpr int T = kUnit * U;
     const int64_t n = a.n;
     const int64_t full_tiles = n / T;
@@ -1216,7 +1216,7 @@ cudaError_t launch_rs_norm(const ClipArgs& a, cudaStream_t st)
 
 cudaError_t launch_adamw_ag(const ClipArgs& a, cudaStream_t st)
 {
-    const int64_t work = (a.n + 2 * kUnit - 1) / (2 * kUnit);     // tiles of 2 units
+    const int64_t work = (a.n + 4 * kUnit - 1) / (4 * kUnit);     // tiles of 4 units
     auto go = [&](const void* k, auto kern) {
         kern<<<grid_for(k, work < 1 ? 1 : work), kThreads, 0, st>>>(a);
         return cudaGetLastError();
@@ -1352,6 +1352,9 @@ __device__ __forceinline__ float quot_by_recip(float x, float b, float r)
 //          instruction issue);
 //   POW2   a full sign block's |x| sum scaled by the exact 2^-7 instead of
 //          divided by 128 (taken with error feedback).
+// Without error feedback the full blocks of the compile-time (R, M) cases go
+// through int8_transposed and sign_transposed below, which give these bits
+// too with fewer instructions.
 template <int KIND, bool RECIP = false, bool POW2 = false>
 __device__ __forceinline__ void codec(float (&x)[4], const bool (&valid)[4], int64_t block_count,
                                       float (&d)[4])
@@ -1417,6 +1420,125 @@ __device__ __forceinline__ void codec(float (&x)[4], const bool (&valid)[4], int
                                                            : __fdiv_rn(t, (float)block_count);
 #pragma unroll
         for (int k = 0; k < 4; ++k) d[k] = x[k] < 0.0f ? -sc : sc;
+    }
+}
+
+// int8 codec of every rank's full block without error feedback, with the
+// block scales computed across lanes: lane l derives the scale and its
+// reciprocal of rank l % RC once, instead of every lane for every rank, and
+// rank r's pair is then broadcast from lane r.  Inside the fast range of
+// quot_by_recip the clamp to [-127, 127] and the zero-scale test are no-ops:
+// |x| <= amax and sc = RN(amax / 127) >= (amax / 127)(1 - 2^-24) give
+// |x / sc| < 127 (1 + 2^-23) < 127.5, so the rounded quotient is at most 127
+// in magnitude.  Outside that range the codec's IEEE path runs unchanged.
+template <int RC, int MC>
+__device__ __forceinline__ void int8_transposed(const uint2 (&gx)[RC * MC], int lane,
+                                                float (&acc)[4])
+{
+    float x[RC][4];
+    uint32_t amax[RC];
+#pragma unroll
+    for (int r = 0; r < RC; ++r) {
+#pragma unroll
+        for (int j = 0; j < MC; ++j) {
+            const uint2 u = gx[r * MC + j];
+            const float y[4] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y)};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x[r][k] = j == 0 ? y[k] : __fadd_rn(x[r][k], y[k]);
+        }
+        uint32_t mx = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mx = max(mx, __float_as_uint(x[r][k]) & 0x7FFFFFFFu);
+        amax[r] = __reduce_max_sync(0xFFFFFFFFu, mx);
+    }
+    const int mine = lane % RC;
+    uint32_t am = amax[0];
+#pragma unroll
+    for (int r = 1; r < RC; ++r) am = mine == r ? amax[r] : am;
+    const float sc_l = __fdiv_rn(__uint_as_float(am), 127.0f);
+    const float rc_l = __frcp_rn(sc_l);
+#pragma unroll
+    for (int r = 0; r < RC; ++r) {
+        const float sc = __shfl_sync(0xFFFFFFFFu, sc_l, r);
+        const float rc = __shfl_sync(0xFFFFFFFFu, rc_l, r);
+        float d[4];
+        if (sc >= 0x1p-100f && sc <= 0x1p100f) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) d[k] = __fmul_rn(rintf(quot_by_recip(x[r][k], sc, rc)), sc);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (sc == 0.0f) {
+                    d[k] = 0.0f;
+                } else {
+                    float q = rintf(__fdiv_rn(x[r][k], sc));
+                    q = fminf(fmaxf(q, -127.0f), 127.0f);
+                    d[k] = __fmul_rn(q, sc);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] = r == 0 ? d[k] : __fadd_rn(acc[k], d[k]);
+    }
+}
+
+// sign codec of every rank's full block without error feedback, the RC
+// block sums reduced together: at each of the first log2(RC) levels of the
+// lane tree a lane keeps half of its remaining ranks and receives its
+// partner's values of them (one shuffle per kept rank instead of one per
+// rank), so lane l ends with rank rank_of(l); the last levels and the
+// division by the count run once per lane, and each rank's magnitude is then
+// broadcast from a lane that holds it.  The additions pair the same lanes as
+// the shuffle-down tree of the codec (lanes 2i and 2i+1, then pairs of pairs,
+// ...), and a + b == b + a in IEEE arithmetic, so every sum has the same bits.
+template <int RC, int MC>
+__device__ __forceinline__ void sign_transposed(const uint2 (&gx)[RC * MC], int lane,
+                                                float (&acc)[4])
+{
+    static_assert((RC & (RC - 1)) == 0 && RC <= 32, "RC must be a power of two");
+    constexpr int P = RC == 1 ? 0 : RC == 2 ? 1 : RC == 4 ? 2 : RC == 8 ? 3 : RC == 16 ? 4 : 5;
+    float x[RC][4];
+    float cur[RC];
+#pragma unroll
+    for (int r = 0; r < RC; ++r) {
+#pragma unroll
+        for (int j = 0; j < MC; ++j) {
+            const uint2 u = gx[r * MC + j];
+            const float y[4] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y)};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x[r][k] = j == 0 ? y[k] : __fadd_rn(x[r][k], y[k]);
+        }
+        cur[r] = __fadd_rn(__fadd_rn(fabsf(x[r][0]), fabsf(x[r][1])),
+                           __fadd_rn(fabsf(x[r][2]), fabsf(x[r][3])));
+    }
+#pragma unroll
+    for (int lvl = 0; lvl < P; ++lvl) {
+        const int half = RC >> (lvl + 1);
+        const bool up = (lane >> lvl) & 1;
+#pragma unroll
+        for (int k = 0; k < half; ++k) {
+            const float send = up ? cur[k] : cur[k + half];
+            const float keep = up ? cur[k + half] : cur[k];
+            cur[k] = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 1 << lvl));
+        }
+    }
+#pragma unroll
+    for (int lvl = P; lvl < 5; ++lvl)
+        cur[0] = __fadd_rn(cur[0], __shfl_xor_sync(0xFFFFFFFFu, cur[0], 1 << lvl));
+    // a full block holds 128 elements: scaling by the exact 2^-7 rounds the
+    // same quotient as dividing by 128
+    const float sc_l = __fmul_rn(cur[0], 1.0f / kCompBlock);
+#pragma unroll
+    for (int r = 0; r < RC; ++r) {
+        int src = 0;                          // a lane whose kept rank is r
+#pragma unroll
+        for (int lvl = 0; lvl < P; ++lvl) src |= ((r >> (P - 1 - lvl)) & 1) << lvl;
+        const float sc = __shfl_sync(0xFFFFFFFFu, sc_l, src);
+        float d[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) d[k] = x[r][k] < 0.0f ? -sc : sc;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] = r == 0 ? d[k] : __fadd_rn(acc[k], d[k]);
     }
 }
 
@@ -1490,10 +1612,12 @@ __global__ void __launch_bounds__(kThreads) k_comp(const __grid_constant__ CompA
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         float4 w4, m4, v4;                        // the owner's state of a full block
         bool have_state = false;
-        // every rank's loads first - and the owner's state - then the codecs
-        // and their warp reductions, so the loads are all in flight before the
-        // first sync; fp16 without error feedback has no sync and runs faster
-        // in the rank-by-rank form (fewer registers, more blocks per SM)
+        // every rank's loads first, then the codecs and their warp reductions,
+        // so the loads are all in flight before the first sync.  Whether the
+        // owner's state joins them was measured per codec: it does for int8
+        // without error feedback (0.86 -> 0.96 of peak), and slows the others.
+        // fp16 without error feedback has no sync and runs faster in the
+        // rank-by-rank form (fewer registers, more blocks per SM).
         if constexpr (RC > 0 && MC > 0 && (KIND != ZERO_COMP_FP16 || EF)) {
             if (full) {
                 uint2 gx[RC * MC];
@@ -1504,30 +1628,41 @@ __global__ void __launch_bounds__(kThreads) k_comp(const __grid_constant__ CompA
 #pragma unroll
                     for (int r = 0; r < RC; ++r) ex[r] = ld_stream(a.E[r] + e);
                 }
-                have_state = false;
+                if constexpr (KIND == ZERO_COMP_INT8 && !EF) {
+                    w4 = ld_stream(a.W + e);
+                    m4 = ld_stream(a.m + e);
+                    v4 = ld_stream(a.v + e);
+                    have_state = true;
+                    int8_transposed<RC, MC>(gx, lane, acc);
+                } else if constexpr (KIND == ZERO_COMP_SIGN && !EF && (RC & (RC - 1)) == 0) {
+                    sign_transposed<RC, MC>(gx, lane, acc);
+                } else {
 #pragma unroll
-                for (int r = 0; r < RC; ++r) {
-                    float x[4];
+                    for (int r = 0; r < RC; ++r) {
+                        float x[4];
 #pragma unroll
-                    for (int j = 0; j < MC; ++j) {
-                        const uint2 u = gx[r * MC + j];
-                        const float y[4] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y)};
+                        for (int j = 0; j < MC; ++j) {
+                            const uint2 u = gx[r * MC + j];
+                            const float y[4] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y),
+                                                bf16_hi(u.y)};
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) x[k] = j == 0 ? y[k] : __fadd_rn(x[k], y[k]);
+                            for (int k = 0; k < 4; ++k) x[k] = j == 0 ? y[k] : __fadd_rn(x[k], y[k]);
+                        }
+                        if constexpr (EF) {
+                            x[0] = __fadd_rn(x[0], ex[r].x);
+                            x[1] = __fadd_rn(x[1], ex[r].y);
+                            x[2] = __fadd_rn(x[2], ex[r].z);
+                            x[3] = __fadd_rn(x[3], ex[r].w);
+                        }
+                        float d[4];
+                        codec<KIND, !EF, EF>(x, valid, block_count, d);
+                        if constexpr (EF)
+                            st_stream(a.E[r] + e,
+                                      make_float4(__fsub_rn(x[0], d[0]), __fsub_rn(x[1], d[1]),
+                                                  __fsub_rn(x[2], d[2]), __fsub_rn(x[3], d[3])));
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) acc[k] = r == 0 ? d[k] : __fadd_rn(acc[k], d[k]);
                     }
-                    if constexpr (EF) {
-                        x[0] = __fadd_rn(x[0], ex[r].x);
-                        x[1] = __fadd_rn(x[1], ex[r].y);
-                        x[2] = __fadd_rn(x[2], ex[r].z);
-                        x[3] = __fadd_rn(x[3], ex[r].w);
-                    }
-                    float d[4];
-                    codec<KIND, !EF, EF>(x, valid, block_count, d);
-                    if constexpr (EF)
-                        st_stream(a.E[r] + e, make_float4(__fsub_rn(x[0], d[0]), __fsub_rn(x[1], d[1]),
-                                                          __fsub_rn(x[2], d[2]), __fsub_rn(x[3], d[3])));
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) acc[k] = r == 0 ? d[k] : __fadd_rn(acc[k], d[k]);
                 }
             } else {
                 comp_ranks_generic<KIND, EF>(a, R, M, e, full, valid, block_count, acc);
