@@ -1482,35 +1482,28 @@ __device__ __forceinline__ void int8_transposed(const uint2 (&gx)[RC * MC], int 
     }
 }
 
-// sign codec of every rank's full block without error feedback, the RC
-// block sums reduced together: at each of the first log2(RC) levels of the
-// lane tree a lane keeps half of its remaining ranks and receives its
-// partner's values of them (one shuffle per kept rank instead of one per
-// rank), so lane l ends with rank rank_of(l); the last levels and the
-// division by the count run once per lane, and each rank's magnitude is then
-// broadcast from a lane that holds it.  The additions pair the same lanes as
-// the shuffle-down tree of the codec (lanes 2i and 2i+1, then pairs of pairs,
-// ...), and a + b == b + a in IEEE arithmetic, so every sum has the same bits.
-template <int RC, int MC>
-__device__ __forceinline__ void sign_transposed(const uint2 (&gx)[RC * MC], int lane,
-                                                float (&acc)[4])
+// Magnitudes of the sign codec for RC full blocks at once (x[r] holds a
+// lane's 4 elements of rank r's block): sc[r] = (pairwise sum of |x| over
+// the block) / 128, the RC sums reduced together.  At each of the first
+// log2(RC) levels of the lane tree a lane keeps half of its remaining ranks
+// and receives its partner's values of them (one shuffle per kept rank
+// instead of one per rank), so lane l ends with one rank; the last levels and
+// the scaling run once per lane, and each rank's magnitude is then broadcast
+// from a lane that holds it.  The additions pair the same lanes as the
+// shuffle-down tree of the codec (lanes 2i and 2i+1, then pairs of pairs,
+// ...), and a + b == b + a in IEEE arithmetic, so every sum has the same bits;
+// scaling by the exact 2^-7 rounds the same quotient as dividing by 128.
+template <int RC>
+__device__ __forceinline__ void sign_scales_joint(const float (&x)[RC][4], int lane,
+                                                  float (&sc)[RC])
 {
     static_assert((RC & (RC - 1)) == 0 && RC <= 32, "RC must be a power of two");
     constexpr int P = RC == 1 ? 0 : RC == 2 ? 1 : RC == 4 ? 2 : RC == 8 ? 3 : RC == 16 ? 4 : 5;
-    float x[RC][4];
     float cur[RC];
 #pragma unroll
-    for (int r = 0; r < RC; ++r) {
-#pragma unroll
-        for (int j = 0; j < MC; ++j) {
-            const uint2 u = gx[r * MC + j];
-            const float y[4] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y)};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) x[r][k] = j == 0 ? y[k] : __fadd_rn(x[r][k], y[k]);
-        }
+    for (int r = 0; r < RC; ++r)
         cur[r] = __fadd_rn(__fadd_rn(fabsf(x[r][0]), fabsf(x[r][1])),
                            __fadd_rn(fabsf(x[r][2]), fabsf(x[r][3])));
-    }
 #pragma unroll
     for (int lvl = 0; lvl < P; ++lvl) {
         const int half = RC >> (lvl + 1);
@@ -1525,18 +1518,40 @@ __device__ __forceinline__ void sign_transposed(const uint2 (&gx)[RC * MC], int 
 #pragma unroll
     for (int lvl = P; lvl < 5; ++lvl)
         cur[0] = __fadd_rn(cur[0], __shfl_xor_sync(0xFFFFFFFFu, cur[0], 1 << lvl));
-    // a full block holds 128 elements: scaling by the exact 2^-7 rounds the
-    // same quotient as dividing by 128
     const float sc_l = __fmul_rn(cur[0], 1.0f / kCompBlock);
 #pragma unroll
     for (int r = 0; r < RC; ++r) {
         int src = 0;                          // a lane whose kept rank is r
 #pragma unroll
         for (int lvl = 0; lvl < P; ++lvl) src |= ((r >> (P - 1 - lvl)) & 1) << lvl;
-        const float sc = __shfl_sync(0xFFFFFFFFu, sc_l, src);
+        sc[r] = __shfl_sync(0xFFFFFFFFu, sc_l, src);
+    }
+}
+
+// sign codec of every rank's full block without error feedback, through
+// sign_scales_joint, and the decoded values summed in rank order
+template <int RC, int MC>
+__device__ __forceinline__ void sign_transposed(const uint2 (&gx)[RC * MC], int lane,
+                                                float (&acc)[4])
+{
+    float x[RC][4];
+#pragma unroll
+    for (int r = 0; r < RC; ++r) {
+#pragma unroll
+        for (int j = 0; j < MC; ++j) {
+            const uint2 u = gx[r * MC + j];
+            const float y[4] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y)};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x[r][k] = j == 0 ? y[k] : __fadd_rn(x[r][k], y[k]);
+        }
+    }
+    float sc[RC];
+    sign_scales_joint<RC>(x, lane, sc);
+#pragma unroll
+    for (int r = 0; r < RC; ++r) {
         float d[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) d[k] = x[r][k] < 0.0f ? -sc : sc;
+        for (int k = 0; k < 4; ++k) d[k] = x[r][k] < 0.0f ? -sc[r] : sc[r];
 #pragma unroll
         for (int k = 0; k < 4; ++k) acc[k] = r == 0 ? d[k] : __fadd_rn(acc[k], d[k]);
     }
@@ -1879,6 +1894,8 @@ __global__ void __launch_bounds__(kThreads) k_onebit(const __grid_constant__ One
 #pragma unroll
         for (int k = 0; k < 4; ++k) valid[k] = e + k < n;
         float mo[4], es[4], w[4], vv[4], dsum[4];
+        float4 q_es, q_w, q_v;                    // the owner's state of a full block
+        bool have_owner = false;
         if (full) {
             const float4 q = ld_stream(a.m + e);
             mo[0] = q.x; mo[1] = q.y; mo[2] = q.z; mo[3] = q.w;
@@ -1896,6 +1913,46 @@ __global__ void __launch_bounds__(kThreads) k_onebit(const __grid_constant__ One
                 for (int q = 0; q < RC * MC; ++q) gx[q] = ld_stream(a.g.p[q] + e);
 #pragma unroll
                 for (int r = 0; r < RC; ++r) ex[r] = ld_stream(a.E[r] + e);
+                q_es = ld_stream(a.Es + e);
+                q_w = ld_stream(a.W + e);
+                q_v = ld_stream(a.v + e);
+                have_owner = true;
+                if constexpr ((RC & (RC - 1)) == 0) {
+                    // the worker codecs of all ranks, their block sums
+                    // reduced together (sign_scales_joint)
+                    float x[RC][4];
+#pragma unroll
+                    for (int r = 0; r < RC; ++r) {
+                        float loc[4];
+#pragma unroll
+                        for (int j = 0; j < MC; ++j) {
+                            const uint2 u = gx[r * MC + j];
+                            const float y[4] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y),
+                                                bf16_hi(u.y)};
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) loc[k] = j == 0 ? y[k] : __fadd_rn(loc[k], y[k]);
+                        }
+                        const float res[4] = {ex[r].x, ex[r].y, ex[r].z, ex[r].w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float gl = div_by(loc[k], a.s.denom_m, a.s.inv_m, a.s.m_pow2);
+                            const float ml = __fadd_rn(__fmul_rn(a.s.b1, mo[k]), __fmul_rn(a.s.omb1, gl));
+                            x[r][k] = __fadd_rn(ml, res[k]);
+                        }
+                    }
+                    float sc[RC];
+                    sign_scales_joint<RC>(x, lane, sc);
+#pragma unroll
+                    for (int r = 0; r < RC; ++r) {
+                        float d[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) d[k] = x[r][k] < 0.0f ? -sc[r] : sc[r];
+                        st_stream(a.E[r] + e, make_float4(__fsub_rn(x[r][0], d[0]), __fsub_rn(x[r][1], d[1]),
+                                                          __fsub_rn(x[r][2], d[2]), __fsub_rn(x[r][3], d[3])));
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) dsum[k] = r == 0 ? d[k] : __fadd_rn(dsum[k], d[k]);
+                    }
+                } else {
 #pragma unroll
                 for (int r = 0; r < RC; ++r) {
                     float loc[4];
@@ -1912,6 +1969,7 @@ __global__ void __launch_bounds__(kThreads) k_onebit(const __grid_constant__ One
                     st_stream(a.E[r] + e, make_float4(x[0], x[1], x[2], x[3]));
 #pragma unroll
                     for (int k = 0; k < 4; ++k) dsum[k] = r == 0 ? d[k] : __fadd_rn(dsum[k], d[k]);
+                }
                 }
             }
         }
@@ -1951,7 +2009,12 @@ __global__ void __launch_bounds__(kThreads) k_onebit(const __grid_constant__ One
         }
         // the owner: average, its residual, the codec again, the update
         if (full) {
-            const float4 q = ld_stream(a.Es + e), wq = ld_stream(a.W + e), vq = ld_stream(a.v + e);
+            if (!have_owner) {
+                q_es = ld_stream(a.Es + e);
+                q_w = ld_stream(a.W + e);
+                q_v = ld_stream(a.v + e);
+            }
+            const float4 q = q_es, wq = q_w, vq = q_v;
             es[0] = q.x; es[1] = q.y; es[2] = q.z; es[3] = q.w;
             w[0] = wq.x; w[1] = wq.y; w[2] = wq.z; w[3] = wq.w;
             vv[0] = vq.x; vv[1] = vq.y; vv[2] = vq.z; vv[3] = vq.w;
