@@ -76,3 +76,17 @@ def test_full_size_sampled(name, variant):
     assert replicas_equal, "replicas differ somewhere"
     assert pad_clean, "state pad written"
     assert status == 0, f"device status {status}"
+
+
+@pytest.mark.parametrize("R", [2, 4, 8])
+@pytest.mark.parametrize("S", [1 << 10, 1 << 16, 1 << 22, 1 << 28])
+def test_flat_sweep_points_sampled(R, S):
+    """The flat-vector sweep (fp32 master shard of 4 KB to 1 GB, N = R*S) at
+    its smallest, two middle and largest shard sizes: sampled parity of the
+    fused step against the oracle, replicas and pad checked everywhere.  The
+    largest point at R = 8 holds about 88 GB on the device."""
+    wl = W.sweep_point(R, S)
+    res, replicas_equal, pad_clean, status, k = _run_full(wl, z.ZERO_VARIANT_FUSED)
+    bad = {key: v for key, v in res.items() if v}
+    assert not bad, (wl.name, bad, k)
+    assert replicas_equal and pad_clean and status == 0
