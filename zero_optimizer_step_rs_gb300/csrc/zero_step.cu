@@ -272,12 +272,21 @@ int blocks_per_sm(int dev, const void* kernel)
     return nb;
 }
 
-// persistent grid: every SM gets its resident blocks, capped by the work
-unsigned grid_for(const void* kernel, int64_t work_blocks)
+// persistent grid: every SM gets its resident blocks, capped by the work.
+// quarter_blocks > 0 caps it further at quarter_blocks / 4 blocks per SM
+// once every block has at least 4 work units: for some kernels a sweep of
+// grid sizes on GB300 found HBM busier with fewer blocks than fit (the
+// launch sites give the measured values), while smaller launches, bound by
+// latency and ramp-up, run faster with every block that fits.
+unsigned grid_for(const void* kernel, int64_t work_blocks, int quarter_blocks = 0)
 {
     int dev = 0;
     cudaGetDevice(&dev);
-    const int64_t cap = (int64_t)device_sms(dev) * blocks_per_sm(dev, kernel);
+    int64_t cap = (int64_t)device_sms(dev) * blocks_per_sm(dev, kernel);
+    if (quarter_blocks > 0 && work_blocks >= 4 * cap) {
+        const int64_t q = (int64_t)quarter_blocks * device_sms(dev) / 4;
+        if (q >= 1 && q < cap) cap = q;
+    }
     int64_t g = work_blocks < cap ? work_blocks : cap;
     return (unsigned)(g < 1 ? 1 : g);
 }
@@ -366,13 +375,30 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ Fuse
 
 // ----------------------------------------------------- fused dispatch --
 
+// Blocks per SM (in quarters) of k_fused where fewer than the resident
+// maximum measured faster: whole-step time against grid size on GB300
+// (152 SMs) over the 1B- and 4B-shaped workloads and flat vectors of 0.4 to
+// 2 G params.  R=2: 2 blocks/SM, 0.93-0.94 -> 0.98 of the copy peak (4
+// resident).  R=4: 2.5, 0.94-0.95 -> 0.97 (4 resident).  ZeRO-3 output with
+// R=8: 2.75, 0.95-0.96 -> 0.98; with R=4: 3, 0.95 -> 0.98 (4 resident).  0
+// keeps the resident maximum (R=8 runs 2 blocks/SM, its maximum).
+template <int RC, int MC, int OUT>
+constexpr int fused_quarter_blocks()
+{
+    if (MC != 1) return 0;
+    if (OUT == 0) return RC == 2 ? 8 : RC == 4 ? 10 : 0;
+    if (OUT == 2) return RC == 8 ? 11 : RC == 4 ? 12 : 0;
+    return 0;
+}
+
 template <int RC, int MC, bool CHECK, int OUT = 0>
 cudaError_t launch_fused_t(const FusedArgs& a, cudaStream_t st)
 {
     constexpr int U = 2;
     const void* k = reinterpret_cast<const void*>(&k_fused<RC, MC, U, CHECK, OUT>);
     const int64_t tiles = (a.n + kUnit * U - 1) / (kUnit * U);
-    k_fused<RC, MC, U, CHECK, OUT><<<grid_for(k, tiles), kThreads, 0, st>>>(a);
+    const unsigned grid = grid_for(k, tiles, fused_quarter_blocks<RC, MC, OUT>());
+    k_fused<RC, MC, U, CHECK, OUT><<<grid, kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -2787,7 +2813,10 @@ extern "C" zero_status zero3_update(const zero_plan_t* plan, const float* grad_s
     a.s = step_scalars(*hp, step, plan->R, plan->M);
     const void* k = reinterpret_cast<const void*>(&k_z3_update);
     const int64_t work = (a.n / kVec + kThreads - 1) / kThreads;
-    k_z3_update<<<grid_for(k, work < 1 ? 1 : work), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    // 3 blocks per SM of the 5 that fit: 0.955 -> 0.98 of the copy peak on
+    // the 1B-shaped workload (grid-size sweep)
+    const unsigned grid = grid_for(k, work < 1 ? 1 : work, 12);
+    k_z3_update<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
     return cuda_status(cudaGetLastError());
 }
 
