@@ -557,8 +557,11 @@ cudaError_t launch_rs(const StagedArgs& a, cudaStream_t st)
 {
     const int R = a.R, M = a.M;
     const int64_t work = (a.S + kUnit - 1) / kUnit;      // at most one block per unit of a shard
+    // 4 blocks per SM (6 or 8 fit): 0.941 -> 0.957 of the copy peak for the
+    // staged step on the R=7, M=4 workload, +0.3-0.5 % on the others (grid-size
+    // sweep)
     auto go = [&](const void* k, auto kern) {
-        const int64_t per_rank = (int64_t)grid_for(k, work * a.R) / a.R;    // never past one wave
+        const int64_t per_rank = (int64_t)grid_for(k, work * a.R, 16) / a.R;    // never past one wave
         dim3 grid((unsigned)(per_rank < 1 ? 1 : per_rank), (unsigned)a.R);
         kern<<<grid, kThreads, 0, st>>>(a);
         return cudaGetLastError();
@@ -1752,7 +1755,12 @@ cudaError_t launch_comp_t(const CompArgs& a, cudaStream_t st)
     const void* k = reinterpret_cast<const void*>(&k_comp<RC, MC, KIND, EF>);
     const int64_t blocks = (a.n + kCompBlock - 1) / kCompBlock;   // one warp each
     const int64_t work = (blocks + kThreads / 32 - 1) / (kThreads / 32);
-    k_comp<RC, MC, KIND, EF><<<grid_for(k, work < 1 ? 1 : work), kThreads, 0, st>>>(a);
+    // the sign codec without error feedback: 3.5 blocks per SM of the 4 that
+    // fit, 0.962 -> 0.974 of the copy peak on the 1B-shaped workload and
+    // 0.98 -> 1.0 on the GPT-2-shaped one (grid-size sweep); every other
+    // codec measured fastest with all resident blocks
+    constexpr int quarters = (KIND == ZERO_COMP_SIGN && !EF) ? 14 : 0;
+    k_comp<RC, MC, KIND, EF><<<grid_for(k, work < 1 ? 1 : work, quarters), kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 
