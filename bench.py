@@ -452,6 +452,14 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"{world} independent replica(s) of an R={wl.R} "
                                   "emulated ZeRO group"},
         "hbm_gbs": round(alg_bytes / (ms_per_step / 1e3) / 1e9, 1),
+        # the pages' normalised collective bandwidth (CS336 Lecture 7 book,
+        # sections 5.2 and 5.3): a reduce-scatter or all-gather of a B-byte
+        # message over R ranks counts B (R-1)/R, an all-reduce twice that;
+        # the emulated step does one reduce-scatter and one all-gather of
+        # 2N-byte bf16 messages (micro-batches summed locally; ZeRO-3 has no
+        # all-gather in the step), timed by the whole step
+        "emulated_busbw_gbs": round((1 if zero3 else 2) * 2 * N * (wl.R - 1) / wl.R
+                                    / (ms_per_step / 1e3) / 1e9, 1),
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
