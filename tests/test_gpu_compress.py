@@ -197,3 +197,12 @@ def test_codecs_on_extreme_blocks(kind, R, M, ef):
             nan = np.isnan(want)
             assert np.array_equal(np.isnan(got), nan)
             assert np.array_equal(got.view(np.uint32)[~nan], want.view(np.uint32)[~nan])
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("ef", [False, True])
+def test_compressed_step_at_a_persistent_grid_size(kind, ef):
+    """4 M elements at R = 8: enough 128-element blocks that every launch
+    runs its persistent grid (for the sign codec without error feedback the
+    grid below the resident maximum), whole vector against the oracle."""
+    _run(W.flat(8, 1, 4_000_037, seed=41, step=1, state="synthetic"), kind, ef, [1, 2])

@@ -135,6 +135,31 @@ def test_full_size_zero3_llama():
     assert torch.equal(full.view(torch.int16), shards[:ds.N].view(torch.int16))
 
 
+@pytest.mark.parametrize("R", [4, 8])
+def test_zero3_step_sampled_at_a_persistent_grid_size(R):
+    """200 M elements: the ZeRO-3 step runs its persistent grid below the
+    resident maximum (R = 4 and R = 8); sampled elements against the oracle,
+    and the shards' bf16 equal to the updated master everywhere."""
+    wl = W.flat(R, 1, 200_000_003, seed=R + 50, step=3, state="synthetic")
+    ds = H.DeviceState(wl, staged_scratch=False)
+    ds.fill_state_device()
+    ds.fill_grads_device(wl.step)
+    shards = torch.zeros(ds.padded, dtype=torch.bfloat16, device="cuda")
+    z.zero3_step(ds.plan, ds.grads, ds.W, ds.m, ds.v, shards, ds.hp, wl.step)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(R)
+    pick = np.unique(np.concatenate([rng.integers(0, ds.N, 20_000), np.arange(ds.N - 3000, ds.N),
+                                     np.arange(0, 3000)]))
+    it = torch.from_numpy(pick).cuda()
+    W0 = W.host_w0_at(wl, pick)
+    m0, v0 = W.host_mv0_at(wl, pick)
+    want = H.oracle_run(wl, {wl.step: W.host_grads_at(wl, wl.step, pick)}, W0, m0, v0, [wl.step])
+    assert np.array_equal(H.u16_from_bf16(shards[it]), want[3][0])
+    for got, exp in ((ds.W, want[0]), (ds.m, want[1]), (ds.v, want[2])):
+        assert np.array_equal(got[it].cpu().numpy().view(np.uint32), exp.view(np.uint32))
+    assert torch.equal(shards[:ds.N].view(torch.int16), ds.W[:ds.N].to(torch.bfloat16).view(torch.int16))
+
+
 # ----------------------------------------- per-unit reduce-scatter (FSDP) --
 
 def _random_units(n, rng, pieces):
