@@ -244,6 +244,18 @@ def kernel_source_hash() -> str:
     return hashlib.sha256(body.encode()).hexdigest()[:16]
 
 
+def _mem_available_bytes():
+    """MemAvailable of this node from /proc/meminfo, or None."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except (OSError, ValueError, IndexError):
+        pass
+    return None
+
+
 def traffic_per_param():
     """Measured DRAM bytes per parameter of the fused kernel from the
     committed ncu summary, if it was taken on the current kernel source."""
@@ -386,7 +398,17 @@ def run_ours(args, rank, world, local_rank):
 
     # -------- end to end through the host-buffer entry point
     e2e = None
-    if not args.no_e2e and args.variant == "fused":
+    want_e2e = not args.no_e2e and args.variant == "fused"
+    # every rank of this node pins its own copy of the gradients and the
+    # replica; decided together before any rank pins, so all ranks take the
+    # same branch (the collectives below need every rank)
+    host_need = world * (2 * wl.R * wl.M + 2) * N
+    host_avail = _mem_available_bytes()
+    too_big = bool(host_avail) and host_need > 0.6 * host_avail
+    if want_e2e and max_over_ranks(1.0 if too_big else 0.0, dev) > 0:
+        e2e = {"unavailable": f"{world} rank(s) would pin {host_need / 1e9:.1f} GB of host memory "
+                              f"for the gradients; {(host_avail or 0) / 1e9:.1f} GB is available"}
+    elif want_e2e:
         host_g = [torch.empty(N, dtype=torch.bfloat16, pin_memory=True) for _ in ds.grads]
         for h, d in zip(host_g, ds.grads):
             h.copy_(d[:N])
