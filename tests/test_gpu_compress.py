@@ -206,3 +206,65 @@ def test_compressed_step_at_a_persistent_grid_size(kind, ef):
     runs its persistent grid (for the sign codec without error feedback the
     grid below the resident maximum), whole vector against the oracle."""
     _run(W.flat(8, 1, 4_000_037, seed=41, step=1, state="synthetic"), kind, ef, [1, 2])
+
+
+# ------------------------------------------------------------- full size --
+
+def _sample_blocks(wl, plan, seed=777, n_random=160):
+    """Whole 128-element compression blocks: random ones, the first and
+    last, those at shard and tensor boundaries; the ragged last block last,
+    so every block of the concatenation starts at a multiple of 128."""
+    N, S = plan.N, plan.S
+    nblk = (N + 127) // 128
+    rng = np.random.default_rng(seed)
+    blocks = set(rng.integers(0, nblk, n_random).tolist()) | {0, 1, nblk - 2, nblk - 1}
+    for r in range(1, wl.R):
+        blocks |= {r * S // 128 - 1, r * S // 128}
+    for off in wl.offsets[1:-1]:
+        blocks.add(int(off) // 128)
+    blocks = sorted(b for b in blocks if 0 <= b < nblk)
+    return np.concatenate([np.arange(b * 128, min((b + 1) * 128, N)) for b in blocks]).astype(np.int64)
+
+
+@pytest.mark.parametrize("name,kind,ef", [
+    ("llama-3.2-1b", KINDS[2], False), ("llama-3.2-1b", KINDS[1], False),
+    ("llama-3.2-1b", KINDS[1], True), ("gpt2-small", KINDS[2], True),
+    ("gpt2-small", KINDS[0], False), ("uneven", KINDS[2], False), ("uneven", KINDS[1], True)])
+def test_compressed_full_size_sampled_blocks(name, kind, ef):
+    """The workloads at full size, in the launch configuration the benchmark
+    times: every step from the workload's first to its measured step on the
+    device, the oracle on sampled whole blocks (the codec acts per block,
+    the rest per element); replicas equal and the pad untouched everywhere."""
+    gk, ok = kind
+    wl = W.ALL[name]()
+    steps = list(range(wl.first_step(), wl.step + 1))
+    ds = H.DeviceState(wl, staged_scratch=False)
+    ds.fill_state_device()
+    Ed = [torch.zeros(ds.N, dtype=torch.float32, device="cuda") for _ in range(wl.R)] if ef else None
+    for t in steps:
+        ds.fill_grads_device(t)
+        z.zero_step_compressed(ds.plan, ds.grads, ds.W, ds.m, ds.v, ds.params, ds.hp, t, gk, Ed)
+    torch.cuda.synchronize()
+    idx = _sample_blocks(wl, ds.plan)
+    it = torch.from_numpy(idx).to(ds.W.device)
+    got = (ds.W[it].cpu().numpy(), ds.m[it].cpu().numpy(), ds.v[it].cpu().numpy(),
+           [H.u16_from_bf16(p[it]) for p in ds.params])
+    got_E = [e[it].cpu().numpy() for e in Ed] if ef else None
+    replicas_equal = all(torch.equal(p, ds.params[0]) for p in ds.params[1:])
+    pad_clean = all(int(torch.count_nonzero(t[ds.N:])) == 0 for t in (ds.W, ds.m, ds.v))
+    del ds, Ed, it
+    torch.cuda.empty_cache()
+    Wc = W.host_w0_at(wl, idx)
+    mc, vc = W.host_mv0_at(wl, idx)
+    Pc = [np.zeros(idx.size, np.uint16) for _ in range(wl.R)]
+    Ec = [np.zeros(idx.size, np.float32) for _ in range(wl.R)] if ef else None
+    hp = oracle.hparams(**wl.hparams())
+    for t in steps:
+        oracle.dp_step_compressed(W.host_grads_at(wl, t, idx), Wc, mc, vc, Pc, hp, t, wl.R, wl.M,
+                                  ok, Ec)
+    res = H.compare(got, (Wc, mc, vc, Pc))
+    assert not {k: v for k, v in res.items() if v}, (name, res, idx.size)
+    if ef:
+        for g, e in zip(got_E, Ec):
+            assert np.array_equal(g.view(np.uint32), e.view(np.uint32))
+    assert replicas_equal and pad_clean

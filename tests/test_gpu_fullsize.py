@@ -90,3 +90,14 @@ def test_flat_sweep_points_sampled(R, S):
     bad = {key: v for key, v in res.items() if v}
     assert not bad, (wl.name, bad, k)
     assert replicas_equal and pad_clean and status == 0
+
+
+@pytest.mark.parametrize("name", ["gpt2-small", "llama-3.2-1b"])
+def test_full_size_sampled_tma_variant(name):
+    """The TMA-bulk-staged variant (R*M <= 16) at full size, sampled against
+    the oracle like the other variants."""
+    wl = W.ALL[name]()
+    res, replicas_equal, pad_clean, status, k = _run_full(wl, z.ZERO_VARIANT_FUSED_TMA)
+    bad = {key: v for key, v in res.items() if v}
+    assert not bad, (name, bad, k)
+    assert replicas_equal and pad_clean and status == 0
