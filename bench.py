@@ -13,9 +13,9 @@ no L2 flush is needed between steps.
 
 Timing: W warm-up steps, then K steps bracketed by a barrier and
 cuda.synchronize on both sides, CUDA events on the launching stream, max over
-ranks.  Each rank (one per GPU) runs its own emulated ZeRO group: the path
-has no cross-GPU exchange on this build, so N>1 runs N independent replicas
-("weak" scaling).  The JSON line also carries the roofline of the dominant
+ranks.  Each rank (one per GPU) runs its own emulated ZeRO group: the
+emulated ranks live in one GPU's memory and nothing crosses GPUs, so N>1
+runs N independent replicas ("weak" scaling).  The JSON line also carries the roofline of the dominant
 kernel, the end-to-end number through the host-buffer entry point, the
 oracle timed on the host cores, and the SM clocks sampled during the timed
 region.

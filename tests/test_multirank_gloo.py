@@ -1,7 +1,7 @@
 """The N>1 host logic of bench.py on CPU with world_size-2 gloo ranks.
 
-On this build each rank runs its own emulated ZeRO group (N independent
-replicas, no cross-GPU data path); the only thing ranks share is the timing
+Each rank runs its own emulated ZeRO group (N independent replicas, no
+cross-GPU data path); the only thing ranks share is the timing
 reduction (max over ranks) and rank 0 alone printing the JSON line.
 """
 import io
