@@ -838,6 +838,105 @@ def run_table(args):
     return rows
 
 
+# --------------------------------------------------------- checkpoints --
+
+def run_ckpt(args):
+    """Sharded checkpoint of the GPT-2- and 1B-shaped workloads' state (14 B
+    per param: bf16 param, fp32 master, m, v; one file per rank shard): the
+    pause on the step's stream (from the call, which pins the staging buffer,
+    to the end of the device-to-host copies) and the time until every shard
+    file is fsync'ed and renamed; then a load under the same R and one
+    resharded to R' = R/2.  The files go to a temporary directory that is
+    removed afterwards."""
+    import shutil
+
+    import torch
+
+    import zero_optimizer_step_rs_gb300 as z
+    from tests import harness as H
+    from zgen import workloads as W
+
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    base = os.environ.get("TMPDIR") or tempfile.gettempdir()
+    for name in ("gpt2-small", "llama-3.2-1b"):
+        wl = W.ALL[name]()
+        nbytes = 14 * wl.N
+        free = shutil.disk_usage(base).free
+        if free < 2.5 * nbytes:
+            print(json.dumps({"workload": name, "variant": "checkpoint",
+                              "skipped": f"{free / 1e9:.1f} GB free under {base}, "
+                                         f"need {2.5 * nbytes / 1e9:.1f} GB"}), flush=True)
+            continue
+        ds = H.DeviceState(wl, staged_scratch=False)
+        ds.fill_state_device()
+        ds.fill_grads_device(wl.step)
+        ds.step(wl.step)
+        torch.cuda.synchronize()
+        d = tempfile.mkdtemp(prefix="zckpt_", dir=base)
+        try:
+            rows = {}
+
+            def save(sub):
+                """One save: GPU-stream pause from the call to the end of the
+                copies (events), host time of the call, seconds until every
+                file is durable."""
+                os.makedirs(sub)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                e0.record(stream)
+                job = z.zero_ckpt_save_async(ds.plan, ds.params[0], ds.W, ds.m, ds.v, wl.step,
+                                             ds.hp, sub, n_threads=8)
+                t_call = time.perf_counter() - t0
+                e1.record(stream)
+                e1.synchronize()
+                job.wait()
+                return e0.elapsed_time(e1), t_call, time.perf_counter() - t0
+
+            def settle():
+                # background writeback of earlier files can slow the copies
+                # into host memory: let it finish between measurements
+                os.sync()
+                time.sleep(3)
+
+            settle()
+            # the library pins its own staging buffer for the save
+            rows["pause_ms"], rows["call_s"], rows["save_s"] = save(os.path.join(d, "save1"))
+            rows["copy_ms"] = rows["pause_ms"] - 1e3 * rows["call_s"]
+            settle()
+            sub = os.path.join(d, "save1")
+            t0 = time.perf_counter()
+            z.zero_ckpt_load(ds.plan, sub, ds.params, ds.W, ds.m, ds.v)
+            rows["load_s"] = time.perf_counter() - t0
+            R2 = max(1, wl.R // 2)
+            plan2 = z.Plan([int(x) for x in (wl.offsets[1:] - wl.offsets[:-1])], R2, wl.M, wl.stage,
+                           wl.align)
+            W2, m2, v2 = (torch.empty(plan2.c.padded, dtype=torch.float32, device="cuda")
+                          for _ in range(3))
+            P2 = [torch.empty(plan2.c.N, dtype=torch.bfloat16, device="cuda") for _ in range(R2)]
+            t0 = time.perf_counter()
+            z.zero_ckpt_load(plan2, sub, P2, W2, m2, v2)
+            rows["reshard_load_s"] = time.perf_counter() - t0
+            same = torch.equal(W2[:wl.N].view(torch.int32), ds.W[:wl.N].view(torch.int32))
+            del W2, m2, v2, P2
+        finally:
+            shutil.rmtree(d, ignore_errors=True)
+        row = {"workload": name, "variant": "checkpoint", "R": wl.R, "N": wl.N,
+               "bytes": nbytes, "stream_pause_ms": round(rows["pause_ms"], 2),
+               "staging_alloc_and_enqueue_s": round(rows["call_s"], 3),
+               "copy_ms": round(rows["copy_ms"], 2),
+               "copy_GB_s": round(nbytes / (rows["copy_ms"] / 1e3) / 1e9, 1),
+               "save_s": round(rows["save_s"], 3), "save_GB_s": round(nbytes / rows["save_s"] / 1e9, 2),
+               "load_s": round(rows["load_s"], 3), "load_GB_s": round(nbytes / rows["load_s"] / 1e9, 2),
+               "reshard_R": R2, "reshard_load_s": round(rows["reshard_load_s"], 3),
+               "reshard_load_GB_s": round(nbytes / rows["reshard_load_s"] / 1e9, 2),
+               "reshard_master_bit_identical": bool(same), "dir": base}
+        print(json.dumps(row), flush=True)
+        del ds
+        torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------- reference arm --
 
 def run_reference(args):
@@ -888,6 +987,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--table", action="store_true",
                     help="every workload and the flat sweep, one JSON line each")
+    ap.add_argument("--ckpt", action="store_true",
+                    help="checkpoint save / load / reshard timings of two workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -898,6 +999,9 @@ def main():
 
     if args.table:
         run_table(args)
+        return 0
+    if args.ckpt:
+        run_ckpt(args)
         return 0
 
     if args.impl == "reference":

@@ -491,6 +491,9 @@ extern "C" zero_status zero_ckpt_save_async(const zero_plan_t* plan, const uint1
     }
     ok = ok && cudaEventRecord(job->copied, st) == cudaSuccess;
     if (!ok) {
+        // copies already enqueued may still be writing into the staging
+        // buffer: wait for the stream before freeing it
+        cudaStreamSynchronize(st);
         if (job->copied) cudaEventDestroy(job->copied);
         cudaFreeHost(job->staging);
         delete job;
