@@ -23,7 +23,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 SOURCES = [os.path.join(CSRC, "zero_step.cu"), os.path.join(CSRC, "plan.cpp"),
            os.path.join(CSRC, "ckpt.cpp")]
-HEADERS = [os.path.join(INCLUDE, "zero_step.h")]
+HEADERS = [os.path.join(INCLUDE, "zero_step.h")] + sorted(
+    os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh"))
 
 
 def nvcc() -> str:

@@ -1,0 +1,363 @@
+// zero_clip.cuh - the step with global-norm clipping (zero_step_clipped).
+// Part of the zero_step.cu translation unit: included at its end, it uses that
+// file's scalars, device helpers, launch helpers and argument checks.
+
+// =========================================== step with global-norm clipping ==
+// zero_step_clipped: the averaged gradient of every element is stashed in
+// fp32 scratch while its square feeds a fixed pairwise tree (fp32, leaves
+// g*g, zero padding to a power of two); the tree is finished level by level,
+// one thread turns the squared norm into the clip coefficient (and the
+// skip decision for a non-finite norm), and a last pass applies it with the
+// AdamW update and the R-way bf16 all-gather.
+//
+// Tree decomposition: in the streaming pass each warp reduces 256
+// consecutive leaves (32 lanes x 8 leaves: a 3-level tree in registers, then
+// 5 levels of shuffles) - exactly an aligned subtree of the global tree - and
+// writes one partial, with no block-wide barrier; each further level is a
+// block reducing 2048 partials (8 leaves per thread, the warp levels, then 3
+// levels across the 8 warps), again an aligned subtree.  Adding a zero
+// (padding) changes no value, so the result equals the tree over the leaves
+// padded to the next power of two for any N and any grid.
+namespace {
+
+constexpr int kTreeLeaves = 2048;                 // leaves per tree block (256 x 8)
+constexpr int kWarpLeaves = 256;                  // leaves per warp in the streaming pass
+
+struct ClipCtl {
+    double sumsq;          // squared norm (the fp32 tree value, widened)
+    float coef;            // multiplier when clip != 0
+    int32_t clip;          // 1: multiply the averaged gradients by coef
+    int32_t skip;          // 1: non-finite norm and skipping requested
+    int32_t pad[9];
+};
+
+struct ClipLayout {
+    int64_t g_off, ctl_off, total;
+    int levels;
+    int64_t lvl_off[8], lvl_len[8];
+};
+
+int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
+
+ClipLayout clip_layout(const zero_plan_t* plan)
+{
+    ClipLayout L{};
+    L.g_off = 0;
+    int64_t off = round256(4 * plan->padded);
+    int64_t len = (plan->N + kWarpLeaves - 1) / kWarpLeaves;
+    if (len < 1) len = 1;
+    L.levels = 0;
+    while (true) {
+        L.lvl_off[L.levels] = off;
+        L.lvl_len[L.levels] = len;
+        off += round256(4 * len);
+        ++L.levels;
+        if (len == 1 || L.levels == 8) break;
+        len = (len + kTreeLeaves - 1) / kTreeLeaves;
+    }
+    L.ctl_off = off;
+    L.total = off + round256((int64_t)sizeof(ClipCtl));
+    return L;
+}
+
+// sum of a thread's 8 leaves, then the warp and block levels; returns the
+// block's value in thread 0
+__device__ __forceinline__ float tree8(const float (&x)[8])
+{
+    return __fadd_rn(__fadd_rn(__fadd_rn(x[0], x[1]), __fadd_rn(x[2], x[3])),
+                     __fadd_rn(__fadd_rn(x[4], x[5]), __fadd_rn(x[6], x[7])));
+}
+
+__device__ __forceinline__ float warp_tree(float v)
+{
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_down_sync(0xFFFFFFFFu, v, off);
+        v = __fadd_rn(v, o);           // meaningful in lanes that are multiples of 2*off
+    }
+    return v;                          // lane 0 holds the warp's subtree
+}
+
+__device__ __forceinline__ float block_tree(float v)
+{
+    __shared__ float warp_sum[kThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_down_sync(0xFFFFFFFFu, v, off);
+        v = __fadd_rn(v, o);           // meaningful in lanes that are multiples of 2*off
+    }
+    if (lane == 0) warp_sum[warp] = v;
+    __syncthreads();
+    float r = 0.0f;
+    if (threadIdx.x == 0) {
+        const float* w = warp_sum;
+        r = __fadd_rn(__fadd_rn(__fadd_rn(w[0], w[1]), __fadd_rn(w[2], w[3])),
+                      __fadd_rn(__fadd_rn(w[4], w[5]), __fadd_rn(w[6], w[7])));
+    }
+    __syncthreads();                   // warp_sum is reused by the next tile
+    return r;
+}
+
+struct ClipArgs {
+    GradPtrs g;
+    ReplicaPtrs P;
+    float* gs;             // averaged gradients (padded floats; [0, N) used)
+    float* lvl0;           // first tree level: one partial per 256 elements (per warp)
+    float* W;
+    float* m;
+    float* v;
+    ClipCtl* ctl;
+    int64_t n;
+    int32_t R, M;
+    StepScalars s;
+};
+
+// pass 1: averaged gradient of 8 consecutive elements per thread, stashed,
+// and the tile's pairwise partial of their squares
+template <int RC, int MC>
+__global__ void __launch_bounds__(kThreads) k_rs_norm(const __grid_constant__ ClipArgs a)
+{
+    const int R = RC > 0 ? RC : a.R;
+    const int M = MC > 0 ? MC : a.M;
+    const int64_t n = a.n;
+    const int64_t tiles = (n + kTreeLeaves - 1) / kTreeLeaves;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int64_t e = tile * kTreeLeaves + (int64_t)threadIdx.x * 8;
+        float g[8];
+        if (e + 8 <= n) {
+            float lo[4], hi[4];
+            grad_sum4<RC, MC>(a.g, R, M, e, lo);
+            grad_sum4<RC, MC>(a.g, R, M, e + 4, hi);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                g[k] = scale_grad(a.s, lo[k]);
+                g[4 + k] = scale_grad(a.s, hi[k]);
+            }
+            st_stream(a.gs + e, make_float4(g[0], g[1], g[2], g[3]));
+            st_stream(a.gs + e + 4, make_float4(g[4], g[5], g[6], g[7]));
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                g[k] = 0.0f;
+                if (e + k < n) {
+                    g[k] = scale_grad(a.s, grad_sum1(a.g, R, M, e + k));
+                    a.gs[e + k] = g[k];
+                }
+            }
+        }
+        float sq[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) sq[k] = __fmul_rn(g[k], g[k]);   // padding leaves are +0
+        const float part = warp_tree(tree8(sq));
+        const int64_t wpart = tile * (kTreeLeaves / kWarpLeaves) + (threadIdx.x >> 5);
+        if ((threadIdx.x & 31) == 0 && wpart * kWarpLeaves < n) a.lvl0[wpart] = part;
+    }
+}
+
+// one level of the tree: out[b] = pairwise sum of in[2048 b .. 2048 b + 2047]
+__global__ void __launch_bounds__(kThreads) k_tree(const float* __restrict__ in, int64_t n_in,
+                                                   float* __restrict__ out)
+{
+    const int64_t blocks = (n_in + kTreeLeaves - 1) / kTreeLeaves;
+    for (int64_t b = blockIdx.x; b < blocks; b += gridDim.x) {
+        const int64_t e = b * kTreeLeaves + (int64_t)threadIdx.x * 8;
+        float x[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = e + k < n_in ? in[e + k] : 0.0f;
+        const float part = block_tree(tree8(x));
+        if (threadIdx.x == 0) out[b] = part;
+    }
+}
+
+__global__ void k_clip_coef(const float* __restrict__ root, ClipCtl* ctl, float max_norm,
+                            int32_t skip_nonfinite, int32_t* status, double* sumsq_out)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    const float ss = *root;
+    const double norm = sqrt((double)ss);
+    const double coef = (double)max_norm / (norm + 1e-6);
+    ClipCtl c{};
+    c.sumsq = (double)ss;
+    c.clip = coef < 1.0 ? 1 : 0;
+    c.coef = c.clip ? (float)coef : 1.0f;
+    const bool finite = isfinite(ss);
+    c.skip = (!finite && skip_nonfinite) ? 1 : 0;
+    *ctl = c;
+    if (status) {
+        if (!finite) atomicOr(status, ZERO_DEV_NONFINITE);
+        if (c.skip) atomicOr(status, ZERO_DEV_SKIPPED);
+    }
+    if (sumsq_out) *sumsq_out = c.sumsq;
+}
+
+// pass 2: g' = g * coef (when clipping), AdamW, bf16 all-gather; tiles of
+// 256 threads x 4 elements x 2 units with every load of a tile issued first,
+// as in k_fused
+template <int RC>
+__global__ void __launch_bounds__(kThreads) k_adamw_ag(const __grid_constant__ ClipArgs a)
+{
+    const ClipCtl c = *a.ctl;
+    if (c.skip) return;
+    const int R = RC > 0 ? RC : a.R;
+    constexpr int U = 4;
+    constexpr int T = kUnit * U;
+    const int64_t n = a.n;
+    const int64_t full_tiles = n / T;
+    for (int64_t tile = blockIdx.x; tile < full_tiles; tile += gridDim.x) {
+        const int64_t e0 = tile * T + (int64_t)threadIdx.x * kVec;
+        float4 g[U], w[U], m[U], v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t e = e0 + (int64_t)u * kUnit;
+            g[u] = ld_stream(a.gs + e);
+            w[u] = ld_stream(a.W + e);
+            m[u] = ld_stream(a.m + e);
+            v[u] = ld_stream(a.v + e);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t e = e0 + (int64_t)u * kUnit;
+            float* gp = &g[u].x;
+            float* wp = &w[u].x;
+            float* mp = &m[u].x;
+            float* vp = &v[u].x;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float gk = c.clip ? __fmul_rn(gp[k], c.coef) : gp[k];
+                adamw(a.s, gk, wp[k], mp[k], vp[k]);
+            }
+            st_stream(a.W + e, w[u]);
+            st_stream(a.m + e, m[u]);
+            st_stream(a.v + e, v[u]);
+            const uint2 p = make_uint2(pack_bf16x2(w[u].x, w[u].y), pack_bf16x2(w[u].z, w[u].w));
+            if constexpr (RC > 0) {
+#pragma unroll
+                for (int r = 0; r < RC; ++r) st_stream(a.P.p[r] + e, p);
+            } else {
+                for (int r = 0; r < R; ++r) st_stream(a.P.p[r] + e, p);
+            }
+        }
+    }
+    const int64_t tail0 = full_tiles * T;
+    if (tail0 < n && blockIdx.x == (unsigned)(full_tiles % gridDim.x)) {
+        for (int64_t i = tail0 + threadIdx.x; i < n; i += kThreads) {
+            float g = a.gs[i];
+            if (c.clip) g = __fmul_rn(g, c.coef);
+            float w = a.W[i], m = a.m[i], v = a.v[i];
+            adamw(a.s, g, w, m, v);
+            a.W[i] = w;
+            a.m[i] = m;
+            a.v[i] = v;
+            const uint16_t p = to_bf16(w);
+            for (int r = 0; r < R; ++r) a.P.p[r][i] = p;
+        }
+    }
+}
+
+template <int RC, int MC>
+cudaError_t launch_rs_norm_t(const ClipArgs& a, cudaStream_t st)
+{
+    const void* k = reinterpret_cast<const void*>(&k_rs_norm<RC, MC>);
+    const int64_t tiles = (a.n + kTreeLeaves - 1) / kTreeLeaves;
+    k_rs_norm<RC, MC><<<grid_for(k, tiles), kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rs_norm(const ClipArgs& a, cudaStream_t st)
+{
+    const int R = a.R, M = a.M;
+#define ZERO_CASE(r_, m_) \
+    if (R == r_ && M == m_) return launch_rs_norm_t<r_, m_>(a, st);
+    ZERO_CASE(8, 1) ZERO_CASE(4, 1) ZERO_CASE(2, 1) ZERO_CASE(1, 1) ZERO_CASE(4, 2) ZERO_CASE(7, 4)
+#undef ZERO_CASE
+    return launch_rs_norm_t<0, 0>(a, st);
+}
+
+cudaError_t launch_adamw_ag(const ClipArgs& a, cudaStream_t st)
+{
+    const int64_t work = (a.n + 4 * kUnit - 1) / (4 * kUnit);     // tiles of 4 units
+    auto go = [&](const void* k, auto kern) {
+        kern<<<grid_for(k, work < 1 ? 1 : work), kThreads, 0, st>>>(a);
+        return cudaGetLastError();
+    };
+    switch (a.R) {
+    case 8: return go(reinterpret_cast<const void*>(&k_adamw_ag<8>), k_adamw_ag<8>);
+    case 4: return go(reinterpret_cast<const void*>(&k_adamw_ag<4>), k_adamw_ag<4>);
+    case 2: return go(reinterpret_cast<const void*>(&k_adamw_ag<2>), k_adamw_ag<2>);
+    default: return go(reinterpret_cast<const void*>(&k_adamw_ag<0>), k_adamw_ag<0>);
+    }
+}
+
+}  // namespace
+
+extern "C" int64_t zero_clip_scratch_bytes(const zero_plan_t* plan)
+{
+    if (check_plan(plan) != ZERO_OK) return -1;
+    return clip_layout(plan).total;
+}
+
+extern "C" zero_status zero_step_clipped(const zero_plan_t* plan,
+                                         const uint16_t* const* rank_grads, float* master,
+                                         float* m, float* v, uint16_t* const* rank_params,
+                                         const zero_adamw_hparams* hp, int64_t step,
+                                         float max_norm, void* scratch, int64_t scratch_bytes,
+                                         int32_t flags, int32_t* dev_status, double* dev_sumsq,
+                                         void* stream)
+{
+    if (zero_status e = check_plan(plan)) return e;
+    if (zero_status e = check_hparams(hp, step)) return e;
+    if (!(max_norm > 0.0f) || !std::isfinite(max_norm)) return ZERO_ERR_INVALID_ARG;
+    if (flags & ~(ZERO_FLAG_CHECK_FINITE | ZERO_FLAG_SKIP_NONFINITE)) return ZERO_ERR_INVALID_ARG;
+    if ((flags & ZERO_FLAG_CHECK_FINITE) && !dev_status) return ZERO_ERR_NULL;
+    if (plan->N == 0) return ZERO_OK;
+    const ClipLayout L = clip_layout(plan);
+    Range rs[ZERO_MAX_RM + ZERO_MAX_R + 6];
+    int nr = 0;
+    if (zero_status e = check_grads(plan, rank_grads, rs, nr)) return e;
+    if (zero_status e = check_replicas(plan, rank_params, rs, nr)) return e;
+    if (zero_status e = check_state(plan, master, m, v, rs, nr)) return e;
+    if (zero_status e = check_ptr(scratch)) return e;
+    if (scratch_bytes < L.total) return ZERO_ERR_SIZE;
+    rs[nr++] = rng(scratch, L.total, true);
+    if (dev_status) rs[nr++] = rng(dev_status, 4, true);
+    if (dev_sumsq) {
+        if ((uintptr_t)dev_sumsq & 7u) return ZERO_ERR_ALIGN;
+        rs[nr++] = rng(dev_sumsq, 8, true);
+    }
+    if (zero_status e = check_overlap(rs, nr)) return e;
+
+    char* base = static_cast<char*>(scratch);
+    ClipArgs a{};
+    fill_grad_ptrs(a.g, plan, rank_grads);
+    fill_replica_ptrs(a.P, plan, rank_params);
+    a.gs = reinterpret_cast<float*>(base + L.g_off);
+    a.lvl0 = reinterpret_cast<float*>(base + L.lvl_off[0]);
+    a.W = master;
+    a.m = m;
+    a.v = v;
+    a.ctl = reinterpret_cast<ClipCtl*>(base + L.ctl_off);
+    a.n = plan->N;
+    a.R = plan->R;
+    a.M = plan->M;
+    a.s = step_scalars(*hp, step, plan->R, plan->M);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    cudaError_t err = launch_rs_norm(a, st);
+    for (int l = 1; l < L.levels && err == cudaSuccess; ++l) {
+        const float* in = reinterpret_cast<const float*>(base + L.lvl_off[l - 1]);
+        float* out = reinterpret_cast<float*>(base + L.lvl_off[l]);
+        const void* k = reinterpret_cast<const void*>(&k_tree);
+        k_tree<<<grid_for(k, L.lvl_len[l]), kThreads, 0, st>>>(in, L.lvl_len[l - 1], out);
+        err = cudaGetLastError();
+    }
+    if (err == cudaSuccess) {
+        const float* root = reinterpret_cast<const float*>(base + L.lvl_off[L.levels - 1]);
+        k_clip_coef<<<1, 32, 0, st>>>(root, a.ctl, max_norm,
+                                      (flags & ZERO_FLAG_SKIP_NONFINITE) ? 1 : 0, dev_status,
+                                      dev_sumsq);
+        err = cudaGetLastError();
+    }
+    if (err == cudaSuccess) err = launch_adamw_ag(a, st);
+    return cuda_status(err);
+}
