@@ -142,7 +142,7 @@ def _full_size(name, max_norm_scale):
     return sums, H.compare(got, want), replicas_equal
 
 
-@pytest.mark.parametrize("name", ["gpt2-small", "uneven"])
+@pytest.mark.parametrize("name", ["gpt2-small", "uneven", "llama-3.2-1b"])
 def test_full_size_clipped(name):
     sums, res, replicas_equal = _full_size(name, max_norm_scale=0.05)
     for g, o in sums:
