@@ -33,8 +33,7 @@
  *       [CS25 V6 Lecture 4 notes, "ZeRO-1" and "ZeRO-2" memory equations;
  *        CS324 Lecture 9 notes, exercises 1 and 7]
  *
- * Readings where the pages leave a step open (every one is listed in the
- * repository's design notes):
+ * Readings where the pages leave a step open:
  *   R1 AdamW is torch.optim.AdamW's documented algorithm (decoupled decay
  *      w*(1-lr*wd) first, then m/v EMA, bias correction, eps added after
  *      the bias-corrected square root).
@@ -161,9 +160,9 @@ void oracle_zero_bytes(double N, int32_t P, double bp, double bg, double bo,
 
 /* ------------------------------------------------------------------------
  * Global gradient-norm clipping with a non-finite check, before the update
- * (the training recipe "AdamW + gradient clipping", CS324 Lecture 9 notes,
- * section 7.4; fp32 gradient reduction, LLM infra 06, section 15.3).
- * Readings (listed in the repository's design notes):
+ * (the training recipe of AdamW with gradient clipping, CS324 Lecture 9
+ * notes, section 7.4; fp32 gradient reduction, LLM infra 06, section 15.3).
+ * Readings:
  *   R10 the squared norm is the fp32 pairwise (binary-tree) sum of the
  *       leaves g_i * g_i (fp32 products), i < n, padded with zeros to the
  *       next power of two: one fixed order, so every implementation that

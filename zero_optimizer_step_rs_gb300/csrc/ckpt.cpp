@@ -7,7 +7,8 @@
 //     cards merged (same notes, exercise 11);
 //   - bitwise-identical training from any checkpoint (PaLM, section 3.1);
 //   - sharded parallel writes, atomic rename, asynchronous saves
-//     (LLM infra 06, section 15.4, "checkpoint write crash").
+//     (LLM infra 06, section 15.4, the failure mode of a crash while a
+//     checkpoint is written).
 //
 // Format: one file per rank shard, "shard-RRRRR-of-NNNNN.zck", holding the
 // rank's elements [lo, lo + len) of the flat vector: a 128-byte header, then
