@@ -256,6 +256,16 @@ def _mem_available_bytes():
     return None
 
 
+def e2e_fits_host(host_need: int, device=None):
+    """Whether this node's ranks can pin host_need bytes between them (at
+    most 60 % of the available memory), decided with a max over ranks so
+    that every rank takes the same branch; returns (fits, available bytes
+    seen by this rank)."""
+    avail = _mem_available_bytes()
+    too_big = bool(avail) and host_need > 0.6 * avail
+    return max_over_ranks(1.0 if too_big else 0.0, device) == 0.0, avail
+
+
 def traffic_per_param():
     """Measured DRAM bytes per parameter of the fused kernel from the
     committed ncu summary, if it was taken on the current kernel source."""
@@ -403,9 +413,8 @@ def run_ours(args, rank, world, local_rank):
     # replica; decided together before any rank pins, so all ranks take the
     # same branch (the collectives below need every rank)
     host_need = world * (2 * wl.R * wl.M + 2) * N
-    host_avail = _mem_available_bytes()
-    too_big = bool(host_avail) and host_need > 0.6 * host_avail
-    if want_e2e and max_over_ranks(1.0 if too_big else 0.0, dev) > 0:
+    fits, host_avail = e2e_fits_host(host_need, dev) if want_e2e else (False, None)
+    if want_e2e and not fits:
         e2e = {"unavailable": f"{world} rank(s) would pin {host_need / 1e9:.1f} GB of host memory "
                               f"for the gradients; {(host_avail or 0) / 1e9:.1f} GB is available"}
     elif want_e2e:
