@@ -331,7 +331,8 @@ __global__ void __launch_bounds__(kThreads) k_comp(const __grid_constant__ CompA
         // every rank's loads first, then the codecs and their warp reductions,
         // so the loads are all in flight before the first sync.  Whether the
         // owner's state joins them was measured per codec: it does for int8
-        // without error feedback (0.86 -> 0.96 of peak), and slows the others.
+        // without error feedback while R*M <= 16 (0.86 -> 0.96 of peak at R=8,
+        // M=1; at R=7, M=4 it would cost 0.97 -> 0.90), and slows the others.
         // fp16 without error feedback has no sync and runs faster in the
         // rank-by-rank form (fewer registers, more blocks per SM).
         if constexpr (RC > 0 && MC > 0 && (KIND != ZERO_COMP_FP16 || EF)) {
@@ -345,10 +346,12 @@ __global__ void __launch_bounds__(kThreads) k_comp(const __grid_constant__ CompA
                     for (int r = 0; r < RC; ++r) ex[r] = ld_stream(a.E[r] + e);
                 }
                 if constexpr (KIND == ZERO_COMP_INT8 && !EF) {
-                    w4 = ld_stream(a.W + e);
-                    m4 = ld_stream(a.m + e);
-                    v4 = ld_stream(a.v + e);
-                    have_state = true;
+                    if constexpr (RC * MC <= 16) {
+                        w4 = ld_stream(a.W + e);
+                        m4 = ld_stream(a.m + e);
+                        v4 = ld_stream(a.v + e);
+                        have_state = true;
+                    }
                     int8_transposed<RC, MC>(gx, lane, acc);
                 } else if constexpr (KIND == ZERO_COMP_SIGN && !EF && (RC & (RC - 1)) == 0) {
                     sign_transposed<RC, MC>(gx, lane, acc);
