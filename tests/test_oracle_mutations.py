@@ -6,6 +6,7 @@ offset), compiled on the CPU into a temporary library; the pin suites then
 run against it in a child process and must fail.  The real oracle is never
 modified.
 """
+import concurrent.futures
 import os
 import subprocess
 import sys
@@ -90,21 +91,46 @@ MUTANTS = {
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_pins_catch_planted_mistake(name, tmp_path):
+PIN_SUITES = ["tests/test_oracle_pins.py", "tests/test_oracle_collectives.py",
+              "tests/test_oracle_clip.py", "tests/test_oracle_zero3.py",
+              "tests/test_oracle_compress.py", "tests/test_oracle_onebit.py"]
+
+
+def _run_mutant(name, workdir):
+    """Compile the mutant into its own library and run the pin suites on it in
+    a child process; returns (returncode, tail of the child's output)."""
     old, new = MUTANTS[name]
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutation site for {name} not unique/present"
-    mut_src = tmp_path / "zero_oracle.c"
-    mut_src.write_text(src.replace(old, new))
-    hdr = os.path.join(ROOT, "oracle", "zero_oracle.h")
-    lib = tmp_path / "liboracle_mut.so"
-    subprocess.run(["gcc", *oracle.CFLAGS, "-I", os.path.dirname(hdr), "-o", str(lib),
-                    str(mut_src), "-lm", "-lpthread"], check=True)
-    env = dict(os.environ, ZERO_ORACLE_LIB=str(lib))
+    if src.count(old) != 1:
+        return None, f"mutation site for {name} not unique/present"
+    mut_src = os.path.join(workdir, "zero_oracle.c")
+    with open(mut_src, "w") as f:
+        f.write(src.replace(old, new))
+    hdr_dir = os.path.join(ROOT, "oracle")
+    lib = os.path.join(workdir, "liboracle_mut.so")
+    subprocess.run(["gcc", *oracle.CFLAGS, "-I", hdr_dir, "-o", lib, mut_src, "-lm", "-lpthread"],
+                   check=True)
+    env = dict(os.environ, ZERO_ORACLE_LIB=lib)
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        "tests/test_oracle_pins.py", "tests/test_oracle_collectives.py",
-                        "tests/test_oracle_clip.py", "tests/test_oracle_zero3.py",
-                        "tests/test_oracle_compress.py", "tests/test_oracle_onebit.py"],
-                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
-    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
+                        *PIN_SUITES], cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=600)
+    return r.returncode, r.stdout[-2000:]
+
+
+@pytest.fixture(scope="module")
+def mutant_results(tmp_path_factory):
+    """Every mutant's pin run, the children side by side (one per core): each
+    is an independent process over its own library, so the outcome of one
+    does not depend on the others."""
+    workers = max(1, min(len(MUTANTS), os.cpu_count() or 1))
+    dirs = {n: str(tmp_path_factory.mktemp(n)) for n in MUTANTS}
+    with concurrent.futures.ThreadPoolExecutor(workers) as ex:
+        futs = {n: ex.submit(_run_mutant, n, dirs[n]) for n in MUTANTS}
+        return {n: f.result() for n, f in futs.items()}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, mutant_results):
+    rc, out = mutant_results[name]
+    assert rc is not None, out
+    assert rc != 0, f"mutant {name} survived the pins:\n{out}"
