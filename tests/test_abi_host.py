@@ -344,3 +344,57 @@ def test_zero3_unit_entry_argument_errors():
     assert upd(gs=Wp) == B.ZERO_ERR_OVERLAP
     assert upd(ps=mp) == B.ZERO_ERR_OVERLAP
     assert upd(ps=P[0] + 2) == B.ZERO_ERR_ALIGN
+
+
+def test_compressed_step_argument_errors(plan):
+    import ctypes
+    g, Wp, mp, vp, P, scr, st = fake_bufs(plan)
+    E = [BASE + (1 << 36) + k * (1 << 30) for k in range(plan.R)]
+    L = B.lib()
+
+    def call(kind=B.ZERO_COMP_INT8, residuals=E, step=1, hp=None, grads=g, W=Wp):
+        ga, pa = B._ptrs(grads), B._ptrs(P)
+        ea = B._ptrs(residuals) if residuals is not None else None
+        hp = hp if hp is not None else z.hparams()
+        return L.zero_step_compressed(plan.ptr, ctypes.addressof(ga), W, mp, vp,
+                                      ctypes.addressof(pa), ctypes.byref(hp), step, kind,
+                                      ctypes.addressof(ea) if ea is not None else None, None)
+    assert call(kind=7) == B.ZERO_ERR_INVALID_ARG
+    assert call(kind=-1) == B.ZERO_ERR_INVALID_ARG
+    assert call(step=0) == B.ZERO_ERR_INVALID_ARG
+    assert call(hp=z.hparams(eps=-1.0)) == B.ZERO_ERR_INVALID_ARG
+    assert call(grads=[0] + g[1:]) == B.ZERO_ERR_NULL
+    assert call(W=0) == B.ZERO_ERR_NULL
+    assert call(W=Wp + 8) == B.ZERO_ERR_ALIGN
+    assert call(residuals=E[:-1] + [0]) == B.ZERO_ERR_NULL
+    assert call(residuals=[E[0] + 4] + E[1:]) == B.ZERO_ERR_ALIGN
+    # every residual is an output of N floats: it may overlap no other buffer
+    assert call(residuals=[Wp] + E[1:]) == B.ZERO_ERR_OVERLAP
+    assert call(residuals=[E[0], E[0]] + E[2:]) == B.ZERO_ERR_OVERLAP
+    assert call(residuals=[g[3]] + E[1:]) == B.ZERO_ERR_OVERLAP
+    assert call(residuals=[P[0]] + E[1:]) == B.ZERO_ERR_OVERLAP
+    # residual 1 starting 16 bytes before residual 0 ends overlaps it; right
+    # after its end it does not (the call then fails later, at the first CUDA
+    # call, on a machine without a GPU)
+    assert call(residuals=[E[0], E[0] + 4 * plan.N - 16] + E[2:]) == B.ZERO_ERR_OVERLAP
+    assert call(residuals=[E[0], E[0] + 4 * plan.N] + E[2:]) == B.ZERO_ERR_CUDA
+
+
+def test_no_alloc_step_refuses_plans_beyond_its_array():
+    """The allocation-free staged step holds its scratch in a fixed array of
+    ZERO_NOALLOC_MAX_ELEMS floats: a plan one element past it is refused
+    with ZERO_ERR_SIZE before anything else is looked at."""
+    import ctypes
+    L = B.lib()
+    cap = B.ZERO_NOALLOC_MAX_ELEMS
+    fits = z.Plan([cap], 4, 1, 2)
+    over = z.Plan([cap + 1], 4, 1, 2)
+    assert fits.padded == cap and over.padded > cap
+    hp = z.hparams()
+    for pl, want in ((over, B.ZERO_ERR_SIZE), (fits, B.ZERO_ERR_NULL)):
+        ga = B._ptrs([0] * (pl.R * pl.M))
+        pa = B._ptrs([0] * pl.R)
+        got = L.zero_step_staged_noalloc(pl.ptr, ctypes.addressof(ga), None, None, None,
+                                         ctypes.addressof(pa), ctypes.byref(hp), 1, 0, None,
+                                         None)
+        assert got == want, (pl.padded, got)
