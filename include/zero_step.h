@@ -56,6 +56,10 @@
  *     must be 16-byte aligned.
  *   - No exceptions and no global state cross the ABI; entry points are
  *     thread-safe for distinct buffers.
+ *   - A plan with N = 0 is a no-op for the step entry points: once the
+ *     plan, hyper-parameters, flags and scalar arguments have passed their
+ *     checks, the call returns ZERO_OK without reading a buffer pointer,
+ *     launching anything or writing dev_status / dev_sumsq.
  */
 #ifndef ZERO_STEP_H
 #define ZERO_STEP_H

@@ -398,3 +398,44 @@ def test_no_alloc_step_refuses_plans_beyond_its_array():
                                          ctypes.addressof(pa), ctypes.byref(hp), 1, 0, None,
                                          None)
         assert got == want, (pl.padded, got)
+
+
+def test_empty_plan_is_a_no_op_for_every_step_entry_point():
+    """A plan with N = 0 has nothing to update: after the plan, hyper-parameter
+    and flag checks every step entry point returns ZERO_OK without looking at
+    a buffer pointer (NULLs here) and without a CUDA call."""
+    import ctypes
+    L = B.lib()
+    pl = z.Plan([0], 4, 2, 2)
+    assert (pl.N, pl.S, pl.padded) == (0, 0, 0)
+    hp = ctypes.byref(z.hparams())
+    g = B._ptrs([0] * (pl.R * pl.M))
+    P = B._ptrs([0] * pl.R)
+    ga, pa = ctypes.addressof(g), ctypes.addressof(P)
+    host_out = (ctypes.c_uint16 * 8)()
+    for variant in (B.ZERO_VARIANT_FUSED, B.ZERO_VARIANT_STAGED):
+        assert L.zero_step(pl.ptr, ga, None, None, None, pa, hp, 1, variant, None, 0, 0,
+                           None, None) == B.ZERO_OK
+    assert L.zero_rs_avg(pl.ptr, ga, None, 0, None, None) == B.ZERO_OK
+    assert L.zero_adamw_shard(pl.ptr, None, None, None, None, hp, 1, None) == B.ZERO_OK
+    assert L.zero_ag_cast(pl.ptr, None, pa, None) == B.ZERO_OK
+    assert L.zero_step_host(pl.ptr, ga, None, None, None, None, pa, host_out, hp, 1, 0, None,
+                            None) == B.ZERO_OK
+    assert L.zero_step_staged_noalloc(pl.ptr, ga, None, None, None, pa, hp, 1, 0, None,
+                                      None) == B.ZERO_OK
+    assert L.zero3_step(pl.ptr, ga, None, None, None, None, hp, 1, 0, None, None) == B.ZERO_OK
+    assert L.zero3_update(pl.ptr, None, None, None, None, None, hp, 1, None) == B.ZERO_OK
+    assert L.zero_step_clipped(pl.ptr, ga, None, None, None, pa, hp, 1, 1.0, None, 0, 0, None,
+                               None, None) == B.ZERO_OK
+    for kind in (B.ZERO_COMP_FP16, B.ZERO_COMP_INT8, B.ZERO_COMP_SIGN):
+        assert L.zero_step_compressed(pl.ptr, ga, None, None, None, pa, hp, 1, kind, None,
+                                      None) == B.ZERO_OK
+    # the checks before the empty return still hold
+    assert L.zero_step(pl.ptr, ga, None, None, None, pa, hp, 0, 0, None, 0, 0, None,
+                       None) == B.ZERO_ERR_INVALID_ARG
+    assert L.zero_step_clipped(pl.ptr, ga, None, None, None, pa, hp, 1, 0.0, None, 0, 0, None,
+                               None, None) == B.ZERO_ERR_INVALID_ARG
+    assert L.zero_step_compressed(pl.ptr, ga, None, None, None, pa, hp, 1, 9, None,
+                                  None) == B.ZERO_ERR_INVALID_ARG
+    assert L.zero_step_host(pl.ptr, None, None, None, None, None, pa, host_out, hp, 1, 0, None,
+                            None) == B.ZERO_ERR_NULL
