@@ -59,7 +59,8 @@
  *   - A plan with N = 0 is a no-op for the step entry points: once the
  *     plan, hyper-parameters, flags and scalar arguments have passed their
  *     checks, the call returns ZERO_OK without reading a buffer pointer,
- *     launching anything or writing dev_status / dev_sumsq.
+ *     launching anything or writing dev_status / dev_sumsq.  (The one
+ *     exception: zero_step_onebit checks its residual pointers first.)
  */
 #ifndef ZERO_STEP_H
 #define ZERO_STEP_H
