@@ -101,44 +101,51 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = []
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 10:
-                    continue
-                rows.append(parts)
+            lines = f.readlines()
         os.unlink(self.path)
-        if not rows:
-            return None
-        import datetime
+        return summarise_clocks(lines, self.t_start, self.t_stop)
 
-        def ts(p):
-            try:
-                return datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-            except ValueError:
-                return None
 
-        inside = [p for p in rows if self.t_start and self.t_stop and ts(p) is not None
-                  and self.t_start - 0.1 <= ts(p) <= self.t_stop + 0.1]
-        use = inside or rows
-        sm, reasons, sm_max = [], set(), None
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for p in use:
-            try:
-                mhz, mx = float(p[2]), float(p[3])
-            except ValueError:
-                continue
-            sm_max = mx
-            sm.append(mhz)
-            for name, flag in zip(names, p[6:10]):
-                if flag.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
+CLOCK_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+def summarise_clocks(lines, t_start, t_stop):
+    """Summary of nvidia-smi CSV lines (timestamp, then ClockSampler.FIELDS,
+    no header, no units): the median SM clock, the maximum SM clock and the
+    throttle reasons that were active, over the samples taken between
+    t_start and t_stop (100 ms of slack either side), or over every sample
+    when none fell inside; None without a usable sample."""
+    import datetime
+
+    rows = [[p.strip() for p in line.split(",")] for line in lines]
+    rows = [p for p in rows if len(p) >= 10]
+
+    def ts(p):
+        try:
+            return datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
             return None
-        sm.sort()
-        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": sm_max, "reasons": sorted(reasons),
-                "samples": len(sm), "in_timed_region": bool(inside)}
+
+    inside = [p for p in rows if t_start and t_stop and ts(p) is not None
+              and t_start - 0.1 <= ts(p) <= t_stop + 0.1]
+    use = inside or rows
+    sm, reasons, sm_max = [], set(), None
+    for p in use:
+        try:
+            mhz, mx = float(p[2]), float(p[3])
+        except ValueError:
+            continue
+        sm_max = mx
+        sm.append(mhz)
+        for name, flag in zip(CLOCK_REASONS, p[6:10]):
+            if flag.lower().startswith("active"):
+                reasons.add(name)
+    if not sm:
+        return None
+    sm.sort()
+    return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": sm_max, "reasons": sorted(reasons),
+            "samples": len(sm), "in_timed_region": bool(inside)}
 
 
 def gpu_uuid(device_index: int) -> str:

@@ -1,0 +1,78 @@
+"""Host logic of bench.py that needs no GPU: the summary of the nvidia-smi
+clock samples that goes into the bench line (median SM clock, maximum SM
+clock, throttle reasons seen inside the timed region)."""
+import datetime
+
+import bench
+
+
+def _line(t, sm, mx=2070, reasons=("Not Active",) * 4):
+    stamp = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    return ", ".join([stamp, "0", str(sm), str(mx), "1100.50", "0x0000000000000000",
+                      *reasons]) + "\n"
+
+
+T0 = 1_800_000_000.0
+
+
+def test_median_and_max_over_the_timed_region():
+    lines = [_line(T0 + 0.2 * k, sm) for k, sm in enumerate([1500, 2070, 2070, 1980, 2070])]
+    got = bench.summarise_clocks(lines, T0 + 0.15, T0 + 0.85)
+    # samples at 0.2, 0.4, 0.6, 0.8 fall inside (0.0 is 150 ms before the start)
+    assert got == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 4,
+                   "in_timed_region": True}
+
+
+def test_reasons_are_taken_only_inside_the_timed_region():
+    hot = ("Not Active", "Active", "Not Active", "Active")      # hw_thermal, sw_power_cap
+    lines = [_line(T0, 2070, reasons=("Active",) * 4),          # before the region
+             _line(T0 + 1.0, 1900, reasons=hot), _line(T0 + 1.2, 1950),
+             _line(T0 + 3.0, 2070, reasons=("Active",) * 4)]    # after it
+    got = bench.summarise_clocks(lines, T0 + 0.95, T0 + 1.25)
+    assert got["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert got["samples"] == 2 and got["in_timed_region"]
+    assert got["sm_mhz"] == 1950.0
+
+
+def test_every_sample_is_used_when_none_fell_inside():
+    lines = [_line(T0, 1800), _line(T0 + 0.2, 1900, reasons=("Active",) + ("Not Active",) * 3)]
+    got = bench.summarise_clocks(lines, T0 + 5.0, T0 + 5.01)
+    assert got["samples"] == 2 and not got["in_timed_region"]
+    assert got["reasons"] == ["hw_slowdown"]
+
+
+def test_malformed_and_unsupported_fields_are_skipped():
+    lines = ["\n", "garbage\n", _line(T0, "[N/A]"), _line(T0 + 0.1, 2070)]
+    got = bench.summarise_clocks(lines, T0 - 1, T0 + 1)
+    assert got["samples"] == 1 and got["sm_mhz"] == 2070.0
+    assert bench.summarise_clocks(["x\n"], T0, T0 + 1) is None
+    assert bench.summarise_clocks([], None, None) is None
+
+
+def test_sampler_runs_a_fake_nvidia_smi_and_summarises_its_output(tmp_path, monkeypatch):
+    """The sampler's process handling end to end, with a stand-in
+    nvidia-smi on PATH that prints one sample every 50 ms until stopped."""
+    import os
+    import time
+
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text(
+        "#!/usr/bin/env python3\n"
+        "import datetime, sys, time\n"
+        "while True:\n"
+        "    s = datetime.datetime.now().strftime('%Y/%m/%d %H:%M:%S.%f')[:-3]\n"
+        "    print(f'{s}, 0, 1965, 2070, 900.00, 0x0, Not Active, Not Active, Not Active, "
+        "Active', flush=True)\n"
+        "    time.sleep(0.05)\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
+    s = bench.ClockSampler("0")
+    s.start()
+    s.mark_start()
+    time.sleep(0.4)
+    s.mark_stop()
+    got = s.stop()
+    assert got is not None and got["in_timed_region"]
+    assert got["sm_mhz"] == 1965.0 and got["sm_max_mhz"] == 2070.0
+    assert got["reasons"] == ["sw_power_cap"] and got["samples"] >= 3
+    assert not os.path.exists(s.path)
