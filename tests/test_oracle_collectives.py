@@ -98,3 +98,59 @@ def test_shard_len_hand_computed(n, R, align, S):
 def test_uneven_layout_padding_count():
     S = oracle.shard_len(100000007, 7, 64)
     assert 7 * S - 100000007 == 313
+
+
+def _replica_mismatches(P):
+    """Indices where any replica differs from replica 0, in order (the check
+    zero_check_replicas makes on the device)."""
+    bad = np.zeros(P[0].size, bool)
+    for p in P[1:]:
+        bad |= p != P[0]
+    return np.flatnonzero(bad)
+
+
+@pytest.mark.parametrize("n,R,c,d", [(1000, 4, 2, 0), (4099, 8, 7, 3), (130, 7, 0, 6)])
+def test_dropped_allgather_message_is_found_by_replica_equality(n, R, c, d):
+    """A rank failure made in the card-by-card emulation (LLM infra 06,
+    section 15.4, silent data corruption): card d never receives card c's
+    all-gather message, so its replica keeps last step's values on c's shard.
+    Replica equality finds exactly the elements of that shard whose bf16
+    value changed this step, and no others; a clean step has none."""
+    M, align = 1, 64
+    rng = np.random.default_rng(n + R)
+    S = oracle.shard_len(n, R, align)
+    G = [np.array([oracle.bf16_rne(x) for x in rng.normal(0, 1e-3, n)], np.uint16)
+         for _ in range(R * M)]
+    W = np.zeros(R * S, np.float32)
+    W[:n] = rng.normal(0, 0.02, n)
+    m = np.zeros(R * S, np.float32)
+    v = np.zeros(R * S, np.float32)
+    before = np.array([oracle.bf16_rne(x) for x in W[:n]], np.uint16)
+    P = [before.copy() for _ in range(R)]
+    oracle.zero_step(G, W, m, v, P, oracle.hparams(), 1, R, M, n, S)
+    assert _replica_mismatches(P).size == 0
+    lo, hi = c * S, min((c + 1) * S, n)
+    assert hi > lo
+    P[d][lo:hi] = before[lo:hi]                   # the dropped message
+    got = _replica_mismatches(P)
+    good = P[(d + 1) % R]                         # a card that did receive it
+    changed = lo + np.flatnonzero(good[lo:hi] != before[lo:hi])
+    assert changed.size > 0
+    assert np.array_equal(got, changed)
+
+
+def test_corrupted_replica_element_is_found_by_replica_equality():
+    """One bit flipped in one card's list element after a clean step."""
+    n, R, M = 777, 4, 2
+    rng = np.random.default_rng(5)
+    S = oracle.shard_len(n, R)
+    G = [np.array([oracle.bf16_rne(x) for x in rng.normal(0, 1e-3, n)], np.uint16)
+         for _ in range(R * M)]
+    W = np.zeros(R * S, np.float32)
+    W[:n] = rng.normal(0, 0.02, n)
+    m = np.zeros(R * S, np.float32)
+    v = np.zeros(R * S, np.float32)
+    P = [np.zeros(n, np.uint16) for _ in range(R)]
+    oracle.zero_step(G, W, m, v, P, oracle.hparams(), 1, R, M, n, S)
+    P[3][500] ^= np.uint16(1)
+    assert _replica_mismatches(P).tolist() == [500]
