@@ -439,3 +439,21 @@ def test_empty_plan_is_a_no_op_for_every_step_entry_point():
                                   None) == B.ZERO_ERR_INVALID_ARG
     assert L.zero_step_host(pl.ptr, None, None, None, None, None, pa, host_out, hp, 1, 0, None,
                             None) == B.ZERO_ERR_NULL
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """No fallback: with the shared library absent, the first call through
+    the binding raises instead of computing anything another way (checked in
+    a child process, so this process keeps its loaded library)."""
+    import subprocess
+    import sys
+    code = ("import zero_optimizer_step_rs_gb300.binding as B\n"
+            f"B.LIB_PATH = {str(tmp_path / 'libzero_step.so')!r}\n"
+            "try:\n"
+            "    B.Plan([1000], 2, 1, 1)\n"
+            "except RuntimeError as e:\n"
+            "    assert 'is missing' in str(e), e\n"
+            "    print('raised')\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                       timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "raised", r.stdout + r.stderr
