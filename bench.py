@@ -189,30 +189,82 @@ def oracle_prepare(wl, n, threads=None):
     return {"G": G, "W0": W0, "m0": m0, "v0": v0, "P": P, "threads": threads, "n": n}
 
 
-def oracle_pass(wl, ctx):
-    """One timed pass of the oracle (unchanged) over the prepared sample;
-    returns seconds."""
+# the oracle function that defines each measured step (only the plain step
+# has a multithreaded form; the others run on one core)
+ORACLE_FN = {"fused": "oracle_dp_step_mt", "staged": "oracle_dp_step_mt",
+             "tma": "oracle_dp_step_mt", "clipped": "oracle_dp_step_clipped",
+             "compressed": "oracle_dp_step_compressed", "onebit": "oracle_onebit_step",
+             "zero3": "oracle_zero3_step"}
+
+
+def oracle_step_opts(args=None) -> dict:
+    """The step a bench line measures, as the oracle leg needs it."""
+    if args is None:
+        return {"variant": "fused"}
+    return {"variant": args.variant, "codec": args.codec, "ef": args.ef,
+            "max_norm": args.max_norm}
+
+
+def oracle_threads(ctx, variant: str) -> int:
+    return ctx["threads"] if ORACLE_FN[variant] == "oracle_dp_step_mt" else 1
+
+
+def oracle_pass(wl, ctx, variant="fused", codec="int8", ef=False, max_norm=1.0):
+    """One timed pass of the oracle (unchanged) of the step `variant`
+    measures, over the prepared sample; returns seconds.  Buffers the step
+    needs besides the sample (zero residuals, padded ZeRO-3 state, the
+    parameter shard) are made before the clock starts."""
+    import numpy as np
+
     import oracle
-    Wc, mc, vc = ctx["W0"].copy(), ctx["m0"].copy(), ctx["v0"].copy()
+    n, R, M, t = ctx["n"], wl.R, wl.M, wl.step
     hp = oracle.hparams(**wl.hparams())
-    t0 = time.perf_counter()
-    oracle.dp_step(ctx["G"], Wc, mc, vc, ctx["P"], hp, wl.step, wl.R, wl.M,
-                   nthreads=ctx["threads"])
+    G, P = ctx["G"], ctx["P"]
+    if variant == "zero3":
+        S = oracle.shard_len(n, R)
+        Wc, mc, vc = (np.zeros(R * S, np.float32) for _ in range(3))
+        Wc[:n], mc[:n], vc[:n] = ctx["W0"], ctx["m0"], ctx["v0"]
+        Ps = np.zeros(R * S, np.uint16)
+        t0 = time.perf_counter()
+        oracle.zero3_step(G, Wc, mc, vc, Ps, hp, t, R, M, n, S)
+        return time.perf_counter() - t0
+    Wc, mc, vc = ctx["W0"].copy(), ctx["m0"].copy(), ctx["v0"].copy()
+    if variant == "clipped":
+        t0 = time.perf_counter()
+        oracle.dp_step_clipped(G, Wc, mc, vc, P, hp, t, R, M, max_norm)
+    elif variant == "compressed":
+        kind = {"fp16": oracle.COMP_FP16, "int8": oracle.COMP_INT8,
+                "sign": oracle.COMP_SIGN}[codec]
+        E = [np.zeros(n, np.float32) for _ in range(R)] if ef else None
+        t0 = time.perf_counter()
+        oracle.dp_step_compressed(G, Wc, mc, vc, P, hp, t, R, M, kind, E)
+    elif variant == "onebit":
+        S = oracle.shard_len(n, R, 128)
+        E = [np.zeros(n, np.float32) for _ in range(R)]
+        Es = np.zeros(n, np.float32)
+        t0 = time.perf_counter()
+        oracle.onebit_step(G, Wc, mc, vc, P, hp, t, max(1, t - 1), R, M, S, E, Es)
+    else:
+        t0 = time.perf_counter()
+        oracle.dp_step(G, Wc, mc, vc, P, hp, t, R, M, nthreads=ctx["threads"])
     return time.perf_counter() - t0
 
 
-def oracle_sample_rate(wl, target_s=12.0, sample_elems=1 << 24, threads=None):
-    """Time the oracle on the first sample_elems params of the workload,
-    repeated until target_s of CPU time; returns params/s, cores, text."""
+def oracle_sample_rate(wl, target_s=12.0, sample_elems=1 << 24, threads=None, opts=None):
+    """Time the oracle of the measured step (opts, from oracle_step_opts) on
+    the first sample_elems params of the workload, repeated until target_s of
+    CPU time; returns params/s, cores, text."""
+    opts = opts or {"variant": "fused"}
     n = min(sample_elems, wl.N)
     ctx = oracle_prepare(wl, n, threads)
     reps, elapsed = 0, 0.0
     while elapsed < target_s or reps == 0:
-        elapsed += oracle_pass(wl, ctx)
+        elapsed += oracle_pass(wl, ctx, **opts)
         reps += 1
-    desc = (f"oracle_dp_step_mt over the first {n:,} params of the workload "
-            f"(same R, M, distributions), {reps} passes, {elapsed:.1f} s")
-    return n * reps / elapsed, ctx["threads"], desc
+    cores = oracle_threads(ctx, opts["variant"])
+    desc = (f"{ORACLE_FN[opts['variant']]} over the first {n:,} params of the workload "
+            f"(same R, M, distributions), {cores} thread(s), {reps} passes, {elapsed:.1f} s")
+    return n * reps / elapsed, cores, desc
 
 
 def _tree_levels(N: int):
@@ -470,7 +522,7 @@ def run_ours(args, rank, world, local_rank):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, cores, desc = oracle_sample_rate(wl)
+        rate, cores, desc = oracle_sample_rate(wl, opts=oracle_step_opts(args))
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
 
     if rank != 0:
@@ -957,28 +1009,37 @@ def run_ckpt(args):
 
 def run_reference(args):
     """The oracle as it stands, on the host cores: each step is one pass of
-    oracle_dp_step_mt over a bounded sample (the first 2^22 params) of the
+    the oracle of the measured step (oracle_dp_step_mt for the default
+    fused step) over a bounded sample (the first 2^22 params) of the
     workload."""
     from zgen import workloads as W
     wl = W.by_name(args.workload)
     t0 = time.time()
     sample = min(wl.N, 1 << 22)
     ctx = oracle_prepare(wl, sample)
+    opts = oracle_step_opts(args)
     for _ in range(args.warmup):
-        oracle_pass(wl, ctx)
-    per_step = [oracle_pass(wl, ctx) for _ in range(args.steps)]
+        oracle_pass(wl, ctx, **opts)
+    per_step = [oracle_pass(wl, ctx, **opts) for _ in range(args.steps)]
+    cores = oracle_threads(ctx, args.variant)
     mean_s = sum(per_step) / len(per_step)
     value = sample / mean_s
-    desc = (f"oracle_dp_step_mt over the first {sample:,} params of the workload "
-            f"(same R, M, distributions), {ctx['threads']} threads, one pass per step")
+    desc = (f"{ORACLE_FN[args.variant]} over the first {sample:,} params of the workload "
+            f"(same R, M, distributions), {cores} thread(s), one pass per step")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean_s,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded counter-based generator; shapes of the named parameter set)",
         "config": {"workload": wl.name, "N": wl.N, "R": wl.R, "M": wl.M, "stage": wl.stage,
-                   "step": wl.step, "sample_params_per_step": sample},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": ctx["threads"], "kind": "oracle",
+                   "step": wl.step, "variant": args.variant,
+                   **({"max_norm": args.max_norm} if args.variant == "clipped" else {}),
+                   **({"codec": args.codec, "error_feedback": args.ef}
+                      if args.variant == "compressed" else {}),
+                   **({"freeze_step": max(1, wl.step - 1), "align": 128}
+                      if args.variant == "onebit" else {}),
+                   "sample_params_per_step": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "wall_s": round(time.time() - t0, 1),

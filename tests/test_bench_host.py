@@ -1,7 +1,11 @@
 """Host logic of bench.py that needs no GPU: the summary of the nvidia-smi
 clock samples that goes into the bench line (median SM clock, maximum SM
-clock, throttle reasons seen inside the timed region)."""
+clock, throttle reasons seen inside the timed region), and the oracle leg
+(cpu_baseline and the reference arm) timing the oracle of the measured step."""
 import datetime
+import os
+
+import pytest
 
 import bench
 
@@ -76,3 +80,31 @@ def test_sampler_runs_a_fake_nvidia_smi_and_summarises_its_output(tmp_path, monk
     assert got["sm_mhz"] == 1965.0 and got["sm_max_mhz"] == 2070.0
     assert got["reasons"] == ["sw_power_cap"] and got["samples"] >= 3
     assert not os.path.exists(s.path)
+
+
+
+@pytest.mark.parametrize("variant,extra", [
+    ("fused", {}), ("clipped", {"max_norm": 0.5}), ("zero3", {}), ("onebit", {}),
+    ("compressed", {"codec": "sign", "ef": True}), ("compressed", {"codec": "int8"})])
+def test_reference_arm_times_the_oracle_of_the_measured_step(variant, extra):
+    """bench.py --impl reference (and the cpu_baseline of a --variant line)
+    time the oracle function that defines the step the line measures, on the
+    line's own config, with the thread count that function really uses."""
+    import argparse
+    args = argparse.Namespace(workload="uneven", variant=variant, steps=1, warmup=3,
+                              codec=extra.get("codec", "int8"), ef=extra.get("ef", False),
+                              max_norm=extra.get("max_norm", 1.0))
+    line = bench.run_reference(args)
+    cfg = line["config"]
+    assert line["impl"] == "reference" and cfg["variant"] == variant
+    assert cfg["R"] == 7 and cfg["M"] == 4 and line["value"] > 0
+    fn = bench.ORACLE_FN[variant]
+    assert line["cpu_baseline"]["sample"].startswith(fn)
+    assert (line["cpu_baseline"]["cores"] > 1) == (fn == "oracle_dp_step_mt" and
+                                                    (os.cpu_count() or 1) > 1)
+    if variant == "compressed":
+        assert cfg["codec"] == extra["codec"] and cfg["error_feedback"] == extra.get("ef", False)
+    if variant == "clipped":
+        assert cfg["max_norm"] == 0.5
+    if variant == "onebit":
+        assert cfg["freeze_step"] == 1 and cfg["align"] == 128
