@@ -903,7 +903,35 @@ def run_table(args):
                    "GB_s": round(wl.bytes_per_param() * n / tpass / 1e9, 2)}
             rows.append(row)
             print(json.dumps(row), flush=True)
+    for row in oracle_variant_rows():
+        rows.append(row)
+        print(json.dumps(row), flush=True)
     return rows
+
+
+TABLE_VARIANT_STEPS = (
+    {"variant": "clipped", "max_norm": 1.0},
+    *({"variant": "compressed", "codec": c, "ef": ef}
+      for c in ("fp16", "int8", "sign") for ef in (False, True)),
+    {"variant": "onebit"},
+    {"variant": "zero3"},
+)
+
+
+def oracle_variant_rows(name="llama-3.2-1b", n=1 << 22, reps=3):
+    """The oracles of the clipped, compressed, 1-bit Adam and ZeRO-3 steps
+    (one core each, as they stand) on the first n params of the workload
+    their GPU rows measure; best of reps passes each."""
+    from zgen import workloads as W
+    wl = W.ALL[name]()
+    n = min(wl.N, n)
+    ctx = oracle_prepare(wl, n, threads=1)
+    out = []
+    for opts in TABLE_VARIANT_STEPS:
+        tpass = min(oracle_pass(wl, ctx, **opts) for _ in range(reps))
+        out.append({"workload": name, "oracle": ORACLE_FN[opts["variant"]], **opts,
+                    "oracle_threads": 1, "sample_params": n, "params_per_s": n / tpass})
+    return out
 
 
 # --------------------------------------------------------- checkpoints --

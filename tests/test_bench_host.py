@@ -108,3 +108,13 @@ def test_reference_arm_times_the_oracle_of_the_measured_step(variant, extra):
         assert cfg["max_norm"] == 0.5
     if variant == "onebit":
         assert cfg["freeze_step"] == 1 and cfg["align"] == 128
+
+
+def test_table_oracle_rows_of_the_step_variants():
+    rows = bench.oracle_variant_rows(n=1 << 14, reps=1)
+    assert [r["variant"] for r in rows] == ["clipped"] + ["compressed"] * 6 + ["onebit", "zero3"]
+    assert {(r.get("codec"), r.get("ef")) for r in rows if r["variant"] == "compressed"} == {
+        (c, e) for c in ("fp16", "int8", "sign") for e in (False, True)}
+    for r in rows:
+        assert r["oracle"] == bench.ORACLE_FN[r["variant"]] and r["params_per_s"] > 0
+        assert r["sample_params"] == 1 << 14 and r["oracle_threads"] == 1
