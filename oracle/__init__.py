@@ -9,7 +9,7 @@ it; the seeded input generator ``zgen`` is the only module both sides use.
 The arithmetic lives in ``zero_oracle.c`` (plain C11, one float operation at
 a time, no FMA contraction); this file only builds it with gcc and marshals
 numpy arrays.  See ``zero_oracle.h`` for the passages each function follows
-and for the readings R1-R15 taken where the pages leave a step open.
+and for the readings R1-R16 taken where the pages leave a step open.
 """
 from __future__ import annotations
 

@@ -2,7 +2,7 @@
  * zero_oracle.c - CPU oracle for the ZeRO-1/2 mixed-precision AdamW step.
  *
  * TEST INFRASTRUCTURE, NOT PRODUCT CODE (see zero_oracle.h for who may load
- * it, the passages each function follows and the readings R1-R15).
+ * it, the passages each function follows and the readings R1-R16).
  *
  * Build: gcc -std=c11 -O2 -ffp-contract=off -fno-fast-math -fPIC -shared
  * (-ffp-contract=off keeps every float * and + separately rounded, which is

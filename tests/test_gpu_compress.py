@@ -1,5 +1,6 @@
-"""GPU parity of the step with a compressed reduce-scatter (reading R14):
-zero_step_compressed through the C ABI against oracle.dp_step_compressed,
+"""GPU parity of the step with a compressed reduce-scatter (reading R14 of
+oracle/zero_oracle.h): zero_step_compressed through the C ABI against
+oracle.dp_step_compressed,
 for fp16, block-int8 and sign codecs, with and without error feedback, over
 several steps (the residuals carried between them), ragged sizes around the
 128-element blocks, and run-time (R, M).  Everything bit for bit."""

@@ -1,5 +1,5 @@
-"""GPU parity of the 1-bit Adam step (reading R15): zero_step_onebit through
-the C ABI against oracle.onebit_step, bit for bit.
+"""GPU parity of the 1-bit Adam step (reading R15 of oracle/zero_oracle.h):
+zero_step_onebit through the C ABI against oracle.onebit_step, bit for bit.
 
 - Small cases: ragged sizes around the 128-element blocks, and several
   (R, M) pairs, compile-time and run-time.  The warm-up steps and several

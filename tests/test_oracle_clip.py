@@ -1,4 +1,4 @@
-"""Pins of the oracle's global-norm clipping (readings R10-R12).
+"""Pins of the oracle's global-norm clipping (readings R10-R12 of oracle/zero_oracle.h).
 
 The squared norm is pinned by closed forms, by math.fsum, and by a hand-worked
 case whose pairwise, left-to-right and exact sums all differ

@@ -1,7 +1,8 @@
-"""Pins of the oracle's gradient compression (reading R14): binary16 rounding
-against numpy's float16 (an independent implementation of the same rule) and
-hand-worked int8 / sign blocks; the compressed step reduces to the plain step
-whenever compression is exact; error feedback keeps exactly what was dropped."""
+"""Pins of the oracle's gradient compression (reading R14 of
+oracle/zero_oracle.h): binary16 rounding against numpy's float16 (an
+independent implementation of the same rule) and hand-worked int8 / sign
+blocks; the compressed step reduces to the plain step whenever compression is
+exact; error feedback keeps exactly what was dropped."""
 import numpy as np
 import pytest
 

@@ -1,4 +1,4 @@
-"""Pins of the oracle's 1-bit Adam step (reading R15).
+"""Pins of the oracle's 1-bit Adam step (reading R15 of oracle/zero_oracle.h).
 
 - The warm-up steps are the plain step, bit for bit.
 - A hand-worked two-rank example (tests/golden/onebit_example.txt) fixes the

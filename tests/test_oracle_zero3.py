@@ -1,5 +1,5 @@
-"""Pins of the oracle's ZeRO-3 emulation (reading R13): bit-identical to plain
-DP (CS324 Lecture 9 notes, section 3.4), per-unit all-gathers that rebuild
+"""Pins of the oracle's ZeRO-3 emulation (reading R13 of oracle/zero_oracle.h):
+bit-identical to plain DP (CS324 Lecture 9 notes, section 3.4), per-unit all-gathers that rebuild
 the DP replica, and the pages' per-card traffic (exercise 7)."""
 import numpy as np
 import pytest
