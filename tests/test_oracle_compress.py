@@ -42,6 +42,7 @@ def test_fp16_hand_cases():
 
 
 @pytest.mark.parametrize("key,kind", [("int8", oracle.COMP_INT8), ("int8b", oracle.COMP_INT8),
+                                      ("int8c", oracle.COMP_INT8),
                                       ("sign", oracle.COMP_SIGN), ("signz", oracle.COMP_SIGN)])
 def test_hand_worked_blocks(key, kind):
     gd = load_golden("compress_examples.txt")

@@ -90,6 +90,44 @@ MUTANTS = {
     "onebit_bias_correction_at_t": ("float q = root / sf.bc2_sqrt;", "float q = root / s.bc2_sqrt;"),
 }
 
+# Further slips, one per site: the moment coefficients, the bias-correction
+# and decay scalars, the decay order, the collectives' first and own terms,
+# the codecs' thresholds and sign rules, and the 1-bit update's state.
+MUTANTS.update({
+    "first_moment_uses_beta2": ("float a = s->beta1 * *m;", "float a = s->beta2 * *m;"),
+    "second_moment_uses_one_minus_beta1": ("float d = s->one_minus_beta2 * g;",
+                                           "float d = s->one_minus_beta1 * g;"),
+    "update_uses_old_first_moment": ("float ratio = m1 / den;", "float ratio = *m / den;"),
+    "decay_after_update": ("*w = wd - upd;", "*w = (*w - upd) * s->decay + 0.0f * wd;"),
+    "decay_without_lr": ("out->decay = (float)(1.0 - lr * wd);",
+                         "out->decay = (float)(1.0 - wd + 0.0 * lr);"),
+    "bias_correction_2_uses_beta1": ("double bc2 = 1.0 - pow(b2, t);",
+                                     "double bc2 = 1.0 - pow(b1, t);"),
+    "rs_sum_skips_first_rank": ("float acc = in[0][lo + k];", "float acc = 0.0f * in[0][lo + k];"),
+    "ring_reduce_overwrites": ("cards[dst][e] = cards[dst][e] + msg[(int64_t)k * csz + (e - lo)];",
+                               "cards[dst][e] = msg[(int64_t)k * csz + (e - lo)];"),
+    "zero3_bytes_params_unsharded": ("out[3] = N * (bp + bg + bo) / P;",
+                                     "out[3] = N * bp + N * (bg + bo) / P;"),
+    "clip_uses_sumsq_as_norm": ("double norm = sqrt(sumsq);", "double norm = sumsq;"),
+    "zero3_gather_counts_own_elements": ("if (owner != card) ++from_others;",
+                                         "if (owner != card || 1) ++from_others;"),
+    "fp16_overflow_at_max_finite": ("if (a >= 0x477FF000u)", "if (a > 0x477FE000u)"),
+    "int8_amax_signed": ("float a = fabsf(xb[k]);", "float a = xb[k];"),
+    "sign_of_zero_negative": ("db[k] = xb[k] < 0.0f ? -s : s;", "db[k] = xb[k] <= 0.0f ? -s : s;"),
+    "compressed_divides_by_R": ("float g = acc[i] / s.denom_rm;", "float g = acc[i] / (float)R;"),
+    "onebit_server_average_not_divided": ("y[i] = dsum[i] / denom_r + Es[i];",
+                                          "y[i] = dsum[i] + Es[i] + 0.0f * denom_r;"),
+    "onebit_step_size_at_freeze": ("float upd = s.step_size * ratio;",
+                                   "float upd = sf.step_size * ratio;"),
+    "onebit_no_decay": ("float wd = W[i] * s.decay;", "float wd = W[i];"),
+    "onebit_momentum_not_stored": ("m[i] = mi;", "(void)mi;"),
+    "zero_rs_reads_unshifted_chunk": (
+        "gshard[k] = oracle_avg_grad((const uint16_t* const*)recv_ptr, R, M, k,",
+        "gshard[k] = oracle_avg_grad((const uint16_t* const*)G + 0 * (recv_ptr != 0), R, M, k,"),
+    "zero3_update_cast_truncates": ("Pshard[i] = oracle_bf16_rne(W[i]);",
+                                    "Pshard[i] = (uint16_t)(f2u(W[i]) >> 16);"),
+})
+
 
 PIN_SUITES = ["tests/test_oracle_pins.py", "tests/test_oracle_collectives.py",
               "tests/test_oracle_clip.py", "tests/test_oracle_zero3.py",
