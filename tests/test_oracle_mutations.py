@@ -126,6 +126,35 @@ MUTANTS.update({
         "gshard[k] = oracle_avg_grad((const uint16_t* const*)G + 0 * (recv_ptr != 0), R, M, k,"),
     "zero3_update_cast_truncates": ("Pshard[i] = oracle_bf16_rne(W[i]);",
                                     "Pshard[i] = (uint16_t)(f2u(W[i]) >> 16);"),
+    "zero3_gather_local_index": ("out[i - lo] = Pshard[i];", "out[i - lo] = Pshard[i - lo];"),
+    "zero3_unit_counts_whole_unit": (
+        "if (recv && k % M == 0 && k / M != r) recv[r] += b - a;",
+        "if (recv && k % M == 0 && k / M != r) recv[r] += hi - lo + 0 * (b - a);"),
+    "zero3_unit_writes_local_index": (
+        "gshard[i] = oracle_avg_grad((const uint16_t* const*)ptr, R, M, i - a, denom_rm);",
+        "gshard[i - a] = oracle_avg_grad((const uint16_t* const*)ptr, R, M, i - a, denom_rm);"),
+    "mt_ranges_overlap": ("jb->hi = n * (k + 1) / nthreads;",
+                          "jb->hi = n * (k + 1) / nthreads + (k + 1 < nthreads);"),
+    "denom_R_plus_M": ("out->denom_rm = (float)((double)R * (double)M);",
+                       "out->denom_rm = (float)((double)R + (double)M);"),
+    "bf16_nan_keeps_payload": ("return (uint16_t)0x7FC0u;", "return (uint16_t)((u >> 16) | 0x40u);"),
+    "eps_before_bias_correction": ("float den = q + s->eps;",
+                                   "float den = (root + s->eps) / s->bc2_sqrt + 0.0f * q;"),
+    "dp_cast_before_update": (
+        "float g = oracle_avg_grad(G, R, M, i, s.denom_rm);\n"
+        "        oracle_adamw_elem(&s, g, &W[i], &m[i], &v[i]);\n"
+        "        uint16_t p = oracle_bf16_rne(W[i]);",
+        "float g = oracle_avg_grad(G, R, M, i, s.denom_rm);\n"
+        "        uint16_t p = oracle_bf16_rne(W[i]);\n"
+        "        oracle_adamw_elem(&s, g, &W[i], &m[i], &v[i]);"),
+    "onebit_momentum_coefficients_swapped": (
+        "float ml = s.beta1 * m[i] + s.one_minus_beta1 * gl;",
+        "float ml = s.beta1 * gl + s.one_minus_beta1 * m[i];"),
+    "compressed_ef_of_next_rank": ("x[i] = E ? loc + E[r][i] : loc;",
+                                   "x[i] = E ? loc + E[(r + 1) % R][i] : loc;"),
+    "clip_norm_of_unaveraged_sum": (
+        "for (int64_t i = 0; i < n; ++i) g[i] = oracle_avg_grad(G, R, M, i, s.denom_rm);",
+        "for (int64_t i = 0; i < n; ++i) g[i] = oracle_avg_grad(G, R, M, i, 1.0f + 0.0f * s.denom_rm);"),
 })
 
 
