@@ -457,3 +457,35 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
                        timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == "raised", r.stdout + r.stderr
+
+
+def test_product_and_oracle_share_no_code():
+    """The CUDA path and the oracle are independent: neither library defines
+    or references the other's symbols, and neither source tree includes or
+    imports the other (the input generator zgen is the one shared module)."""
+    import shutil
+    import subprocess
+    import oracle
+    oracle.build()
+    pkg = os.path.join(ROOT, "zero_optimizer_step_rs_gb300")
+    if shutil.which("nm"):
+        prod = subprocess.run(["nm", "-D", B.LIB_PATH], capture_output=True, text=True,
+                              check=True).stdout
+        orc = subprocess.run(["nm", "-D", oracle.LIB_PATH], capture_output=True, text=True,
+                             check=True).stdout
+        assert "oracle_" not in prod
+        assert not re.search(r"\bzero_[a-z]", orc) and "zgen_" not in orc
+    for d in (pkg, os.path.join(pkg, "csrc"), os.path.join(ROOT, "include")):
+        for f in os.listdir(d):
+            if f.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
+                src = open(os.path.join(d, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
+                assert not re.search(r"^\s*#\s*include\s+.*oracle", src, re.M), f
+                assert "liboracle" not in src, f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c", ".h")):
+            src = open(os.path.join(ROOT, "oracle", f)).read()
+            assert not re.search(r"^\s*#\s*include\s+.*(zero_step|csrc)", src, re.M), f
+            assert not re.search(r"^\s*(import|from)\s+zero_optimizer_step_rs_gb300\b",
+                                 src, re.M), f
+            assert "libzero_step" not in src, f
