@@ -314,3 +314,33 @@ def test_nonfinite_gradients_propagate():
     oracle.dp_step(G, W, m, v, P, hp, 1, 1, 1)
     assert np.isnan(W[0]) and np.isnan(W[1]) and np.isfinite(W[2])
     assert P[0][0] == 0x7FC0 and P[0][1] == 0x7FC0
+
+
+def test_compiled_oracle_rounds_every_operation_on_its_own():
+    """Reading R2 is a property of the compiled oracle, not only of its source:
+    a compiler that contracted a*b + c into one fused multiply-add (GNU C's
+    default on some targets, Arm among them) would change low bits.  Over
+    200,000 random elements the compiled step must equal the same sequence
+    evaluated in numpy float32, where every operation is rounded on its own
+    and sqrt and division are correctly rounded."""
+    rng = np.random.default_rng(2024)
+    n, t = 200_000, 7
+    hp = oracle.hparams(lr=3e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+    g16 = np.array([oracle.bf16_rne(x) for x in rng.normal(0, 1e-2, n)], np.uint16)
+    W0 = rng.normal(0, 0.02, n).astype(np.float32)
+    m0 = rng.normal(0, 1e-3, n).astype(np.float32)
+    v0 = (rng.normal(0, 1e-2, n) ** 2).astype(np.float32)
+    W, m, v = W0.copy(), m0.copy(), v0.copy()
+    P = [np.zeros(n, np.uint16)]
+    oracle.dp_step([g16], W, m, v, P, hp, t, 1, 1)
+    s = oracle.make_scalars(hp, t, 1, 1)
+    f = np.float32
+    g = (g16.astype(np.uint32) << 16).view(np.float32) / f(s.denom_rm)
+    wd = W0 * f(s.decay)
+    m1 = f(s.beta1) * m0 + f(s.one_minus_beta1) * g
+    v1 = f(s.beta2) * v0 + (f(s.one_minus_beta2) * g) * g
+    den = np.sqrt(v1) / f(s.bc2_sqrt) + f(s.eps)
+    w1 = wd - f(s.step_size) * (m1 / den)
+    for got, want in ((W, w1), (m, m1), (v, v1)):
+        assert got.dtype == want.dtype == np.float32
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
