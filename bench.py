@@ -60,28 +60,106 @@ def measured_peaks():
 
 # ------------------------------------------------------------ clocks --
 
+class _NvmlClocks:
+    """Read-only NVML queries of one GPU (SM clock, its maximum, board power
+    and the clock-event reasons), through the driver's libnvidia-ml."""
+
+    LIB = "libnvidia-ml.so.1"
+    SM = 1                                            # NVML_CLOCK_SM
+    BITS = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20,
+            "sw_power_cap": 0x4}
+
+    def __init__(self, uuid: str):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL(self.LIB)
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise OSError(f"no NVML handle for {uuid}")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.max_mhz = self._uint(self.lib.nvmlDeviceGetMaxClockInfo, self.SM)
+
+    def _uint(self, fn, *args):
+        x = self.c.c_uint(0)
+        rc = fn(self.h, *args, self.c.byref(x))
+        return x.value if rc == 0 else None
+
+    def line(self) -> str:
+        """One sample in nvidia-smi's CSV form (timestamp, then the fields of
+        ClockSampler.FIELDS)."""
+        import datetime
+        sm = self._uint(self.lib.nvmlDeviceGetClockInfo, self.SM)
+        mw = self._uint(self.lib.nvmlDeviceGetPowerUsage)
+        r = self.c.c_ulonglong(0)
+        ok = self.reasons_fn(self.h, self.c.byref(r)) == 0
+        stamp = datetime.datetime.now().strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        flags = [("Active" if r.value & b else "Not Active") if ok else "[N/A]"
+                 for b in self.BITS.values()]
+        return ", ".join([stamp, "0", str(sm if sm is not None else "[N/A]"),
+                          str(self.max_mhz if self.max_mhz is not None else "[N/A]"),
+                          "%.2f" % (mw / 1e3) if mw is not None else "[N/A]",
+                          "0x%016x" % r.value, *flags]) + "\n"
+
+
 class ClockSampler:
-    """nvidia-smi clocks/throttle reasons sampled every 200 ms in the
-    background; read-only queries."""
+    """SM clocks and throttle reasons sampled in the background while the
+    timed region runs; read-only queries.  NVML is polled every 5 ms from a
+    thread when the driver's library loads (a 0.2 s timed region still gets
+    dozens of samples); otherwise `nvidia-smi -lms 20` runs beside the
+    process."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NVML_PERIOD_S = 0.005
+    SMI_PERIOD_MS = 20
 
-    def __init__(self, gpu_id: str):
+    def __init__(self, gpu_id: str, use_nvml=None):
         self.gpu_id = gpu_id
+        self.use_nvml = use_nvml
         self.proc = None
         self.path = None
+        self.thread = None
+        self.lines = []
+        self.source = None
         self.t_start = self.t_stop = None
 
+    def _start_nvml(self):
+        import threading
+        try:
+            nv = _NvmlClocks(self.gpu_id)
+        except (OSError, AttributeError):
+            return False
+        self._halt = threading.Event()
+
+        def poll():
+            while not self._halt.is_set():
+                try:
+                    self.lines.append(nv.line())
+                except Exception:
+                    pass
+                self._halt.wait(self.NVML_PERIOD_S)
+
+        self.thread = threading.Thread(target=poll, daemon=True)
+        self.thread.start()
+        self.source = f"nvml every {self.NVML_PERIOD_S * 1e3:.0f} ms"
+        return True
+
     def start(self):
+        if self.use_nvml is not False and self._start_nvml():
+            time.sleep(0.1)
+            return
         fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
         os.close(fd)
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu=timestamp,{self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.SMI_PERIOD_MS)],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            self.source = f"nvidia-smi -lms {self.SMI_PERIOD_MS}"
         except OSError:
             self.proc = None
         time.sleep(0.5)
@@ -93,29 +171,41 @@ class ClockSampler:
         self.t_stop = time.time()
 
     def stop(self):
-        if self.proc is None:
+        if self.thread is not None:
+            time.sleep(0.05)
+            self._halt.set()
+            self.thread.join(timeout=5)
+            lines = list(self.lines)
+        elif self.proc is not None:
+            time.sleep(0.3)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            with open(self.path) as f:
+                lines = f.readlines()
+            os.unlink(self.path)
+        else:
             return None
-        time.sleep(0.3)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        with open(self.path) as f:
-            lines = f.readlines()
-        os.unlink(self.path)
-        return summarise_clocks(lines, self.t_start, self.t_stop)
+        slack = 2 * (self.NVML_PERIOD_S if self.thread is not None
+                     else self.SMI_PERIOD_MS / 1e3)
+        out = summarise_clocks(lines, self.t_start, self.t_stop, slack)
+        if out is not None:
+            out["source"] = self.source
+        return out
 
 
 CLOCK_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
 
-def summarise_clocks(lines, t_start, t_stop):
+def summarise_clocks(lines, t_start, t_stop, slack=0.1):
     """Summary of nvidia-smi CSV lines (timestamp, then ClockSampler.FIELDS,
     no header, no units): the median SM clock, the maximum SM clock and the
     throttle reasons that were active, over the samples taken between
-    t_start and t_stop (100 ms of slack either side), or over every sample
-    when none fell inside; None without a usable sample."""
+    t_start and t_stop (`slack` seconds either side, about one sampling
+    period), or over every sample when none fell inside; None without a
+    usable sample."""
     import datetime
 
     rows = [[p.strip() for p in line.split(",")] for line in lines]
@@ -128,7 +218,7 @@ def summarise_clocks(lines, t_start, t_stop):
             return None
 
     inside = [p for p in rows if t_start and t_stop and ts(p) is not None
-              and t_start - 0.1 <= ts(p) <= t_stop + 0.1]
+              and t_start - slack <= ts(p) <= t_stop + slack]
     use = inside or rows
     sm, reasons, sm_max = [], set(), None
     for p in use:
@@ -250,13 +340,19 @@ def oracle_pass(wl, ctx, variant="fused", codec="int8", ef=False, max_norm=1.0):
     return time.perf_counter() - t0
 
 
-def oracle_sample_rate(wl, target_s=12.0, sample_elems=1 << 24, threads=None, opts=None):
+def oracle_sample_rate(wl, target_s=12.0, sample_elems=1 << 24, threads=None, opts=None,
+                       ctx=None):
     """Time the oracle of the measured step (opts, from oracle_step_opts) on
     the first sample_elems params of the workload, repeated until target_s of
-    CPU time; returns params/s, cores, text."""
+    CPU time; returns params/s, cores, text.  ctx: inputs already prepared
+    (oracle_prepare), timed with `threads` threads when given."""
     opts = opts or {"variant": "fused"}
     n = min(sample_elems, wl.N)
-    ctx = oracle_prepare(wl, n, threads)
+    if ctx is None:
+        ctx = oracle_prepare(wl, n, threads)
+    elif threads:
+        ctx = dict(ctx, threads=threads)
+    n = ctx["n"]
     reps, elapsed = 0, 0.0
     while elapsed < target_s or reps == 0:
         elapsed += oracle_pass(wl, ctx, **opts)
@@ -267,13 +363,20 @@ def oracle_sample_rate(wl, target_s=12.0, sample_elems=1 << 24, threads=None, op
     return n * reps / elapsed, cores, desc
 
 
-def _tree_levels(N: int):
-    """Partial counts of the clipped step's norm tree (256 leaves a warp in
-    the streaming pass, then 2048 partials a block)."""
-    lv = [max(1, -(-N // 256))]
-    while lv[-1] > 1:
-        lv.append(-(-lv[-1] // 2048))
-    return lv
+def oracle_baseline(wl, opts, target_s=8.0, sample_elems=1 << 24):
+    """The cpu_baseline object: the oracle of the measured step on all host
+    cores and on one core, over the same prepared sample."""
+    n = min(sample_elems, wl.N)
+    ctx = oracle_prepare(wl, n)
+    rate, cores, desc = oracle_sample_rate(wl, target_s, opts=opts, ctx=ctx)
+    cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+    if cores > 1:
+        r1, c1, d1 = oracle_sample_rate(wl, target_s, threads=1, opts=opts, ctx=ctx)
+    else:
+        r1, c1, d1 = rate, cores, desc
+    cpu.update({"value_1core": r1, "cores_1core": c1, "sample_1core": d1,
+                "host_cores": os.cpu_count()})
+    return cpu
 
 
 def max_over_ranks(x: float, device=None) -> float:
@@ -457,7 +560,7 @@ def run_ours(args, rank, world, local_rank):
     roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved_gbs / peak, 4), "traffic": traffic,
                 "peak_source": peak_src,
-                "kernel": ("clipped step (k_rs_norm, k_tree, k_clip_coef, k_adamw_ag)" if clipped
+                "kernel": ("clipped step (k_rs_norm, k_norm_tree, k_adamw_ag)" if clipped
                            else "k_fused (ZeRO-3 output)" if zero3
                            else f"k_comp ({args.codec}{', error feedback' if args.ef else ''})"
                            if compressed
@@ -514,7 +617,7 @@ def run_ours(args, rank, world, local_rank):
         del host_g, out
 
     if clipped:
-        launches_per_step = 2 + len(_tree_levels(N))   # rs_norm, tree levels, coef, update
+        launches_per_step = 3          # rs_norm, the rest of the norm tree + coefficient, update
     else:
         launches_per_step = 3 if variant == z.ZERO_VARIANT_STAGED else 1
     del ds
@@ -522,8 +625,7 @@ def run_ours(args, rank, world, local_rank):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, cores, desc = oracle_sample_rate(wl, opts=oracle_step_opts(args))
-        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        cpu = oracle_baseline(wl, oracle_step_opts(args))
 
     if rank != 0:
         return None
@@ -582,11 +684,12 @@ def run_table(args):
     sampler.start()
     sampler.mark_start()
 
-    def timed(ds, variant, reps):
+    def timed(ds, variant, reps, cold=True):
         ts = []
         t = ds.wl.step
         for k in range(3 + reps):
-            flush.fill_(k & 0xFF)                      # evict L2 (256 MB > 129 MB)
+            if cold:
+                flush.fill_(k & 0xFF)                  # evict L2 (256 MB > 129 MB)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             ds.step(t, variant=variant)
@@ -605,16 +708,23 @@ def run_table(args):
         ds.fill_state_device()
         ds.fill_grads_device(wl.step)
         torch.cuda.synchronize()
+        resident = bpp(wl, 1) * wl.N < 129e6
         for variant in variants:
-            ms = timed(ds, variant, reps)
-            gbs = bpp(wl, variant) * wl.N / (ms / 1e3) / 1e9
-            row = {"workload": label, "R": wl.R, "M": wl.M, "N": wl.N,
-                   "variant": "fused" if variant == 0 else "staged", "ms": round(ms, 4),
-                   "params_per_s": wl.N / (ms / 1e3), "bytes_per_param": bpp(wl, variant),
-                   "GB_s": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
-                   "l2_resident": bpp(wl, variant) * wl.N < 129e6}
-            rows.append(row)
-            print(json.dumps(row), flush=True)
+            # a workload that fits in L2 is timed twice: after a flush (cold
+            # L2, the flush's dirty lines written back during the launch) and
+            # back to back with its inputs resident (warm L2)
+            for cold in ((True, False) if resident else (True,)):
+                ms = timed(ds, variant, reps, cold)
+                gbs = bpp(wl, variant) * wl.N / (ms / 1e3) / 1e9
+                row = {"workload": label, "R": wl.R, "M": wl.M, "N": wl.N,
+                       "variant": "fused" if variant == 0 else "staged", "ms": round(ms, 4),
+                       "params_per_s": wl.N / (ms / 1e3), "bytes_per_param": bpp(wl, variant),
+                       "GB_s": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
+                       "l2": ("cold (256 MB flush before each launch)" if cold
+                              else "warm (inputs resident, launches back to back)")
+                       if resident else "inputs far larger than L2; flushed before each launch"}
+                rows.append(row)
+                print(json.dumps(row), flush=True)
         del ds
         torch.cuda.empty_cache()
 
@@ -655,14 +765,27 @@ def run_table(args):
             full = torch.empty(wl.N, dtype=torch.bfloat16, device="cuda")
             for label, cuts, graph in (("unit = tensor (146 units)", offs, False),
                                        ("unit = tensor (146 units), one CUDA graph", offs, True),
+                                       ("unit = tensor (146 units), one zero3_gather_units "
+                                        "launch", offs, "table"),
                                        ("unit = layer (18 units)", layers, False),
                                        ("unit = layer (18 units), one CUDA graph", layers, True),
+                                       ("unit = layer (18 units), one zero3_gather_units "
+                                        "launch", layers, "table"),
                                        ("unit = whole model (1 unit)", [0, wl.N], False)):
                 def gather_all():
                     for lo, hi in zip(cuts[:-1], cuts[1:]):
                         z.zero3_gather(ds.plan, shards, lo, hi, [full[:hi - lo]])
                 run = gather_all
-                if graph:
+                if graph == "table":
+                    # every unit into its own slice of the model buffer (the
+                    # table's destinations may not overlap); the table is
+                    # built once and passed as is on every call
+                    pairs = list(zip(cuts[:-1], cuts[1:]))
+                    table = z.gather_unit_table([(lo, hi, full[lo:hi]) for lo, hi in pairs])
+
+                    def run():
+                        z.zero3_gather_units(ds.plan, shards, table, len(pairs))
+                elif graph:
                     # the same launches captured once and replayed: no host
                     # work between them (the eager rows above have already
                     # run every kernel once)
@@ -683,7 +806,7 @@ def run_table(args):
                         ts.append(e0.elapsed_time(e1))
                 ms = float(np.median(ts))
                 row = {"workload": name, "variant": "zero3_gather", "unit": label,
-                       "launches": len(cuts) - 1, "ms": round(ms, 4),
+                       "launches": 1 if graph == "table" else len(cuts) - 1, "ms": round(ms, 4),
                        "GB_s": round(4 * wl.N / (ms / 1e3) / 1e9, 1),
                        "frac_of_measured_peak": round(4 * wl.N / (ms / 1e3) / 1e9 / peak, 4)}
                 rows.append(row)
@@ -871,7 +994,7 @@ def run_table(args):
     ms = float(np.median(ts))
     b = 2 * wl.R * wl.M + 4 + 4 + 24 + 2 * wl.R
     row = {"workload": "llama-3.2-1b", "R": wl.R, "M": wl.M, "N": wl.N, "variant": "clipped",
-           "launches": 2 + len(_tree_levels(wl.N)), "ms": round(ms, 4),
+           "launches": 3, "ms": round(ms, 4),
            "params_per_s": wl.N / (ms / 1e3), "bytes_per_param": b,
            "GB_s": round(b * wl.N / (ms / 1e3) / 1e9, 1),
            "frac_of_measured_peak": round(b * wl.N / (ms / 1e3) / 1e9 / peak, 4)}

@@ -83,8 +83,8 @@ typedef enum {
     ZERO_ERR_SIZE = -4,            /* sizes beyond the limits / scratch too small */
     ZERO_ERR_OVERLAP = -5,         /* an output overlaps another buffer        */
     ZERO_ERR_CUDA = -6,            /* a CUDA launch or copy failed             */
-    ZERO_ERR_DEVICE_TIMEOUT = -7,  /* reserved for device-side bounded waits   */
-    ZERO_ERR_NONFINITE = -8,       /* reported through the device status word  */
+    ZERO_ERR_DEVICE_TIMEOUT = -7,  /* a bounded device wait ran out (zero_get_device_status) */
+    ZERO_ERR_NONFINITE = -8,       /* a non-finite gradient or norm (zero_get_device_status) */
     ZERO_ERR_IO = -9,              /* a checkpoint file could not be written/read */
     ZERO_ERR_CORRUPT = -10         /* a checkpoint header or checksum is wrong  */
 } zero_status;
@@ -93,6 +93,11 @@ typedef enum {
 #define ZERO_DEV_NONFINITE 1       /* an averaged gradient (or the norm) was Inf or NaN */
 #define ZERO_DEV_TIMEOUT 2         /* a bounded device wait ran out (TMA variant) */
 #define ZERO_DEV_SKIPPED 4         /* zero_step_clipped skipped the update      */
+/* Set with ZERO_DEV_TIMEOUT when, after a wait ran out, the block's own
+ * bounded wait for the copies it had already issued ran out as well: the
+ * block left with copies in flight into its shared memory, so treat the CUDA
+ * context as suspect (finish or reset it) rather than continue training. */
+#define ZERO_DEV_DRAIN_FAILED 8
 
 /* Flags for zero_step / zero_rs_avg. */
 #define ZERO_FLAG_CHECK_FINITE 1   /* set ZERO_DEV_NONFINITE when g is non-finite */
@@ -169,7 +174,8 @@ int32_t zero_plan_owner(const zero_plan_t* plan, int64_t i);
  * One optimizer step (see the top of this file for the arithmetic).
  *   rank_grads  host array of R*M device pointers, entry r*M + j = rank r,
  *               micro-batch j; each N bf16, read only (entries may alias
- *               one another).
+ *               one another), except in the staged ZeRO-2 mode without
+ *               scratch described under `scratch`.
  *   master, m, v  device, plan->padded floats each, updated in place.
  *   rank_params host array of R device pointers, each N bf16, written.
  *   hp          AdamW hyper-parameters (0 <= beta1, beta2 < 1; lr, eps,
@@ -184,6 +190,13 @@ int32_t zero_plan_owner(const zero_plan_t* plan, int64_t i);
  *   scratch     device scratch of scratch_bytes bytes; the staged variant
  *               needs plan->scratch_bytes_staged (fp32 reduced gradient of
  *               every shard); ignored (may be NULL) for the fused variant.
+ *               ZeRO-2 gives up the gradients once they are reduced (CS25 V6
+ *               Lecture 4 notes, "ZeRO-2"): with plan->stage == 2 and
+ *               R*M >= 2 the staged variant accepts scratch = NULL and then
+ *               keeps the reduced gradient in rank_grads[0] and
+ *               rank_grads[1] (the low and high 16 bits of each element's
+ *               fp32 value), whose contents are unspecified afterwards; those
+ *               two buffers are then outputs and may alias no other buffer.
  *   flags       0, ZERO_FLAG_CHECK_FINITE, and for the TMA variant
  *               ZERO_FLAG_DEBUG_EXPIRE_WAITS (test only).
  *   dev_status  optional device int32 the kernels OR ZERO_DEV_* bits into.
@@ -196,6 +209,25 @@ zero_status zero_step(const zero_plan_t* plan, const uint16_t* const* rank_grads
                       const zero_adamw_hparams* hp, int64_t step, int32_t variant,
                       void* scratch, int64_t scratch_bytes, int32_t flags,
                       int32_t* dev_status, void* stream);
+
+/*
+ * Read the device status word after the steps that wrote it (failure
+ * detection: find and report a failed step instead of hanging or going on
+ * silently; LLM infra 06, section 15.4).
+ *   dev_status  the caller's device int32 passed to the steps (4-byte
+ *               aligned).  It is read, not cleared: zero it before the next
+ *               steps that should report afresh.
+ *   stream      the stream the steps ran on: the call enqueues the read of
+ *               the word on it and waits for the stream to finish.
+ *   out         optional host int32: receives the word (ZERO_DEV_* bits).
+ * Returns ZERO_ERR_DEVICE_TIMEOUT when ZERO_DEV_TIMEOUT is set (with or
+ * without ZERO_DEV_DRAIN_FAILED), else ZERO_ERR_NONFINITE when
+ * ZERO_DEV_NONFINITE is set (zero_step_clipped's ZERO_DEV_SKIPPED comes with
+ * it), else ZERO_OK; ZERO_ERR_NULL for a NULL dev_status, ZERO_ERR_ALIGN for
+ * a misaligned one, ZERO_ERR_CUDA when the copy or the wait fails (*out is
+ * then not written).
+ */
+zero_status zero_get_device_status(const int32_t* dev_status, void* stream, int32_t* out);
 
 /*
  * Staged step 1, reduce-scatter + average: for each rank r and each element
@@ -358,6 +390,31 @@ zero_status zero3_gather(const zero_plan_t* plan, const uint16_t* param_shards, 
                          int64_t hi, uint16_t* const* outs, int32_t n_out, void* stream);
 
 /*
+ * ZeRO-3 all-gather of a table of units in one launch: for every entry k,
+ * units[k].out[i - lo] = param_shards[i] for i in [units[k].lo, units[k].hi),
+ * exactly as zero3_gather of that unit with one destination.  Built for the
+ * many small units of a per-tensor schedule, whose separate launches would
+ * leave the GPU idle between them (CS25 V6 Lecture 4 notes, "ZeRO-3 / FSDP":
+ * each unit is materialised just before use; LLM infra 06, section 3.1).
+ *   units    host array of n_units entries, read during the call only (the
+ *            table travels with the launch, so it may be reused at once).
+ *            Each: 0 <= lo <= hi <= N, any lo; out device, hi - lo bf16,
+ *            16-byte aligned (may be NULL when lo == hi).  Outputs must not
+ *            overlap each other or the shards (ZERO_ERR_OVERLAP); the units'
+ *            source ranges may overlap.  To write one unit into several
+ *            buffers, list it once per buffer.
+ *   n_units  0 .. ZERO_MAX_GATHER_UNITS (0 is a no-op).
+ * Traffic: 2 + 2 bytes per element of every unit.
+ */
+#define ZERO_MAX_GATHER_UNITS 1024
+typedef struct {
+    int64_t lo, hi;
+    uint16_t* out;
+} zero_gather_unit;
+zero_status zero3_gather_units(const zero_plan_t* plan, const uint16_t* param_shards,
+                               const zero_gather_unit* units, int32_t n_units, void* stream);
+
+/*
  * ZeRO-3 gradient reduce-scatter of one unit, right after that unit's
  * backward (CS25 V6 Lecture 4 notes, "ZeRO-3 / FSDP": the backward
  * materialises each unit's parameters again and reduce-scatters its
@@ -428,8 +485,12 @@ zero_status zero_step_host(const zero_plan_t* plan, const uint16_t* const* host_
  *   - The plan must have plan->padded <= ZERO_NOALLOC_MAX_ELEMS, else
  *     ZERO_ERR_SIZE is returned and nothing is launched.
  *   - The first call on a device looks up the array's device address
- *     (once per device, with that device current); make that first call
- *     before any stream capture.  A failed lookup returns ZERO_ERR_CUDA.
+ *     (once per device, with that device current, and again if the
+ *     device's context has been replaced since, e.g. by cudaDeviceReset);
+ *     make that first call before any stream capture.  A failed lookup
+ *     returns ZERO_ERR_CUDA.
+ *   - `stream` must belong to the current device (the array's address is
+ *     that device's), else ZERO_ERR_INVALID_ARG.
  *   - Calls no cudaMalloc, cudaFree or other allocating routine.
  *   - Every call on a device shares the one array and it keeps the last
  *     call's contents; nothing needs clearing, because the reduce-scatter

@@ -173,11 +173,32 @@ def test_step_overlap(plan):
 def test_step_staged_scratch(plan):
     g, Wp, mp, vp, P, scr, st = fake_bufs(plan)
     need = plan.scratch_bytes_staged
-    assert call_step(plan, g, Wp, mp, vp, P, variant=1, scratch=None) == B.ZERO_ERR_NULL
     assert call_step(plan, g, Wp, mp, vp, P, variant=1, scratch=scr,
                      sbytes=need - 4) == B.ZERO_ERR_SIZE
     assert call_step(plan, g, Wp, mp, vp, P, variant=1, scratch=Wp,
                      sbytes=need) == B.ZERO_ERR_OVERLAP
+    # ZeRO-1 keeps its gradients: the staged step needs scratch
+    z1 = z.Plan([100_000], 4, 2, 1)
+    assert call_step(z1, g, Wp, mp, vp, P, variant=1, scratch=None) == B.ZERO_ERR_NULL
+    # one gradient buffer cannot hold the fp32 result: scratch needed
+    one = z.Plan([100_000], 1, 1, 2)
+    g1, W1, m1, v1, P1, _, _ = fake_bufs(one)
+    assert call_step(one, g1, W1, m1, v1, P1, variant=1, scratch=None) == B.ZERO_ERR_NULL
+
+
+def test_staged_zero2_without_scratch_writes_two_gradient_buffers(plan):
+    """ZeRO-2 without scratch: gradient buffers 0 and 1 become outputs (the
+    reduced gradient's low and high halves), so they may alias nothing; the
+    other gradient buffers stay read-only inputs that may alias each other."""
+    g, Wp, mp, vp, P, scr, st = fake_bufs(plan)
+    assert call_step(plan, [g[0], g[0]] + g[2:], Wp, mp, vp, P, variant=1) == B.ZERO_ERR_OVERLAP
+    assert call_step(plan, g[:2] + [g[1]] + g[3:], Wp, mp, vp, P,
+                     variant=1) == B.ZERO_ERR_OVERLAP
+    assert call_step(plan, g[:3] + [g[0] + 64] + g[4:], Wp, mp, vp, P,
+                     variant=1) == B.ZERO_ERR_OVERLAP
+    # inputs 2.. may alias one another; the call then gets past validation and
+    # fails at the launch on a machine without a GPU
+    assert call_step(plan, g[:2] + [g[2]] * 6, Wp, mp, vp, P, variant=1) == B.ZERO_ERR_CUDA
 
 
 def test_staged_entry_errors(plan):
@@ -224,13 +245,19 @@ def test_binding_rejects_host_tensors_for_device_arguments():
 
 def test_clip_scratch_bytes_layout():
     # fp32 gradient stash (4 * padded) + one 256-byte-rounded segment per tree
-    # level (ceil(N/256) warp partials, then ceil(./2048) ... down to 1) + control
-    p = z.Plan([65536], 4, 2, 1)
+    # level (ceil(N/256) warp partials, then ceil(./2048) ... down to 1) +
+    # control + one 4-byte arrival counter per group above the second level
+    def r256(x):
+        return -(-x // 256) * 256
+    p = z.Plan([65536], 4, 2, 1)                     # 256 -> 1 partials: no counters
     assert z.zero_clip_scratch_bytes(p) == 4 * 65536 + 1024 + 256 + 256
     p = z.Plan([1_235_814_400], 8, 1, 2)             # 4,827,400 -> 2,358 -> 2 -> 1 partials
     levels = [4_827_400, 2_358, 2, 1]
-    want = 4 * p.padded + sum(-(-4 * n // 256) * 256 for n in levels) + 256
+    want = (4 * p.padded + sum(r256(4 * n) for n in levels) + 256
+            + r256(4 * sum(levels[2:])))
     assert z.zero_clip_scratch_bytes(p) == want
+    p = z.Plan([200], 2, 1, 2)                        # one partial: no counters
+    assert z.zero_clip_scratch_bytes(p) == 4 * p.padded + 256 + 256
 
 
 def test_clipped_step_argument_errors():
@@ -398,6 +425,59 @@ def test_no_alloc_step_refuses_plans_beyond_its_array():
                                          ctypes.addressof(pa), ctypes.byref(hp), 1, 0, None,
                                          None)
         assert got == want, (pl.padded, got)
+
+
+def test_gather_units_argument_errors():
+    """zero3_gather_units validates the whole table before any launch: unit
+    bounds, NULL and misaligned destinations, overlapping destinations (and a
+    destination over the shards), the table size; a table of empty units is
+    a no-op that needs no shard pointer."""
+    import ctypes
+    L = B.lib()
+    pl = z.Plan([10_000], 4, 1, 2)
+    U = B.zero_gather_unit
+    SH = 0x100000                                   # fake, 16-byte aligned; never dereferenced
+
+    def call(units, n=None, shards=SH):
+        arr = (U * max(1, len(units)))(*[U(*u) for u in units])
+        return L.zero3_gather_units(pl.ptr, shards, arr, len(units) if n is None else n, None)
+
+    far = 0x10000000
+    assert call([], 0) == B.ZERO_OK
+    assert call([(0, 10, far)], -1) == B.ZERO_ERR_INVALID_ARG
+    assert call([(0, 10, far)], B.ZERO_MAX_GATHER_UNITS + 1) == B.ZERO_ERR_INVALID_ARG
+    assert L.zero3_gather_units(pl.ptr, SH, None, 1, None) == B.ZERO_ERR_NULL
+    assert call([(5, 4, far)]) == B.ZERO_ERR_INVALID_ARG             # hi < lo
+    assert call([(-1, 4, far)]) == B.ZERO_ERR_INVALID_ARG
+    assert call([(0, 10_001, far)]) == B.ZERO_ERR_INVALID_ARG        # past N
+    assert call([(0, 10, None)]) == B.ZERO_ERR_NULL
+    assert call([(0, 10, far + 2)]) == B.ZERO_ERR_ALIGN
+    assert call([(0, 10, far), (3, 13, far + 16)]) == B.ZERO_ERR_OVERLAP
+    assert call([(0, 10, SH + 64)]) == B.ZERO_ERR_OVERLAP            # writes over the shards
+    assert call([(0, 10, far)], shards=None) == B.ZERO_ERR_NULL
+    assert call([(0, 10, far)], shards=SH + 8) == B.ZERO_ERR_ALIGN
+    assert call([(7, 7, None), (10_000, 10_000, None)], shards=None) == B.ZERO_OK
+    with pytest.raises(ValueError):
+        z.gather_unit_table([(0, 10, torch.zeros(10, dtype=torch.bfloat16))])  # host tensor
+
+
+def test_device_status_argument_errors():
+    """zero_get_device_status checks its word's pointer before any CUDA call:
+    NULL -> ZERO_ERR_NULL, not 4-byte aligned -> ZERO_ERR_ALIGN, and the host
+    output is left untouched."""
+    import ctypes
+    L = B.lib()
+    out = ctypes.c_int32(-12345)
+    assert L.zero_get_device_status(None, None, ctypes.byref(out)) == B.ZERO_ERR_NULL
+    for bad in (0x1001, 0x1002, 0x1003):
+        assert L.zero_get_device_status(bad, None, ctypes.byref(out)) == B.ZERO_ERR_ALIGN
+    assert out.value == -12345
+    with pytest.raises(B.ZeroError) as e:
+        z.zero_get_device_status(0x1002, stream=0)
+    assert e.value.code == B.ZERO_ERR_ALIGN
+    # the status codes the call maps the device bits to have names
+    for code in (B.ZERO_ERR_DEVICE_TIMEOUT, B.ZERO_ERR_NONFINITE):
+        assert z.zero_status_string(code) != "unknown status"
 
 
 def test_empty_plan_is_a_no_op_for_every_step_entry_point():

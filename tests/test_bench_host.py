@@ -70,7 +70,7 @@ def test_sampler_runs_a_fake_nvidia_smi_and_summarises_its_output(tmp_path, monk
         "    time.sleep(0.05)\n")
     fake.chmod(0o755)
     monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
-    s = bench.ClockSampler("0")
+    s = bench.ClockSampler("0", use_nvml=False)
     s.start()
     s.mark_start()
     time.sleep(0.4)
@@ -79,8 +79,41 @@ def test_sampler_runs_a_fake_nvidia_smi_and_summarises_its_output(tmp_path, monk
     assert got is not None and got["in_timed_region"]
     assert got["sm_mhz"] == 1965.0 and got["sm_max_mhz"] == 2070.0
     assert got["reasons"] == ["sw_power_cap"] and got["samples"] >= 3
+    assert got["source"] == "nvidia-smi -lms 20"
     assert not os.path.exists(s.path)
 
+
+def test_sampler_polls_nvml_when_the_library_loads(tmp_path, monkeypatch):
+    """The NVML path of the sampler against a stand-in libnvidia-ml built
+    here: a 0.2 s region gets dozens of samples at the 5 ms period, and the
+    event-reason bits map to the same names as nvidia-smi's columns."""
+    import shutil
+    import subprocess
+    import time
+    if not shutil.which("gcc"):
+        pytest.skip("gcc needed for the stand-in library")
+    src = tmp_path / "fake_nvml.c"
+    src.write_text(
+        "int nvmlInit_v2(void) { return 0; }\n"
+        "int nvmlDeviceGetHandleByUUID(const char* u, void** h) { *h = (void*)1; return 0; }\n"
+        "int nvmlDeviceGetMaxClockInfo(void* h, int t, unsigned* v) { *v = 2070; return 0; }\n"
+        "int nvmlDeviceGetClockInfo(void* h, int t, unsigned* v) { *v = 1995; return 0; }\n"
+        "int nvmlDeviceGetPowerUsage(void* h, unsigned* v) { *v = 812500; return 0; }\n"
+        "int nvmlDeviceGetCurrentClocksEventReasons(void* h, unsigned long long* r)\n"
+        "{ *r = 0x4 | 0x40; return 0; }\n")
+    lib = tmp_path / "libfakenvml.so"
+    subprocess.run(["gcc", "-shared", "-fPIC", "-o", str(lib), str(src)], check=True)
+    monkeypatch.setattr(bench._NvmlClocks, "LIB", str(lib))
+    s = bench.ClockSampler("GPU-fake")
+    s.start()
+    s.mark_start()
+    time.sleep(0.2)
+    s.mark_stop()
+    got = s.stop()
+    assert got["source"] == "nvml every 5 ms" and got["in_timed_region"]
+    assert got["samples"] >= 10
+    assert got["sm_mhz"] == 1995.0 and got["sm_max_mhz"] == 2070.0
+    assert got["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
 
 
 @pytest.mark.parametrize("variant,extra", [
@@ -118,3 +151,20 @@ def test_table_oracle_rows_of_the_step_variants():
     for r in rows:
         assert r["oracle"] == bench.ORACLE_FN[r["variant"]] and r["params_per_s"] > 0
         assert r["sample_params"] == 1 << 14 and r["oracle_threads"] == 1
+
+
+def test_cpu_baseline_carries_the_all_core_and_one_core_oracle_rates():
+    """The bench line's cpu_baseline times the oracle of the measured step on
+    every host core and on one core, over the same prepared sample."""
+    from zgen import workloads as W
+    wl = W.uneven()
+    cpu = bench.oracle_baseline(wl, {"variant": "fused"}, target_s=0.05, sample_elems=1 << 16)
+    assert cpu["kind"] == "oracle" and cpu["unit"] == "params/s"
+    assert cpu["value"] > 0 and cpu["value_1core"] > 0
+    assert cpu["cores"] == (os.cpu_count() or 1) and cpu["cores_1core"] == 1
+    assert cpu["sample"].startswith("oracle_dp_step_mt over the first 65,536 params")
+    assert "1 thread(s)" in cpu["sample_1core"]
+    # a single-core oracle (the clipped step's) is reported once
+    one = bench.oracle_baseline(wl, {"variant": "clipped", "max_norm": 1.0}, target_s=0.05,
+                                sample_elems=1 << 14)
+    assert one["cores"] == 1 and one["value_1core"] == one["value"]

@@ -65,7 +65,12 @@ def test_async_save_snapshots_the_state_before_the_next_step(tmp_path):
     assert step == wl.step
     assert np.array_equal(params, before[3][0])
     assert np.array_equal(Wh[:N].view(np.uint32), before[0].view(np.uint32))
+    assert np.array_equal(mh[:N].view(np.uint32), before[1].view(np.uint32))
     assert np.array_equal(vh[:N].view(np.uint32), before[2].view(np.uint32))
+    # the step after the save did change all three, so the snapshot is not the later state
+    after = ds.result()
+    for k in range(3):
+        assert not np.array_equal(after[k].view(np.uint32), before[k].view(np.uint32))
 
 
 @pytest.mark.parametrize("R_new", [7, 1, 16])

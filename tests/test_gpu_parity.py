@@ -202,6 +202,81 @@ def test_guard_bands_and_padding_untouched():
         assert torch.all(t.view(torch.int32)[N:] == canary), "state pad touched"
 
 
+@pytest.mark.parametrize("name,target", [("uneven", 250_003), ("llama-3.2-1b", 400_000),
+                                         ("tiny", 65_536)])
+def test_staged_zero2_without_scratch_matches_oracle(name, target):
+    """ZeRO-2 gives up the gradients once reduced: the staged step without
+    scratch keeps the fp32 reduced gradient in gradient buffers 0 and 1 and
+    must give the oracle's bits, over two steps with fresh gradients."""
+    wl = dataclasses.replace(W.ALL[name]().scaled(target), stage=2)
+    steps = [wl.first_step(), wl.first_step() + 1]
+    _, W0, m0, v0 = H.host_inputs(wl, steps[0])
+    idx = np.arange(wl.N, dtype=np.int64)
+    Gs = {t: W.host_grads_at(wl, t, idx) for t in steps}
+    want = H.oracle_run(wl, Gs, W0, m0, v0, steps)
+    ds = H.DeviceState(wl, staged_scratch=False)
+    ds.upload_state(W0, m0, v0)
+    for t in steps:
+        ds.upload_grads(Gs[t])
+        z.zero_step(ds.plan, ds.grads, ds.W, ds.m, ds.v, ds.params, ds.hp, t,
+                    variant=z.ZERO_VARIANT_STAGED, scratch=None, flags=z.ZERO_FLAG_CHECK_FINITE,
+                    dev_status=ds.status)
+    torch.cuda.synchronize()
+    _assert_parity(H.compare(ds.result(), want))
+    assert int(ds.status.item()) == 0
+
+
+def test_staged_zero2_without_scratch_touches_only_two_gradient_buffers():
+    """Guard bands around every buffer: the mode writes gradient buffers 0
+    and 1 and nothing else beside the state and the replicas; the other
+    gradient buffers, the guards and the state pad keep their bits."""
+    wl = dataclasses.replace(W.uneven().scaled(30_011), stage=2)
+    plan = z.Plan(wl.numels, wl.R, wl.M, wl.stage, wl.align)
+    N, padded, RM = plan.N, plan.padded, wl.R * wl.M
+    GB = 64
+    dev = torch.device("cuda")
+    canary = 0x7FA5A5A5
+    G, W0, m0, v0 = H.host_inputs(wl, 1)
+    gbufs = [torch.full((N + 4 * GB,), -1, dtype=torch.int16, device=dev) for _ in range(RM)]
+    grads = [b[2 * GB:2 * GB + N].view(torch.bfloat16) for b in gbufs]
+    pbufs = [torch.full((N + 4 * GB,), -1, dtype=torch.int16, device=dev) for _ in range(wl.R)]
+    params = [b[2 * GB:2 * GB + N].view(torch.bfloat16) for b in pbufs]
+    sbufs = [torch.full((padded + 2 * GB,), canary, dtype=torch.int32, device=dev)
+             for _ in range(3)]
+    Wt, mt, vt = [b[GB:GB + padded].view(torch.float32) for b in sbufs]
+    for t, g in zip(grads, G):
+        t.copy_(H.bf16_from_u16(g, dev))
+    for t, a in ((Wt, W0), (mt, m0), (vt, v0)):
+        t[:N].copy_(torch.from_numpy(a))
+    before = [b.clone() for b in gbufs]
+    hp = z.hparams(**wl.hparams())
+    z.zero_step(plan, grads, Wt, mt, vt, params, hp, 1, z.ZERO_VARIANT_STAGED, scratch=None)
+    torch.cuda.synchronize()
+    for q, (b, b0) in enumerate(zip(gbufs, before)):
+        assert torch.equal(b[:2 * GB], b0[:2 * GB]) and torch.equal(b[-2 * GB:], b0[-2 * GB:])
+        if q >= 2:
+            assert torch.equal(b, b0), f"gradient buffer {q} written"
+    for b in pbufs:
+        assert torch.all(b[:2 * GB] == -1) and torch.all(b[-2 * GB:] == -1)
+    for b in sbufs:
+        assert torch.all(b[:GB] == canary) and torch.all(b[-GB:] == canary)
+    for t in (Wt, mt, vt):
+        assert torch.all(t.view(torch.int32)[N:] == canary), "state pad touched"
+    # buffers 0 and 1 hold the reduced gradient's halves: reassembled, the oracle's average
+    import ctypes
+    ga = (ctypes.c_void_p * RM)(*[g.ctypes.data for g in G])
+    L = oracle.lib()
+    want_g = np.array([L.oracle_avg_grad(ctypes.addressof(ga), wl.R, wl.M, i,
+                                         float(RM)) for i in range(N)], np.float32)
+    lo = H.u16_from_bf16(grads[0]).astype(np.uint32)
+    hi = H.u16_from_bf16(grads[1]).astype(np.uint32)
+    assert np.array_equal(lo | (hi << 16), want_g.view(np.uint32))
+    want = H.oracle_run(wl, {1: G}, W0, m0, v0, [1])
+    got = (Wt[:N].cpu().numpy(), mt[:N].cpu().numpy(), vt[:N].cpu().numpy(),
+           [H.u16_from_bf16(p) for p in params])
+    _assert_parity(H.compare(got, want))
+
+
 def test_staged_entry_points_one_by_one():
     wl = W.uneven().scaled(40_000)
     G, W0, m0, v0 = H.host_inputs(wl, 1)

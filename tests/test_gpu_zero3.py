@@ -272,3 +272,92 @@ def test_full_size_unit_reduce_scatter_llama_layers():
     for a, b in ((W1, ds.W), (m1, ds.m), (v1, ds.v)):
         assert torch.equal(a[:N].view(torch.int32), b[:N].view(torch.int32))
     assert int(ds.status.item()) == 0
+
+
+# ------------------------------------------- the table of units, one launch --
+
+def _table_case(plan, shards_np, shards, units):
+    """Gather `units` ((lo, hi) pairs) in one zero3_gather_units call into
+    guarded buffers; every unit must equal oracle.zero3_gather bit for bit
+    and the guards must be untouched."""
+    G = 64
+    bufs, outs = [], []
+    for lo, hi in units:
+        b = torch.full((hi - lo + 2 * G + 8,), -7, dtype=torch.int16, device="cuda")
+        bufs.append(b)
+        outs.append(b[G:G + hi - lo].view(torch.bfloat16) if hi > lo else None)
+    z.zero3_gather_units(plan, shards, [(lo, hi, o) for (lo, hi), o in zip(units, outs)])
+    torch.cuda.synchronize()
+    for k, ((lo, hi), b, o) in enumerate(zip(units, bufs, outs)):
+        if hi > lo:
+            want, _ = oracle.zero3_gather(shards_np, plan.N, plan.R, plan.S, lo, hi, k % plan.R)
+            assert np.array_equal(H.u16_from_bf16(o), want), (k, lo, hi)
+        L = hi - lo
+        assert torch.all(b[:G] == -7) and torch.all(b[G + L:] == -7), (k, lo, hi)
+
+
+def _random_shards(plan, seed):
+    rng = np.random.default_rng(seed)
+    shards_np = rng.integers(0, 2 ** 16, plan.padded, dtype=np.uint16)
+    shards = torch.from_numpy(shards_np.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    return shards_np, shards
+
+
+def test_gather_units_every_alignment_length_and_empty_units():
+    N, R = 8 * 4096, 8                                     # no padding: the last shard ends the buffer
+    plan = z.Plan([N], R, 1, 2, 64)
+    shards_np, shards = _random_shards(plan, 3)
+    units = []
+    for lo in list(range(0, 24)) + [N - 40 + k for k in range(8)]:
+        for L in (0, 1, 7, 8, 9, 17, 33, 2047, 2048, 2049, 4103):
+            if lo + L <= N:
+                units.append((lo, lo + L))
+    units += [(N - 1000 - s, N) for s in range(8)] + [(s, N) for s in range(3)]
+    units += [(4096 * 3 - 5, 4096 * 5 + 3), (100, 100), (N, N)]
+    rng = np.random.default_rng(4)
+    rng.shuffle(units)
+    for k in range(0, len(units), 300):                   # several tables, any order
+        _table_case(plan, shards_np, shards, units[k:k + 300])
+
+
+def test_gather_units_full_table_and_overlapping_sources():
+    """A table of ZERO_MAX_GATHER_UNITS units over a padded, uneven layout,
+    many of them reading the same source ranges."""
+    plan = z.Plan([500_003], 7, 1, 2, 64)
+    assert plan.padded > plan.N
+    shards_np, shards = _random_shards(plan, 5)
+    rng = np.random.default_rng(6)
+    lo = rng.integers(0, plan.N, z.ZERO_MAX_GATHER_UNITS)
+    ln = rng.integers(0, 3000, z.ZERO_MAX_GATHER_UNITS)
+    units = [(int(a), int(min(plan.N, a + b))) for a, b in zip(lo, ln)]
+    units[:8] = [(0, 8), (0, 8), (plan.N - 3, plan.N), (plan.N - 3, plan.N), (5, 5),
+                 (plan.S - 1, plan.S + 1), (2 * plan.S - 9, 2 * plan.S + 9), (1, plan.N)]
+    _table_case(plan, shards_np, shards, units)
+
+
+def test_gather_units_equal_one_unit_gathers_on_the_1b_tables():
+    """The 146 per-tensor units and the 18 per-layer units of the
+    Llama-3.2-1B-shaped set, over shards filled by the seeded generator: one
+    table launch equals the oracle's gather of each unit, every element."""
+    import zgen
+    wl = W.llama32_1b()
+    plan = z.Plan(wl.numels, wl.R, wl.M, wl.stage, wl.align)
+    shards = torch.empty(plan.padded, dtype=torch.bfloat16, device="cuda")
+    stream_id = (1 << 50) + 17
+    zgen.dev_grad(shards.data_ptr(), wl.seed, stream_id, 0, plan.padded, 1e-2,
+                  cuda_stream=torch.cuda.current_stream().cuda_stream)
+    shards_np = zgen.host_grad(wl.seed, stream_id, 0, plan.padded, 1e-2)
+    offs = [int(x) for x in wl.offsets]
+    per_tensor = list(zip(offs[:-1], offs[1:]))
+    # per layer: the embedding, 16 decoder layers of 9 tensors, the final norm
+    layer_bounds = [offs[0], offs[1]] + [offs[1 + 9 * (k + 1)] for k in range(16)] + [offs[-1]]
+    per_layer = list(zip(layer_bounds[:-1], layer_bounds[1:]))
+    assert len(per_tensor) == 146 and len(per_layer) == 18
+    for table in (per_tensor, per_layer):
+        outs = [torch.empty(hi - lo, dtype=torch.bfloat16, device="cuda") for lo, hi in table]
+        z.zero3_gather_units(plan, shards, [(lo, hi, o) for (lo, hi), o in zip(table, outs)])
+        torch.cuda.synchronize()
+        for (lo, hi), o in zip(table, outs):
+            want, _ = oracle.zero3_gather(shards_np, plan.N, plan.R, plan.S, lo, hi, 0)
+            assert np.array_equal(H.u16_from_bf16(o), want), (lo, hi)
+        del outs

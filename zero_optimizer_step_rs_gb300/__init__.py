@@ -13,6 +13,8 @@ from .binding import (  # noqa: F401
     zero_step, zero_step_host, zero_step_staged_noalloc, zero_step_clipped,
     zero_clip_scratch_bytes, ZERO_DEV_SKIPPED, ZERO_FLAG_SKIP_NONFINITE, zero3_step, zero3_gather,
     zero_ckpt_write_host, zero_ckpt_read_host, zero_ckpt_save_async, zero_ckpt_job_wait,
-    zero_ckpt_load, zero_step_compressed, zero_check_replicas, zero_step_onebit, zero3_rs_unit, zero3_update, ZERO_COMP_FP16, ZERO_COMP_INT8, ZERO_COMP_SIGN, ZERO_DEV_NONFINITE, ZERO_FLAG_CHECK_FINITE, ZERO_VARIANT_FUSED,
+    zero_ckpt_load, zero_step_compressed, zero_check_replicas, zero_step_onebit, zero3_rs_unit, zero3_update, zero_get_device_status, zero3_gather_units,
+    gather_unit_table, ZERO_MAX_GATHER_UNITS,
+    ZERO_DEV_DRAIN_FAILED, ZERO_COMP_FP16, ZERO_COMP_INT8, ZERO_COMP_SIGN, ZERO_DEV_NONFINITE, ZERO_FLAG_CHECK_FINITE, ZERO_VARIANT_FUSED,
     ZERO_VARIANT_STAGED, ZERO_VARIANT_FUSED_TMA, ZERO_DEV_TIMEOUT, ZERO_FLAG_DEBUG_EXPIRE_WAITS,
 )

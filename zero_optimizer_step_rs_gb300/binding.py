@@ -34,6 +34,7 @@ ZERO_VARIANT_FUSED = 0
 ZERO_VARIANT_STAGED = 1
 ZERO_VARIANT_FUSED_TMA = 2
 ZERO_DEV_TIMEOUT = 2
+ZERO_DEV_DRAIN_FAILED = 8
 ZERO_FLAG_DEBUG_EXPIRE_WAITS = 1 << 30
 ZERO_COMP_FP16 = 1
 ZERO_COMP_INT8 = 2
@@ -41,6 +42,7 @@ ZERO_COMP_SIGN = 3
 ZERO_MAX_R = 64
 ZERO_MAX_RM = 256
 ZERO_NOALLOC_MAX_ELEMS = 4 * 1024 * 1024
+ZERO_MAX_GATHER_UNITS = 1024
 
 EXPORTED = ("zero_abi_version", "zero_status_string", "zero_plan_create", "zero_plan_destroy",
             "zero_plan_owner", "zero_step", "zero_rs_avg", "zero_adamw_shard", "zero_ag_cast",
@@ -48,7 +50,8 @@ EXPORTED = ("zero_abi_version", "zero_status_string", "zero_plan_create", "zero_
             "zero_clip_scratch_bytes", "zero3_step", "zero3_gather", "zero_ckpt_write_host",
             "zero_ckpt_read_host", "zero_ckpt_save_async", "zero_ckpt_job_wait",
             "zero_ckpt_load", "zero_step_compressed", "zero_check_replicas", "zero_step_onebit",
-            "zero3_rs_unit", "zero3_update")
+            "zero3_rs_unit", "zero3_update", "zero_get_device_status",
+            "zero3_gather_units")
 
 
 class ZeroError(RuntimeError):
@@ -65,6 +68,10 @@ class zero_plan_t(ctypes.Structure):
                 ("bytes_per_rank_dp", ctypes.c_int64), ("bytes_per_rank_z1", ctypes.c_int64),
                 ("bytes_per_rank_z2", ctypes.c_int64), ("bytes_per_rank_z3", ctypes.c_int64),
                 ("bytes_per_rank", ctypes.c_int64), ("scratch_bytes_staged", ctypes.c_int64)]
+
+
+class zero_gather_unit(ctypes.Structure):
+    _fields_ = [("lo", ctypes.c_int64), ("hi", ctypes.c_int64), ("out", ctypes.c_void_p)]
 
 
 class zero_adamw_hparams(ctypes.Structure):
@@ -148,6 +155,10 @@ def lib():
         L.zero3_update.argtypes = [P(zero_plan_t), vp, vp, vp, vp, vp, P(zero_adamw_hparams), i64,
                                    vp]
         L.zero3_update.restype = ctypes.c_int
+        L.zero_get_device_status.argtypes = [vp, vp, P(i32)]
+        L.zero_get_device_status.restype = ctypes.c_int
+        L.zero3_gather_units.argtypes = [P(zero_plan_t), vp, P(zero_gather_unit), i32, vp]
+        L.zero3_gather_units.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -292,6 +303,22 @@ def zero_step(plan: Plan, rank_grads, master, m, v, rank_params, hp: zero_adamw_
                            ctypes.addressof(pa), ctypes.byref(hp), step, variant,
                            _addr(scratch), sbytes, flags, _addr(dev_status), _stream(stream)),
            "zero_step")
+
+
+def zero_get_device_status(dev_status, stream=None, raise_on_error: bool = False):
+    """Wait for `stream`, read the caller's device status word (an int32
+    device tensor, or an address) and return (code, word): code is ZERO_OK,
+    ZERO_ERR_DEVICE_TIMEOUT or ZERO_ERR_NONFINITE as the word's bits say.
+    Argument and CUDA errors always raise; with raise_on_error the two
+    device conditions raise ZeroError as well."""
+    _check_tensor(dev_status, "i32", 1, "dev_status")
+    word = ctypes.c_int32(0)
+    code = int(lib().zero_get_device_status(_addr(dev_status), _stream(stream),
+                                            ctypes.byref(word)))
+    if code not in (ZERO_OK, ZERO_ERR_DEVICE_TIMEOUT, ZERO_ERR_NONFINITE) or (
+            raise_on_error and code != ZERO_OK):
+        raise ZeroError(code, "zero_get_device_status")
+    return code, int(word.value)
 
 
 def zero_rs_avg(plan: Plan, rank_grads, g_shards, flags: int = 0, dev_status=None,
@@ -441,6 +468,34 @@ def zero3_gather(plan: Plan, param_shards, lo: int, hi: int, outs, stream=None) 
     oa = _ptrs([_addr(o) for o in outs])
     _check(lib().zero3_gather(plan.ptr, _addr(param_shards), lo, hi, ctypes.addressof(oa),
                               len(outs), _stream(stream)), "zero3_gather")
+
+
+def gather_unit_table(units) -> ctypes.Array:
+    """A C array of zero_gather_unit from (lo, hi, out) triples (out a bf16
+    device tensor of hi - lo elements, an address, or None for an empty
+    unit); build it once and pass it to zero3_gather_units on every call."""
+    units = list(units)
+    arr = (zero_gather_unit * max(1, len(units)))()
+    for k, (lo, hi, out) in enumerate(units):
+        _check_tensor(out, "bf16", hi - lo, f"units[{k}].out")
+        arr[k] = zero_gather_unit(int(lo), int(hi), _addr(out))
+    return arr
+
+
+def zero3_gather_units(plan: Plan, param_shards, units, n_units: Optional[int] = None,
+                       stream=None) -> None:
+    """All-gather of a table of units in one launch.  units: a table from
+    gather_unit_table, or (lo, hi, out) triples (converted on every call)."""
+    c = plan.c
+    _check_tensor(param_shards, "bf16", c.padded, "param_shards")
+    if not isinstance(units, ctypes.Array):
+        units = list(units)
+        n_units = len(units)
+        units = gather_unit_table(units)
+    elif n_units is None:
+        n_units = len(units)
+    _check(lib().zero3_gather_units(plan.ptr, _addr(param_shards), units, n_units,
+                                    _stream(stream)), "zero3_gather_units")
 
 
 # -------------------------------------------------------------- checkpoints --

@@ -103,6 +103,87 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t st)
     }
 }
 
+// k_gather_units: the same copy over a table of units in one launch.  Each
+// unit is cut into chunks of 256 threads x 2 vectors of 8 elements; a block
+// takes chunks grid-stride over the whole table.  A chunk's unit is the
+// previous chunk's while it still fits, else found by a binary search of the
+// units' first chunks (block-uniform, so the table is read from the
+// constant bank by broadcast).  Both source loads of a thread are issued
+// before its stores.  A unit's shift lo mod 8 is uniform over its chunks;
+// the same funnel-shift realignment as k_gather picks each destination
+// vector out of two aligned source vectors.
+constexpr int kGatherVecs = 2;                     // 8-element vectors per thread per chunk
+constexpr int kGatherChunk = kThreads * 8 * kGatherVecs;
+
+struct GatherUnit {
+    int64_t lo, len;
+    uint16_t* out;
+};
+
+struct GatherUnitsArgs {
+    const uint16_t* src;
+    int64_t src_len;                                   // plan->padded
+    int32_t n_units;
+    uint32_t total_chunks;
+    uint32_t chunk0[ZERO_MAX_GATHER_UNITS + 1];        // first chunk of each unit, then the total
+    GatherUnit u[ZERO_MAX_GATHER_UNITS];
+};
+
+__device__ __forceinline__ uint4 realign_rt(int s, uint4 A, uint4 B)
+{
+    switch (s) {
+    case 0: return A;
+    case 1: return realign8<1>(A, B);
+    case 2: return realign8<2>(A, B);
+    case 3: return realign8<3>(A, B);
+    case 4: return realign8<4>(A, B);
+    case 5: return realign8<5>(A, B);
+    case 6: return realign8<6>(A, B);
+    default: return realign8<7>(A, B);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) k_gather_units(const __grid_constant__ GatherUnitsArgs a)
+{
+    int u = 0;
+    for (uint32_t c = blockIdx.x; c < a.total_chunks; c += gridDim.x) {
+        if (c >= a.chunk0[u + 1]) {                 // past the unit: last unit whose first chunk <= c
+            int ulo = u + 1, uhi = a.n_units - 1;
+            while (ulo < uhi) {
+                const int mid = (ulo + uhi + 1) >> 1;
+                if (a.chunk0[mid] <= c) ulo = mid;
+                else uhi = mid - 1;
+            }
+            u = ulo;
+        }
+        const GatherUnit& U = a.u[u];
+        const int s = (int)(U.lo & 7);
+        const int64_t base = (int64_t)(c - a.chunk0[u]) * kGatherChunk + (int64_t)threadIdx.x * 8;
+        uint4 A[kGatherVecs], B[kGatherVecs];
+        bool vec[kGatherVecs];
+#pragma unroll
+        for (int j = 0; j < kGatherVecs; ++j) {
+            const int64_t d = base + (int64_t)j * kThreads * 8;
+            const int64_t sb = U.lo - s + d;              // 8-element (16-byte) aligned
+            vec[j] = d + 8 <= U.len && sb + (s ? 16 : 8) <= a.src_len;
+            if (vec[j]) {
+                A[j] = __ldcs(reinterpret_cast<const uint4*>(a.src + sb));
+                B[j] = s ? __ldcs(reinterpret_cast<const uint4*>(a.src + sb + 8)) : A[j];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kGatherVecs; ++j) {
+            const int64_t d = base + (int64_t)j * kThreads * 8;
+            if (vec[j]) {
+                __stcs(reinterpret_cast<uint4*>(U.out + d), realign_rt(s, A[j], B[j]));
+            } else if (d < U.len) {
+                const int64_t end = U.len - d < 8 ? U.len - d : 8;
+                for (int64_t k = 0; k < end; ++k) U.out[d + k] = a.src[U.lo + d + k];
+            }
+        }
+    }
+}
+
 }  // namespace
 
 extern "C" zero_status zero3_step(const zero_plan_t* plan, const uint16_t* const* rank_grads,
@@ -166,6 +247,44 @@ extern "C" zero_status zero3_gather(const zero_plan_t* plan, const uint16_t* par
     a.len = hi - lo;
     a.n_out = n_out;
     return cuda_status(launch_gather(a, static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" zero_status zero3_gather_units(const zero_plan_t* plan, const uint16_t* param_shards,
+                                          const zero_gather_unit* units, int32_t n_units,
+                                          void* stream)
+{
+    if (zero_status e = check_plan(plan)) return e;
+    if (n_units < 0 || n_units > ZERO_MAX_GATHER_UNITS) return ZERO_ERR_INVALID_ARG;
+    if (n_units == 0) return ZERO_OK;
+    if (!units) return ZERO_ERR_NULL;
+    static thread_local GatherUnitsArgs a;           // ~29 KB: off the stack
+    static thread_local Range rs[ZERO_MAX_GATHER_UNITS + 1];
+    int nr = 0;
+    uint64_t chunks = 0;
+    for (int k = 0; k < n_units; ++k) {
+        const zero_gather_unit& u = units[k];
+        if (u.lo < 0 || u.hi < u.lo || u.hi > plan->N) return ZERO_ERR_INVALID_ARG;
+        a.chunk0[k] = (uint32_t)chunks;
+        a.u[k] = GatherUnit{u.lo, u.hi - u.lo, u.out};
+        if (u.hi == u.lo) continue;
+        if (zero_status e = check_ptr(u.out)) return e;
+        rs[nr++] = rng(u.out, 2 * (u.hi - u.lo), true);
+        chunks += (uint64_t)((u.hi - u.lo + kGatherChunk - 1) / kGatherChunk);
+        if (chunks > UINT32_MAX) return ZERO_ERR_SIZE;
+    }
+    if (chunks == 0) return ZERO_OK;
+    if (zero_status e = check_ptr(param_shards)) return e;
+    rs[nr++] = rng(param_shards, 2 * plan->padded, false);
+    if (zero_status e = check_overlap(rs, nr)) return e;
+    a.chunk0[n_units] = (uint32_t)chunks;
+    a.src = param_shards;
+    a.src_len = plan->padded;
+    a.n_units = n_units;
+    a.total_chunks = (uint32_t)chunks;
+    const void* k = reinterpret_cast<const void*>(&k_gather_units);
+    k_gather_units<<<grid_for(k, (int64_t)chunks), kThreads, 0,
+                     static_cast<cudaStream_t>(stream)>>>(a);
+    return cuda_status(cudaGetLastError());
 }
 
 // ============================================= ZeRO-3, unit by unit (FSDP) ==

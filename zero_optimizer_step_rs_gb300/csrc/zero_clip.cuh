@@ -5,19 +5,28 @@
 // =========================================== step with global-norm clipping ==
 // zero_step_clipped: the averaged gradient of every element is stashed in
 // fp32 scratch while its square feeds a fixed pairwise tree (fp32, leaves
-// g*g, zero padding to a power of two); the tree is finished level by level,
-// one thread turns the squared norm into the clip coefficient (and the
-// skip decision for a non-finite norm), and a last pass applies it with the
-// AdamW update and the R-way bf16 all-gather.
+// g*g, zero padding to a power of two); a small second kernel finishes the
+// tree and turns the squared norm into the clip coefficient (and the skip
+// decision for a non-finite norm), and a last pass applies it with the AdamW
+// update and the R-way bf16 all-gather: three launches.
 //
 // Tree decomposition: in the streaming pass each warp reduces 256
 // consecutive leaves (32 lanes x 8 leaves: a 3-level tree in registers, then
 // 5 levels of shuffles) - exactly an aligned subtree of the global tree - and
 // writes one partial, with no block-wide barrier; each further level is a
-// block reducing 2048 partials (8 leaves per thread, the warp levels, then 3
-// levels across the 8 warps), again an aligned subtree.  Adding a zero
-// (padding) changes no value, so the result equals the tree over the leaves
-// padded to the next power of two for any N and any grid.
+// block reducing 2048 partials (8 per thread, the warp levels, then 3 levels
+// across the 8 warps), again an aligned subtree.  Adding a zero (padding)
+// changes no value, so the root equals the tree over the leaves padded to
+// the next power of two for any N and any grid.
+//
+// The levels above the first are finished in one launch with arrival
+// tickets, without any wait: the blocks reduce the groups of 2048 first-level
+// partials; a block that has written its group's sum makes it visible
+// (__threadfence) and takes a ticket on the counter of its group one level
+// up, and the block that draws that group's last ticket reduces it in turn;
+// the block that completes the root computes the coefficient.  No block ever
+// waits for another.  The counters are zeroed by the streaming pass, which
+// the tree launch follows in stream order.
 namespace {
 
 constexpr int kTreeLeaves = 2048;                 // leaves per tree block (256 x 8)
@@ -32,9 +41,10 @@ struct ClipCtl {
 };
 
 struct ClipLayout {
-    int64_t g_off, ctl_off, total;
+    int64_t g_off, ctl_off, cnt_off, cnt_bytes, total;
     int levels;
     int64_t lvl_off[8], lvl_len[8];
+    int64_t cnt_base[8];   // first counter of level k >= 2 (index into the counter array)
 };
 
 int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
@@ -56,12 +66,18 @@ ClipLayout clip_layout(const zero_plan_t* plan)
         len = (len + kTreeLeaves - 1) / kTreeLeaves;
     }
     L.ctl_off = off;
-    L.total = off + round256((int64_t)sizeof(ClipCtl));
+    L.cnt_off = off + round256((int64_t)sizeof(ClipCtl));
+    int64_t cnt = 0;                              // one counter per group above level 1
+    for (int k = 2; k < L.levels; ++k) {
+        L.cnt_base[k] = cnt;
+        cnt += L.lvl_len[k];
+    }
+    L.cnt_bytes = 4 * cnt;
+    L.total = L.cnt_off + round256(L.cnt_bytes);
     return L;
 }
 
-// sum of a thread's 8 leaves, then the warp and block levels; returns the
-// block's value in thread 0
+// pairwise sum of 8 consecutive leaves (a perfect tree of 3 levels)
 __device__ __forceinline__ float tree8(const float (&x)[8])
 {
     return __fadd_rn(__fadd_rn(__fadd_rn(x[0], x[1]), __fadd_rn(x[2], x[3])),
@@ -82,11 +98,7 @@ __device__ __forceinline__ float block_tree(float v)
 {
     __shared__ float warp_sum[kThreads / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float o = __shfl_down_sync(0xFFFFFFFFu, v, off);
-        v = __fadd_rn(v, o);           // meaningful in lanes that are multiples of 2*off
-    }
+    v = warp_tree(v);
     if (lane == 0) warp_sum[warp] = v;
     __syncthreads();
     float r = 0.0f;
@@ -95,15 +107,20 @@ __device__ __forceinline__ float block_tree(float v)
         r = __fadd_rn(__fadd_rn(__fadd_rn(w[0], w[1]), __fadd_rn(w[2], w[3])),
                       __fadd_rn(__fadd_rn(w[4], w[5]), __fadd_rn(w[6], w[7])));
     }
-    __syncthreads();                   // warp_sum is reused by the next tile
-    return r;
+    __syncthreads();                   // warp_sum is reused by the next group
+    return r;                          // thread 0 holds the block's subtree
 }
 
 struct ClipArgs {
     GradPtrs g;
     ReplicaPtrs P;
     float* gs;             // averaged gradients (padded floats; [0, N) used)
-    float* lvl0;           // first tree level: one partial per 256 elements (per warp)
+    float* lvl[8];         // tree levels: level 0 has one partial per 256 elements (per warp)
+    int64_t lvl_len[8];
+    uint32_t* cnt[8];      // arrival counters of the groups of level k >= 2
+    uint32_t* cnt_all;     // all counters, zeroed by the streaming pass
+    int64_t n_cnt;
+    int32_t levels;
     float* W;
     float* m;
     float* v;
@@ -111,7 +128,79 @@ struct ClipArgs {
     int64_t n;
     int32_t R, M;
     StepScalars s;
+    float max_norm;
+    int32_t skip_nonfinite;
+    int32_t* status;
+    double* sumsq_out;
 };
+
+// The squared norm into the clip coefficient (double, as clip_grad_norm_
+// computes it) and the skip decision, by the one thread that holds the root.
+__device__ void clip_finish(const ClipArgs& a, float ss)
+{
+    const double norm = sqrt((double)ss);
+    const double coef = (double)a.max_norm / (norm + 1e-6);
+    ClipCtl c{};
+    c.sumsq = (double)ss;
+    c.clip = coef < 1.0 ? 1 : 0;
+    c.coef = c.clip ? (float)coef : 1.0f;
+    const bool finite = isfinite(ss);
+    c.skip = (!finite && a.skip_nonfinite) ? 1 : 0;
+    *a.ctl = c;
+    if (a.status) {
+        if (!finite) atomicOr(a.status, ZERO_DEV_NONFINITE);
+        if (c.skip) atomicOr(a.status, ZERO_DEV_SKIPPED);
+    }
+    if (a.sumsq_out) *a.sumsq_out = c.sumsq;
+}
+
+// sum of group b of level k - 1 (at most 2048 partials, read from L2: other
+// blocks wrote them) into partial b of level k; the value in thread 0
+__device__ __forceinline__ float reduce_group(const ClipArgs& a, int k, int64_t b)
+{
+    const int64_t lo = b * kTreeLeaves;
+    const int64_t n_in = a.lvl_len[k - 1];
+    const float* in = a.lvl[k - 1];
+    const int64_t e = lo + (int64_t)threadIdx.x * 8;
+    float x[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = e + j < n_in ? __ldcg(in + e + j) : 0.0f;
+    const float v = block_tree(tree8(x));
+    if (threadIdx.x == 0) a.lvl[k][b] = v;
+    return v;
+}
+
+// the levels above the first, then the coefficient: one launch
+__global__ void __launch_bounds__(kThreads) k_norm_tree(const __grid_constant__ ClipArgs a)
+{
+    __shared__ uint32_t last;
+    if (a.levels == 1) {                           // a single first-level partial is the root
+        if (blockIdx.x == 0 && threadIdx.x == 0) clip_finish(a, a.lvl[0][0]);
+        return;
+    }
+    for (int64_t g = blockIdx.x; g < a.lvl_len[1]; g += gridDim.x) {
+        float v = reduce_group(a, 1, g);
+        int64_t idx = g;
+        int k = 2;
+        for (; k < a.levels; ++k) {                // climb while this block is the last arrival
+            const int64_t b = idx / kTreeLeaves;
+            const int64_t n_in = a.lvl_len[k - 1] - b * kTreeLeaves;
+            const uint32_t expect = (uint32_t)(n_in < kTreeLeaves ? n_in : kTreeLeaves);
+            if (threadIdx.x == 0) {
+                __threadfence();                   // partial idx of level k - 1, before the ticket
+                last = atomicAdd(&a.cnt[k][b], 1u) == expect - 1;
+            }
+            __syncthreads();
+            const bool mine = last;
+            __syncthreads();                       // `last` is reused at the next level
+            if (!mine) break;
+            __threadfence();                       // the group's partials, after the tickets
+            v = reduce_group(a, k, b);
+            idx = b;
+        }
+        if (k == a.levels && threadIdx.x == 0) clip_finish(a, v);
+    }
+}
 
 // pass 1: averaged gradient of 8 consecutive elements per thread, stashed,
 // and the tile's pairwise partial of their squares
@@ -151,44 +240,11 @@ __global__ void __launch_bounds__(kThreads) k_rs_norm(const __grid_constant__ Cl
         for (int k = 0; k < 8; ++k) sq[k] = __fmul_rn(g[k], g[k]);   // padding leaves are +0
         const float part = warp_tree(tree8(sq));
         const int64_t wpart = tile * (kTreeLeaves / kWarpLeaves) + (threadIdx.x >> 5);
-        if ((threadIdx.x & 31) == 0 && wpart * kWarpLeaves < n) a.lvl0[wpart] = part;
+        if ((threadIdx.x & 31) == 0 && wpart * kWarpLeaves < n) a.lvl[0][wpart] = part;
     }
-}
-
-// one level of the tree: out[b] = pairwise sum of in[2048 b .. 2048 b + 2047]
-__global__ void __launch_bounds__(kThreads) k_tree(const float* __restrict__ in, int64_t n_in,
-                                                   float* __restrict__ out)
-{
-    const int64_t blocks = (n_in + kTreeLeaves - 1) / kTreeLeaves;
-    for (int64_t b = blockIdx.x; b < blocks; b += gridDim.x) {
-        const int64_t e = b * kTreeLeaves + (int64_t)threadIdx.x * 8;
-        float x[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) x[k] = e + k < n_in ? in[e + k] : 0.0f;
-        const float part = block_tree(tree8(x));
-        if (threadIdx.x == 0) out[b] = part;
-    }
-}
-
-__global__ void k_clip_coef(const float* __restrict__ root, ClipCtl* ctl, float max_norm,
-                            int32_t skip_nonfinite, int32_t* status, double* sumsq_out)
-{
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
-    const float ss = *root;
-    const double norm = sqrt((double)ss);
-    const double coef = (double)max_norm / (norm + 1e-6);
-    ClipCtl c{};
-    c.sumsq = (double)ss;
-    c.clip = coef < 1.0 ? 1 : 0;
-    c.coef = c.clip ? (float)coef : 1.0f;
-    const bool finite = isfinite(ss);
-    c.skip = (!finite && skip_nonfinite) ? 1 : 0;
-    *ctl = c;
-    if (status) {
-        if (!finite) atomicOr(status, ZERO_DEV_NONFINITE);
-        if (c.skip) atomicOr(status, ZERO_DEV_SKIPPED);
-    }
-    if (sumsq_out) *sumsq_out = c.sumsq;
+    // the tree launch that follows takes tickets on these counters
+    if (blockIdx.x == 0)
+        for (int64_t i = threadIdx.x; i < a.n_cnt; i += kThreads) a.cnt_all[i] = 0u;
 }
 
 // pass 2: g' = g * coef (when clipping), AdamW, bf16 all-gather; tiles of
@@ -332,7 +388,19 @@ extern "C" zero_status zero_step_clipped(const zero_plan_t* plan,
     fill_grad_ptrs(a.g, plan, rank_grads);
     fill_replica_ptrs(a.P, plan, rank_params);
     a.gs = reinterpret_cast<float*>(base + L.g_off);
-    a.lvl0 = reinterpret_cast<float*>(base + L.lvl_off[0]);
+    uint32_t* counters = reinterpret_cast<uint32_t*>(base + L.cnt_off);
+    a.levels = L.levels;
+    for (int k = 0; k < L.levels; ++k) {
+        a.lvl[k] = reinterpret_cast<float*>(base + L.lvl_off[k]);
+        a.lvl_len[k] = L.lvl_len[k];
+        a.cnt[k] = k >= 2 ? counters + L.cnt_base[k] : nullptr;
+    }
+    a.cnt_all = counters;
+    a.n_cnt = L.cnt_bytes / 4;
+    a.max_norm = max_norm;
+    a.skip_nonfinite = (flags & ZERO_FLAG_SKIP_NONFINITE) ? 1 : 0;
+    a.status = dev_status;
+    a.sumsq_out = dev_sumsq;
     a.W = master;
     a.m = m;
     a.v = v;
@@ -344,18 +412,9 @@ extern "C" zero_status zero_step_clipped(const zero_plan_t* plan,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     cudaError_t err = launch_rs_norm(a, st);
-    for (int l = 1; l < L.levels && err == cudaSuccess; ++l) {
-        const float* in = reinterpret_cast<const float*>(base + L.lvl_off[l - 1]);
-        float* out = reinterpret_cast<float*>(base + L.lvl_off[l]);
-        const void* k = reinterpret_cast<const void*>(&k_tree);
-        k_tree<<<grid_for(k, L.lvl_len[l]), kThreads, 0, st>>>(in, L.lvl_len[l - 1], out);
-        err = cudaGetLastError();
-    }
     if (err == cudaSuccess) {
-        const float* root = reinterpret_cast<const float*>(base + L.lvl_off[L.levels - 1]);
-        k_clip_coef<<<1, 32, 0, st>>>(root, a.ctl, max_norm,
-                                      (flags & ZERO_FLAG_SKIP_NONFINITE) ? 1 : 0, dev_status,
-                                      dev_sumsq);
+        const void* k = reinterpret_cast<const void*>(&k_norm_tree);
+        k_norm_tree<<<L.levels > 1 ? grid_for(k, L.lvl_len[1]) : 1, kThreads, 0, st>>>(a);
         err = cudaGetLastError();
     }
     if (err == cudaSuccess) err = launch_adamw_ag(a, st);

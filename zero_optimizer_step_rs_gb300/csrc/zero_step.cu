@@ -31,6 +31,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <mutex>
@@ -104,6 +105,8 @@ struct StagedArgs {
     ReplicaPtrs P;
     const float* gs;      // scratch gradient (rs_avg writes it, adamw reads it)
     float* gs_out;
+    uint16_t* g_lo;       // or, when set, the gradient kept in two gradient buffers:
+    uint16_t* g_hi;       // the low and high 16 bits of each element's fp32 value
     float* W;
     float* m;
     float* v;
@@ -258,14 +261,14 @@ int device_sms(int dev)
     return d.sms > 0 ? d.sms : 1;
 }
 
-int blocks_per_sm(int dev, const void* kernel)
+int blocks_per_sm(int dev, const void* kernel, int threads = kThreads)
 {
     std::lock_guard<std::mutex> lk(g_mu);
     DevInfo& d = g_dev[dev & 63];
     auto it = d.occ.find(kernel);
     if (it != d.occ.end()) return it->second;
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, 0) != cudaSuccess ||
         nb < 1)
         nb = 1;
     d.occ[kernel] = nb;
@@ -278,11 +281,12 @@ int blocks_per_sm(int dev, const void* kernel)
 // grid sizes on GB300 found HBM busier with fewer blocks than fit (the
 // launch sites give the measured values), while smaller launches, bound by
 // latency and ramp-up, run faster with every block that fits.
-unsigned grid_for(const void* kernel, int64_t work_blocks, int quarter_blocks = 0)
+unsigned grid_for(const void* kernel, int64_t work_blocks, int quarter_blocks = 0,
+                  int threads = kThreads)
 {
     int dev = 0;
     cudaGetDevice(&dev);
-    int64_t cap = (int64_t)device_sms(dev) * blocks_per_sm(dev, kernel);
+    int64_t cap = (int64_t)device_sms(dev) * blocks_per_sm(dev, kernel, threads);
     if (quarter_blocks > 0 && work_blocks >= 4 * cap) {
         const int64_t q = (int64_t)quarter_blocks * device_sms(dev) / 4;
         if (q >= 1 && q < cap) cap = q;
@@ -300,12 +304,13 @@ unsigned grid_for(const void* kernel, int64_t work_blocks, int quarter_blocks = 
 //      zero-copy mode writes replica 0 to host memory as well)
 //   2  one buffer a.P.p[0] in the padded layout of the state: each rank
 //      casts into its own parameter shard, no all-gather   (ZeRO-3)
-template <int RC, int MC, int U, bool CHECK, int OUT>
-__global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ FusedArgs a)
+template <int RC, int MC, int U, bool CHECK, int OUT, int TPB = kThreads>
+__global__ void __launch_bounds__(TPB) k_fused(const __grid_constant__ FusedArgs a)
 {
     const int R = RC > 0 ? RC : a.R;
     const int M = MC > 0 ? MC : a.M;
-    constexpr int T = kUnit * U;
+    constexpr int kU = TPB * kVec;             // elements per block per unit
+    constexpr int T = kU * U;
     const int64_t n = a.n;
     const int64_t full_tiles = n / T;
     bool bad = false;
@@ -316,7 +321,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ Fuse
         float4 w[U], mm[U], vv[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int64_t e = e0 + (int64_t)u * kUnit;
+            const int64_t e = e0 + (int64_t)u * kU;
             w[u] = ld_stream(a.W + e);
             mm[u] = ld_stream(a.m + e);
             vv[u] = ld_stream(a.v + e);
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ Fuse
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int64_t e = e0 + (int64_t)u * kUnit;
+            const int64_t e = e0 + (int64_t)u * kU;
             float* wp = &w[u].x;
             float* mp = &mm[u].x;
             float* vp = &vv[u].x;
@@ -353,7 +358,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ Fuse
     // last partial tile, element by element, by the block that owns it
     const int64_t tail0 = full_tiles * T;
     if (tail0 < n && blockIdx.x == (unsigned)(full_tiles % gridDim.x)) {
-        for (int64_t i = tail0 + threadIdx.x; i < n; i += kThreads) {
+        for (int64_t i = tail0 + threadIdx.x; i < n; i += TPB) {
             const float g = scale_grad(a.s, grad_sum1(a.g, R, M, i));
             if (CHECK) bad |= !isfinite(g);
             float w = a.W[i], m = a.m[i], v = a.v[i];
@@ -391,12 +396,29 @@ constexpr int fused_quarter_blocks()
     return 0;
 }
 
+// A vector too short to give every resident block of the full-size tiling a
+// tile (fewer than one wave) leaves SMs idle, and its step is bound by
+// latency, not bandwidth: it takes tiles of one unit of kSmallThreads
+// threads instead, spread over more SMs.
+constexpr int kSmallThreads = 128;
+constexpr int kSmallUnits = 1;
+
 template <int RC, int MC, bool CHECK, int OUT = 0>
 cudaError_t launch_fused_t(const FusedArgs& a, cudaStream_t st)
 {
     constexpr int U = 2;
     const void* k = reinterpret_cast<const void*>(&k_fused<RC, MC, U, CHECK, OUT>);
     const int64_t tiles = (a.n + kUnit * U - 1) / (kUnit * U);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (tiles < (int64_t)device_sms(dev) * blocks_per_sm(dev, k)) {
+        constexpr int TS = kSmallThreads, US = kSmallUnits;
+        const void* ks = reinterpret_cast<const void*>(&k_fused<RC, MC, US, CHECK, OUT, TS>);
+        const int64_t small_tiles = (a.n + TS * kVec * US - 1) / (TS * kVec * US);
+        const unsigned grid = grid_for(ks, small_tiles, 0, TS);
+        k_fused<RC, MC, US, CHECK, OUT, TS><<<grid, TS, 0, st>>>(a);
+        return cudaGetLastError();
+    }
     const unsigned grid = grid_for(k, tiles, fused_quarter_blocks<RC, MC, OUT>());
     k_fused<RC, MC, U, CHECK, OUT><<<grid, kThreads, 0, st>>>(a);
     return cudaGetLastError();
@@ -468,7 +490,19 @@ __global__ void __launch_bounds__(kThreads) k_rs_avg(const __grid_constant__ Sta
             o.z = scale_grad(a.s, acc[u][2]);
             o.w = scale_grad(a.s, acc[u][3]);
             if (CHECK) bad |= !(isfinite(o.x) && isfinite(o.y) && isfinite(o.z) && isfinite(o.w));
-            st_stream(a.gs_out + e0 + (int64_t)u * kUnit, o);
+            const int64_t e = e0 + (int64_t)u * kUnit;
+            if (a.g_lo) {
+                // every gradient of these elements has been read above: their
+                // slots in buffers 0 and 1 are free to hold the result
+                const uint32_t b0 = __float_as_uint(o.x), b1 = __float_as_uint(o.y);
+                const uint32_t b2 = __float_as_uint(o.z), b3 = __float_as_uint(o.w);
+                st_stream(a.g_lo + e, make_uint2(__byte_perm(b0, b1, 0x5410),
+                                                 __byte_perm(b2, b3, 0x5410)));
+                st_stream(a.g_hi + e, make_uint2(__byte_perm(b0, b1, 0x7632),
+                                                 __byte_perm(b2, b3, 0x7632)));
+            } else {
+                st_stream(a.gs_out + e, o);
+            }
         }
     }
     // the shard's last partial tile, element by element, by the block that owns it
@@ -477,7 +511,12 @@ __global__ void __launch_bounds__(kThreads) k_rs_avg(const __grid_constant__ Sta
         for (int64_t i = tail0 + threadIdx.x; i < lo + len; i += kThreads) {
             const float g = scale_grad(a.s, grad_sum1(a.g, R, M, i));
             if (CHECK) bad |= !isfinite(g);
-            a.gs_out[i] = g;
+            if (a.g_lo) {
+                a.g_lo[i] = (uint16_t)(__float_as_uint(g) & 0xFFFFu);
+                a.g_hi[i] = (uint16_t)(__float_as_uint(g) >> 16);
+            } else {
+                a.gs_out[i] = g;
+            }
         }
     }
     report_nonfinite<CHECK>(bad, a.status);
@@ -491,7 +530,16 @@ __global__ void __launch_bounds__(kThreads) k_adamw(const __grid_constant__ Stag
     for (int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x; q < nvec;
          q += (int64_t)gridDim.x * kThreads) {
         const int64_t e = lo + q * kVec;
-        const float4 g = ld_stream(a.gs + e);
+        float4 g;
+        if (a.g_lo) {
+            const uint2 l = ld_stream(a.g_lo + e), h = ld_stream(a.g_hi + e);
+            g = make_float4(__uint_as_float(__byte_perm(l.x, h.x, 0x5410)),
+                            __uint_as_float(__byte_perm(l.x, h.x, 0x7632)),
+                            __uint_as_float(__byte_perm(l.y, h.y, 0x5410)),
+                            __uint_as_float(__byte_perm(l.y, h.y, 0x7632)));
+        } else {
+            g = ld_stream(a.gs + e);
+        }
         float4 w = ld_stream(a.W + e), m = ld_stream(a.m + e), v = ld_stream(a.v + e);
         adamw(a.s, g.x, w.x, m.x, v.x);
         adamw(a.s, g.y, w.y, m.y, v.y);
@@ -504,7 +552,10 @@ __global__ void __launch_bounds__(kThreads) k_adamw(const __grid_constant__ Stag
     if (blockIdx.x == 0) {
         for (int64_t i = lo + nvec * kVec + threadIdx.x; i < lo + len; i += kThreads) {
             float w = a.W[i], m = a.m[i], v = a.v[i];
-            adamw(a.s, a.gs[i], w, m, v);
+            const float g = a.g_lo ? __uint_as_float((uint32_t)a.g_lo[i] |
+                                                     ((uint32_t)a.g_hi[i] << 16))
+                                   : a.gs[i];
+            adamw(a.s, g, w, m, v);
             a.W[i] = w;
             a.m[i] = m;
             a.v[i] = v;
@@ -512,30 +563,45 @@ __global__ void __launch_bounds__(kThreads) k_adamw(const __grid_constant__ Stag
     }
 }
 
-template <int RC>
+template <int RC, int VPT>
 __global__ void __launch_bounds__(kThreads) k_ag_cast(const __grid_constant__ StagedArgs a)
 {
-    // 8 elements per thread: two float4 loads of W, one 16-byte store per
-    // replica.  A shard starts on a multiple of 4 elements only, so the vector
-    // loop starts at the shard's first multiple of 8; the head before it and
-    // the tail after the last full vector are done element by element.
+    // VPT vectors of 8 elements per thread per iteration, blockDim vectors
+    // apart (each warp instruction stays contiguous): two float4 loads of W
+    // and one 16-byte store per replica each, every load issued first.  A
+    // shard starts on a multiple of 4 elements only, so the vector loop
+    // starts at the shard's first multiple of 8; the head before it and the
+    // tail after the last full vector are done element by element.
     const int R = RC > 0 ? RC : a.R;
     const int r = blockIdx.y;
     const int64_t lo = (int64_t)r * a.S, len = shard_len(a.n, a.S, r);
     const int64_t hi = lo + len;
     const int64_t v0 = (lo + 7) / 8 * 8;                  // first 8-aligned element
     const int64_t n8 = hi > v0 ? (hi - v0) / 8 : 0;
-    for (int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x; q < n8;
-         q += (int64_t)gridDim.x * kThreads) {
-        const int64_t e = v0 + q * 8;
-        const float4 w0 = ld_stream(a.W + e), w1 = ld_stream(a.W + e + 4);
-        const uint4 p = make_uint4(pack_bf16x2(w0.x, w0.y), pack_bf16x2(w0.z, w0.w),
-                                   pack_bf16x2(w1.x, w1.y), pack_bf16x2(w1.z, w1.w));
-        if constexpr (RC > 0) {
+    for (int64_t q0 = (int64_t)blockIdx.x * kThreads * VPT + threadIdx.x; q0 < n8;
+         q0 += (int64_t)gridDim.x * kThreads * VPT) {
+        float4 w0[VPT], w1[VPT];
 #pragma unroll
-            for (int k = 0; k < RC; ++k) __stcs(reinterpret_cast<uint4*>(a.P.p[k] + e), p);
-        } else {
-            for (int k = 0; k < R; ++k) __stcs(reinterpret_cast<uint4*>(a.P.p[k] + e), p);
+        for (int j = 0; j < VPT; ++j) {
+            const int64_t q = q0 + (int64_t)j * kThreads;
+            if (q < n8) {
+                w0[j] = ld_stream(a.W + v0 + q * 8);
+                w1[j] = ld_stream(a.W + v0 + q * 8 + 4);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int64_t q = q0 + (int64_t)j * kThreads;
+            if (q >= n8) break;
+            const int64_t e = v0 + q * 8;
+            const uint4 p = make_uint4(pack_bf16x2(w0[j].x, w0[j].y), pack_bf16x2(w0[j].z, w0[j].w),
+                                       pack_bf16x2(w1[j].x, w1[j].y), pack_bf16x2(w1[j].z, w1[j].w));
+            if constexpr (RC > 0) {
+#pragma unroll
+                for (int k = 0; k < RC; ++k) __stcs(reinterpret_cast<uint4*>(a.P.p[k] + e), p);
+            } else {
+                for (int k = 0; k < R; ++k) __stcs(reinterpret_cast<uint4*>(a.P.p[k] + e), p);
+            }
         }
     }
     if (blockIdx.x == 0) {
@@ -586,21 +652,29 @@ cudaError_t launch_adamw(const StagedArgs& a, cudaStream_t st)
     return cudaGetLastError();
 }
 
+constexpr int kAgVecs = 1;             // vectors of 8 elements per thread per iteration
+constexpr int kAgQuarterBlocks = 0;    // grid cap in quarter blocks per SM (0: every resident block)
+
 cudaError_t launch_ag(const StagedArgs& a, cudaStream_t st)
 {
-    const int64_t work = (a.S / 8 + kThreads - 1) / kThreads;
+    const int64_t work = (a.S / 8 + kThreads * kAgVecs - 1) / (kThreads * kAgVecs);
     auto go = [&](const void* k, auto kern) {
-        const int64_t per_rank = (int64_t)grid_for(k, work * a.R) / a.R;    // never past one wave
+        const int64_t per_rank =
+            (int64_t)grid_for(k, work * a.R, kAgQuarterBlocks) / a.R;    // never past one wave
         dim3 grid((unsigned)(per_rank < 1 ? 1 : per_rank), (unsigned)a.R);
         kern<<<grid, kThreads, 0, st>>>(a);
         return cudaGetLastError();
     };
+#define ZERO_AG(r_) \
+    return go(reinterpret_cast<const void*>(&k_ag_cast<r_, kAgVecs>), k_ag_cast<r_, kAgVecs>);
     switch (a.R) {
-    case 8: return go(reinterpret_cast<const void*>(&k_ag_cast<8>), k_ag_cast<8>);
-    case 4: return go(reinterpret_cast<const void*>(&k_ag_cast<4>), k_ag_cast<4>);
-    case 2: return go(reinterpret_cast<const void*>(&k_ag_cast<2>), k_ag_cast<2>);
-    default: return go(reinterpret_cast<const void*>(&k_ag_cast<0>), k_ag_cast<0>);
+    case 8: ZERO_AG(8)
+    case 7: ZERO_AG(7)
+    case 4: ZERO_AG(4)
+    case 2: ZERO_AG(2)
+    default: ZERO_AG(0)
     }
+#undef ZERO_AG
 }
 
 // ---------------------------------------------------------- validation --
@@ -634,13 +708,7 @@ struct Range {
 // Outputs may not overlap anything; inputs may overlap inputs.
 zero_status check_overlap(Range* r, int n)
 {
-    // insertion sort by start (n is at most a few hundred)
-    for (int i = 1; i < n; ++i) {
-        Range x = r[i];
-        int j = i - 1;
-        while (j >= 0 && r[j].lo > x.lo) { r[j + 1] = r[j]; --j; }
-        r[j + 1] = x;
-    }
+    std::sort(r, r + n, [](const Range& x, const Range& y) { return x.lo < y.lo; });
     uintptr_t max_end_all = 0, max_end_out = 0;
     for (int i = 0; i < n; ++i) {
         if (r[i].hi <= r[i].lo) continue;
@@ -739,7 +807,13 @@ extern "C" zero_status zero_step(const zero_plan_t* plan, const uint16_t* const*
     if (zero_status e = check_grads(plan, rank_grads, rs, nr)) return e;
     if (zero_status e = check_replicas(plan, rank_params, rs, nr)) return e;
     if (zero_status e = check_state(plan, master, m, v, rs, nr)) return e;
-    if (variant == ZERO_VARIANT_STAGED) {
+    // ZeRO-2 gives up the gradients once they are reduced: without scratch the
+    // staged step keeps the reduced gradient in gradient buffers 0 and 1
+    const bool in_grads = variant == ZERO_VARIANT_STAGED && !scratch && plan->stage == 2 &&
+                          plan->R * plan->M >= 2;
+    if (in_grads) {
+        rs[0].out = rs[1].out = true;          // written: they may alias nothing
+    } else if (variant == ZERO_VARIANT_STAGED) {
         if (zero_status e = check_ptr(scratch)) return e;
         if (scratch_bytes < plan->scratch_bytes_staged) return ZERO_ERR_SIZE;
         rs[nr++] = rng(scratch, plan->scratch_bytes_staged, true);
@@ -774,6 +848,10 @@ extern "C" zero_status zero_step(const zero_plan_t* plan, const uint16_t* const*
     fill_replica_ptrs(a.P, plan, rank_params);
     a.gs = static_cast<const float*>(scratch);
     a.gs_out = static_cast<float*>(scratch);
+    if (in_grads) {
+        a.g_lo = const_cast<uint16_t*>(rank_grads[0]);
+        a.g_hi = const_cast<uint16_t*>(rank_grads[1]);
+    }
     a.W = master;
     a.m = m;
     a.v = v;
@@ -971,6 +1049,26 @@ extern "C" zero_status zero_step_host(const zero_plan_t* plan, const uint16_t* c
     return cuda_status(check ? launch_fused<true>(a, st) : launch_fused<false>(a, st));
 }
 
+extern "C" zero_status zero_get_device_status(const int32_t* dev_status, void* stream,
+                                              int32_t* out)
+{
+    if (!dev_status) return ZERO_ERR_NULL;
+    if ((uintptr_t)dev_status & 3u) return ZERO_ERR_ALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t word = 0;
+    // ordered after the steps on `stream`; then wait for the stream to finish
+    if (cudaMemcpyAsync(&word, dev_status, sizeof word, cudaMemcpyDeviceToHost, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return ZERO_ERR_CUDA;
+    }
+    if (out) *out = word;
+    if (word & ZERO_DEV_TIMEOUT) return ZERO_ERR_DEVICE_TIMEOUT;
+    if (word & ZERO_DEV_NONFINITE) return ZERO_ERR_NONFINITE;
+    return ZERO_OK;
+}
+
 // The variants and the other entry points, in files of their own (one translation unit).
 #include "zero_clip.cuh"
 #include "zero_compress.cuh"
@@ -984,29 +1082,60 @@ extern "C" zero_status zero_step_host(const zero_plan_t* plan, const uint16_t* c
 // scratch in a fixed device array of this file instead of a caller buffer,
 // for callers that cannot allocate device memory.  The array's address is a
 // device address only on the device side; host code looks it up once per
-// device with cudaGetSymbolAddress (with that device current) and passes it
-// to the kernels like any other scratch pointer.
+// device with cudaGetSymbolAddress (with that device current; again after
+// the device's context has been replaced) and passes it to the kernels like
+// any other scratch pointer.
 namespace {
 
 static __device__ __align__(256) float g_noalloc_scratch[ZERO_NOALLOC_MAX_ELEMS];
 
 std::mutex g_noalloc_mu;
-float* g_noalloc_addr[64] = {};            // per device ordinal, looked up once
+struct NoallocAddr {
+    const void* ctx;                      // the context the address was looked up in
+    float* addr;
+};
+NoallocAddr g_noalloc_addr[64] = {};      // per device ordinal
 
+// The current context's handle, through the driver entry point the runtime
+// hands out (no link to the driver library is needed).  A device reset
+// replaces the primary context and may place the array elsewhere, so the
+// cached address is only reused in the context it was looked up in.
+const void* current_context()
+{
+    using GetCtx = int (*)(void**);
+    static GetCtx fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<GetCtx>(f);
+    }();
+    void* ctx = nullptr;
+    if (!fn || fn(&ctx) != 0) return nullptr;
+    return ctx;
+}
+
+// The array's device address for the current device, looked up once per
+// device (and again after the device's context has been replaced).
 zero_status noalloc_scratch(float** out)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ZERO_ERR_CUDA;
+    const void* ctx = current_context();
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
+    NoallocAddr& slot = g_noalloc_addr[dev];
+    if (!slot.addr || !ctx || slot.ctx != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
             cudaGetLastError();            // clear it so later launch checks do not see it
             return ZERO_ERR_CUDA;
         }
-        g_noalloc_addr[dev] = static_cast<float*>(p);
+        slot.addr = static_cast<float*>(p);
+        slot.ctx = current_context();      // the lookup has made the device's context current
     }
-    *out = g_noalloc_addr[dev];
+    *out = slot.addr;
     return ZERO_OK;
 }
 
@@ -1034,6 +1163,14 @@ extern "C" zero_status zero_step_staged_noalloc(const zero_plan_t* plan,
     if (dev_status) rs[nr++] = rng(dev_status, 4, true);
     if (zero_status e = check_overlap(rs, nr)) return e;
 
+    // the array's address belongs to the current device: the stream must too
+    int dev = -1, sdev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_ERR_CUDA;
+    if (cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess) {
+        cudaGetLastError();
+        return ZERO_ERR_INVALID_ARG;
+    }
+    if (sdev != dev) return ZERO_ERR_INVALID_ARG;
     float* scratch = nullptr;
     if (zero_status e = noalloc_scratch(&scratch)) return e;
 

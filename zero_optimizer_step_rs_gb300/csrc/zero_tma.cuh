@@ -17,7 +17,9 @@
 // (the decision is block-uniform) stops, thread 0 waits - again bounded -
 // for the stage loads it has issued and not consumed, and for its bulk
 // stores, sets ZERO_DEV_TIMEOUT in the status word and the block returns, so
-// no copy can land in shared memory after the block has left.
+// no copy can land in shared memory after the block has left.  If that
+// drain runs out as well, ZERO_DEV_DRAIN_FAILED is set beside it: the block
+// has left with copies in flight and the context is suspect.
 namespace {
 
 constexpr int kTmaTile = 1024;                   // 256 threads x 4 elements
@@ -169,8 +171,12 @@ __global__ void __launch_bounds__(kThreads) k_fused_tma(const __grid_constant__ 
             if (a.status) atomicOr(a.status, ZERO_DEV_TIMEOUT);
             // the loads issued for tiles k_fail .. k_fail+stages-1 must land
             // before this block's shared memory can be given to another block
+            bool drained = true;
             for (int64_t kk = k_fail; kk < k_fail + kTmaStages && kk < my; ++kk)
-                mbar_wait(&full[kk % kTmaStages], (uint32_t)((kk / kTmaStages) & 1), kDrainLimit);
+                drained &= mbar_wait(&full[kk % kTmaStages], (uint32_t)((kk / kTmaStages) & 1),
+                                     kDrainLimit);
+            // copies may still land in this block's shared memory after it leaves
+            if (!drained && a.status) atomicOr(a.status, ZERO_DEV_DRAIN_FAILED);
         }
         __syncthreads();
     }
