@@ -104,16 +104,15 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t st)
 }
 
 // k_gather_units: the same copy over a table of units in one launch.  Each
-// unit is cut into chunks of 256 threads x 2 vectors of 8 elements; a block
-// takes chunks grid-stride over the whole table.  A chunk's unit is the
-// previous chunk's while it still fits, else found by a binary search of the
-// units' first chunks (block-uniform, so the table is read from the
-// constant bank by broadcast).  Both source loads of a thread are issued
-// before its stores.  A unit's shift lo mod 8 is uniform over its chunks;
-// the same funnel-shift realignment as k_gather picks each destination
-// vector out of two aligned source vectors.
-constexpr int kGatherVecs = 2;                     // 8-element vectors per thread per chunk
-constexpr int kGatherChunk = kThreads * 8 * kGatherVecs;
+// unit is cut into chunks of 256 threads x 8 elements; a block takes chunks
+// grid-stride over the whole table.  A chunk's unit is the previous chunk's
+// while it still fits, else found by a binary search of the units' first
+// chunks, which each block copies into shared memory once.  A unit's shift
+// lo mod 8 is uniform over its chunks; the same funnel-shift realignment as
+// k_gather picks the destination vector out of two aligned source vectors.
+// (Two vectors per thread per chunk measured slower: 0.886 against 0.97 of
+// the copy peak for one unit of the whole 1B-shaped model.)
+constexpr int kGatherChunk = kThreads * 8;
 
 struct GatherUnit {
     int64_t lo, len;
@@ -145,41 +144,32 @@ __device__ __forceinline__ uint4 realign_rt(int s, uint4 A, uint4 B)
 
 __global__ void __launch_bounds__(kThreads) k_gather_units(const __grid_constant__ GatherUnitsArgs a)
 {
+    __shared__ uint32_t chunk0[ZERO_MAX_GATHER_UNITS + 1];
+    for (int i = threadIdx.x; i <= a.n_units; i += kThreads) chunk0[i] = a.chunk0[i];
+    __syncthreads();
     int u = 0;
     for (uint32_t c = blockIdx.x; c < a.total_chunks; c += gridDim.x) {
-        if (c >= a.chunk0[u + 1]) {                 // past the unit: last unit whose first chunk <= c
+        if (c >= chunk0[u + 1]) {                   // past the unit: last unit whose first chunk <= c
             int ulo = u + 1, uhi = a.n_units - 1;
             while (ulo < uhi) {
                 const int mid = (ulo + uhi + 1) >> 1;
-                if (a.chunk0[mid] <= c) ulo = mid;
+                if (chunk0[mid] <= c) ulo = mid;
                 else uhi = mid - 1;
             }
             u = ulo;
         }
         const GatherUnit& U = a.u[u];
+        const int64_t d = ((int64_t)(c - chunk0[u]) * kThreads + threadIdx.x) * 8;
+        if (d >= U.len) continue;
         const int s = (int)(U.lo & 7);
-        const int64_t base = (int64_t)(c - a.chunk0[u]) * kGatherChunk + (int64_t)threadIdx.x * 8;
-        uint4 A[kGatherVecs], B[kGatherVecs];
-        bool vec[kGatherVecs];
-#pragma unroll
-        for (int j = 0; j < kGatherVecs; ++j) {
-            const int64_t d = base + (int64_t)j * kThreads * 8;
-            const int64_t sb = U.lo - s + d;              // 8-element (16-byte) aligned
-            vec[j] = d + 8 <= U.len && sb + (s ? 16 : 8) <= a.src_len;
-            if (vec[j]) {
-                A[j] = __ldcs(reinterpret_cast<const uint4*>(a.src + sb));
-                B[j] = s ? __ldcs(reinterpret_cast<const uint4*>(a.src + sb + 8)) : A[j];
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < kGatherVecs; ++j) {
-            const int64_t d = base + (int64_t)j * kThreads * 8;
-            if (vec[j]) {
-                __stcs(reinterpret_cast<uint4*>(U.out + d), realign_rt(s, A[j], B[j]));
-            } else if (d < U.len) {
-                const int64_t end = U.len - d < 8 ? U.len - d : 8;
-                for (int64_t k = 0; k < end; ++k) U.out[d + k] = a.src[U.lo + d + k];
-            }
+        const int64_t sb = U.lo - s + d;                  // 8-element (16-byte) aligned
+        if (d + 8 <= U.len && sb + (s ? 16 : 8) <= a.src_len) {
+            const uint4 A = __ldcs(reinterpret_cast<const uint4*>(a.src + sb));
+            const uint4 B = s ? __ldcs(reinterpret_cast<const uint4*>(a.src + sb + 8)) : A;
+            __stcs(reinterpret_cast<uint4*>(U.out + d), realign_rt(s, A, B));
+        } else {
+            const int64_t end = U.len - d < 8 ? U.len - d : 8;
+            for (int64_t j = 0; j < end; ++j) U.out[d + j] = a.src[U.lo + d + j];
         }
     }
 }

@@ -174,6 +174,7 @@ __device__ __forceinline__ float reduce_group(const ClipArgs& a, int k, int64_t 
 __global__ void __launch_bounds__(kThreads) k_norm_tree(const __grid_constant__ ClipArgs a)
 {
     __shared__ uint32_t last;
+    pdl_enter();
     if (a.levels == 1) {                           // a single first-level partial is the root
         if (blockIdx.x == 0 && threadIdx.x == 0) clip_finish(a, a.lvl[0][0]);
         return;
@@ -207,6 +208,7 @@ __global__ void __launch_bounds__(kThreads) k_norm_tree(const __grid_constant__ 
 template <int RC, int MC>
 __global__ void __launch_bounds__(kThreads) k_rs_norm(const __grid_constant__ ClipArgs a)
 {
+    pdl_enter();
     const int R = RC > 0 ? RC : a.R;
     const int M = MC > 0 ? MC : a.M;
     const int64_t n = a.n;
@@ -253,6 +255,7 @@ __global__ void __launch_bounds__(kThreads) k_rs_norm(const __grid_constant__ Cl
 template <int RC>
 __global__ void __launch_bounds__(kThreads) k_adamw_ag(const __grid_constant__ ClipArgs a)
 {
+    pdl_enter();
     const ClipCtl c = *a.ctl;
     if (c.skip) return;
     const int R = RC > 0 ? RC : a.R;
@@ -316,8 +319,7 @@ cudaError_t launch_rs_norm_t(const ClipArgs& a, cudaStream_t st)
 {
     const void* k = reinterpret_cast<const void*>(&k_rs_norm<RC, MC>);
     const int64_t tiles = (a.n + kTreeLeaves - 1) / kTreeLeaves;
-    k_rs_norm<RC, MC><<<grid_for(k, tiles), kThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_rs_norm<RC, MC>, dim3(grid_for(k, tiles)), kThreads, st, a);
 }
 
 cudaError_t launch_rs_norm(const ClipArgs& a, cudaStream_t st)
@@ -334,8 +336,7 @@ cudaError_t launch_adamw_ag(const ClipArgs& a, cudaStream_t st)
 {
     const int64_t work = (a.n + 4 * kUnit - 1) / (4 * kUnit);     // tiles of 4 units
     auto go = [&](const void* k, auto kern) {
-        kern<<<grid_for(k, work < 1 ? 1 : work), kThreads, 0, st>>>(a);
-        return cudaGetLastError();
+        return launch_pdl(kern, dim3(grid_for(k, work < 1 ? 1 : work)), kThreads, st, a);
     };
     switch (a.R) {
     case 8: return go(reinterpret_cast<const void*>(&k_adamw_ag<8>), k_adamw_ag<8>);
@@ -414,8 +415,8 @@ extern "C" zero_status zero_step_clipped(const zero_plan_t* plan,
     cudaError_t err = launch_rs_norm(a, st);
     if (err == cudaSuccess) {
         const void* k = reinterpret_cast<const void*>(&k_norm_tree);
-        k_norm_tree<<<L.levels > 1 ? grid_for(k, L.lvl_len[1]) : 1, kThreads, 0, st>>>(a);
-        err = cudaGetLastError();
+        err = launch_pdl(k_norm_tree, dim3(L.levels > 1 ? grid_for(k, L.lvl_len[1]) : 1),
+                         kThreads, st, a);
     }
     if (err == cudaSuccess) err = launch_adamw_ag(a, st);
     return cuda_status(err);

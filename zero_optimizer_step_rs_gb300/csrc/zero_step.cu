@@ -33,6 +33,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <utility>
 #include <cmath>
 #include <mutex>
 #include <unordered_map>
@@ -243,7 +244,38 @@ __device__ __forceinline__ void report_nonfinite(bool bad, int32_t* status)
     }
 }
 
+// Programmatic dependent launch.  The kernels of a step are launched with
+// programmatic stream serialization: the next such launch on the stream may
+// be scheduled while the kernel before it still runs, which hides the launch
+// gap between back-to-back steps (and between the kernels of a step).  Every
+// kernel launched this way first allows its own dependent to launch, then
+// waits until the grid before it has completed and its writes are visible,
+// before touching memory.  A launch that follows anything other than such a
+// kernel (a copy, an event, another library's kernel) waits as usual.
+__device__ __forceinline__ void pdl_enter()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------ launch helpers --
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, int threads, cudaStream_t st,
+                       Args&&... args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct DevInfo {
     int sms = 0;
@@ -307,6 +339,7 @@ unsigned grid_for(const void* kernel, int64_t work_blocks, int quarter_blocks = 
 template <int RC, int MC, int U, bool CHECK, int OUT, int TPB = kThreads>
 __global__ void __launch_bounds__(TPB) k_fused(const __grid_constant__ FusedArgs a)
 {
+    pdl_enter();
     const int R = RC > 0 ? RC : a.R;
     const int M = MC > 0 ? MC : a.M;
     constexpr int kU = TPB * kVec;             // elements per block per unit
@@ -398,9 +431,11 @@ constexpr int fused_quarter_blocks()
 
 // A vector too short to give every resident block of the full-size tiling a
 // tile (fewer than one wave) leaves SMs idle, and its step is bound by
-// latency, not bandwidth: it takes tiles of one unit of kSmallThreads
-// threads instead, spread over more SMs.
-constexpr int kSmallThreads = 128;
+// latency, not bandwidth: it takes tiles of one unit instead, spread over
+// twice the blocks.  On GB300 the tiny 65,536-element workload then runs
+// 4.1 us a step back to back (6.2 with two-unit tiles); 64- and 128-thread
+// blocks measured the same.
+constexpr int kSmallThreads = 256;
 constexpr int kSmallUnits = 1;
 
 template <int RC, int MC, bool CHECK, int OUT = 0>
@@ -416,12 +451,10 @@ cudaError_t launch_fused_t(const FusedArgs& a, cudaStream_t st)
         const void* ks = reinterpret_cast<const void*>(&k_fused<RC, MC, US, CHECK, OUT, TS>);
         const int64_t small_tiles = (a.n + TS * kVec * US - 1) / (TS * kVec * US);
         const unsigned grid = grid_for(ks, small_tiles, 0, TS);
-        k_fused<RC, MC, US, CHECK, OUT, TS><<<grid, TS, 0, st>>>(a);
-        return cudaGetLastError();
+        return launch_pdl(k_fused<RC, MC, US, CHECK, OUT, TS>, dim3(grid), TS, st, a);
     }
     const unsigned grid = grid_for(k, tiles, fused_quarter_blocks<RC, MC, OUT>());
-    k_fused<RC, MC, U, CHECK, OUT><<<grid, kThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_fused<RC, MC, U, CHECK, OUT>, dim3(grid), kThreads, st, a);
 }
 
 template <bool CHECK, int OUT>
@@ -467,6 +500,7 @@ __device__ __forceinline__ int64_t shard_len(int64_t n, int64_t S, int r)
 template <int RC, int MC, bool CHECK>
 __global__ void __launch_bounds__(kThreads) k_rs_avg(const __grid_constant__ StagedArgs a)
 {
+    pdl_enter();
     const int R = RC > 0 ? RC : a.R;
     const int M = MC > 0 ? MC : a.M;
     const int r = blockIdx.y;
@@ -524,23 +558,29 @@ __global__ void __launch_bounds__(kThreads) k_rs_avg(const __grid_constant__ Sta
 
 __global__ void __launch_bounds__(kThreads) k_adamw(const __grid_constant__ StagedArgs a)
 {
+    pdl_enter();
     const int r = blockIdx.y;
     const int64_t lo = (int64_t)r * a.S, len = shard_len(a.n, a.S, r);
     const int64_t nvec = len / kVec;
     for (int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x; q < nvec;
          q += (int64_t)gridDim.x * kThreads) {
         const int64_t e = lo + q * kVec;
-        float4 g;
+        // every load issued before the first use (the halves are combined
+        // only after the state loads are in flight)
+        uint2 l{}, h{};
+        float4 g{};
         if (a.g_lo) {
-            const uint2 l = ld_stream(a.g_lo + e), h = ld_stream(a.g_hi + e);
-            g = make_float4(__uint_as_float(__byte_perm(l.x, h.x, 0x5410)),
-                            __uint_as_float(__byte_perm(l.x, h.x, 0x7632)),
-                            __uint_as_float(__byte_perm(l.y, h.y, 0x5410)),
-                            __uint_as_float(__byte_perm(l.y, h.y, 0x7632)));
+            l = ld_stream(a.g_lo + e);
+            h = ld_stream(a.g_hi + e);
         } else {
             g = ld_stream(a.gs + e);
         }
         float4 w = ld_stream(a.W + e), m = ld_stream(a.m + e), v = ld_stream(a.v + e);
+        if (a.g_lo)
+            g = make_float4(__uint_as_float(__byte_perm(l.x, h.x, 0x5410)),
+                            __uint_as_float(__byte_perm(l.x, h.x, 0x7632)),
+                            __uint_as_float(__byte_perm(l.y, h.y, 0x5410)),
+                            __uint_as_float(__byte_perm(l.y, h.y, 0x7632)));
         adamw(a.s, g.x, w.x, m.x, v.x);
         adamw(a.s, g.y, w.y, m.y, v.y);
         adamw(a.s, g.z, w.z, m.z, v.z);
@@ -572,6 +612,7 @@ __global__ void __launch_bounds__(kThreads) k_ag_cast(const __grid_constant__ St
     // shard starts on a multiple of 4 elements only, so the vector loop
     // starts at the shard's first multiple of 8; the head before it and the
     // tail after the last full vector are done element by element.
+    pdl_enter();
     const int R = RC > 0 ? RC : a.R;
     const int r = blockIdx.y;
     const int64_t lo = (int64_t)r * a.S, len = shard_len(a.n, a.S, r);
@@ -629,8 +670,7 @@ cudaError_t launch_rs(const StagedArgs& a, cudaStream_t st)
     auto go = [&](const void* k, auto kern) {
         const int64_t per_rank = (int64_t)grid_for(k, work * a.R, 16) / a.R;    // never past one wave
         dim3 grid((unsigned)(per_rank < 1 ? 1 : per_rank), (unsigned)a.R);
-        kern<<<grid, kThreads, 0, st>>>(a);
-        return cudaGetLastError();
+        return launch_pdl(kern, grid, kThreads, st, a);
     };
 #define ZERO_CASE(r_, m_)                                                      \
     if (R == r_ && M == m_)                                                    \
@@ -648,8 +688,7 @@ cudaError_t launch_adamw(const StagedArgs& a, cudaStream_t st)
     const int64_t work = (a.S / kVec + kThreads - 1) / kThreads;
     const int64_t per_rank = (int64_t)grid_for(k, work * a.R) / a.R;    // never past one wave
     dim3 grid((unsigned)(per_rank < 1 ? 1 : per_rank), (unsigned)a.R);
-    k_adamw<<<grid, kThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_adamw, grid, kThreads, st, a);
 }
 
 constexpr int kAgVecs = 1;             // vectors of 8 elements per thread per iteration
@@ -662,8 +701,7 @@ cudaError_t launch_ag(const StagedArgs& a, cudaStream_t st)
         const int64_t per_rank =
             (int64_t)grid_for(k, work * a.R, kAgQuarterBlocks) / a.R;    // never past one wave
         dim3 grid((unsigned)(per_rank < 1 ? 1 : per_rank), (unsigned)a.R);
-        kern<<<grid, kThreads, 0, st>>>(a);
-        return cudaGetLastError();
+        return launch_pdl(kern, grid, kThreads, st, a);
     };
 #define ZERO_AG(r_) \
     return go(reinterpret_cast<const void*>(&k_ag_cast<r_, kAgVecs>), k_ag_cast<r_, kAgVecs>);
