@@ -282,6 +282,7 @@ def oracle_prepare(wl, n, threads=None):
 # the oracle function that defines each measured step (only the plain step
 # has a multithreaded form; the others run on one core)
 ORACLE_FN = {"fused": "oracle_dp_step_mt", "staged": "oracle_dp_step_mt",
+             "staged_grads": "oracle_dp_step_mt",
              "tma": "oracle_dp_step_mt", "clipped": "oracle_dp_step_clipped",
              "compressed": "oracle_dp_step_compressed", "onebit": "oracle_onebit_step",
              "zero3": "oracle_zero3_step"}
@@ -452,8 +453,9 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     wl = W.by_name(args.workload)
-    variant = {"staged": z.ZERO_VARIANT_STAGED, "tma": z.ZERO_VARIANT_FUSED_TMA}.get(
-        args.variant, z.ZERO_VARIANT_FUSED)
+    variant = {"staged": z.ZERO_VARIANT_STAGED, "staged_grads": z.ZERO_VARIANT_STAGED,
+               "tma": z.ZERO_VARIANT_FUSED_TMA}.get(args.variant, z.ZERO_VARIANT_FUSED)
+    staged_grads = args.variant == "staged_grads"
     clipped = args.variant == "clipped"
     zero3 = args.variant == "zero3"
     compressed = args.variant == "compressed"
@@ -463,7 +465,14 @@ def run_ours(args, rank, world, local_rank):
         wl = dataclasses.replace(wl, align=128)
     stream = torch.cuda.current_stream()
 
-    ds = H.DeviceState(wl, str(dev), staged_scratch=(variant == z.ZERO_VARIANT_STAGED))
+    ds = H.DeviceState(wl, str(dev), staged_scratch=(args.variant == "staged"))
+    if staged_grads:
+        # ZeRO-2 without scratch: the reduced gradient in gradient buffers 0 and 1
+        if not (wl.stage == 2 and wl.R * wl.M >= 2):
+            raise SystemExit("--variant staged_grads needs a ZeRO-2 workload with R*M >= 2")
+        ds.step = lambda t, variant=0, flags=0: z.zero_step(
+            ds.plan, ds.grads, ds.W, ds.m, ds.v, ds.params, ds.hp, t,
+            variant=z.ZERO_VARIANT_STAGED, scratch=None, flags=flags, dev_status=ds.status)
     if clipped:
         ds.step = lambda t, variant=0, flags=0: ds.step_clipped(t, args.max_norm, flags=flags)
     elif zero3:
@@ -565,6 +574,8 @@ def run_ours(args, rank, world, local_rank):
                            else f"k_comp ({args.codec}{', error feedback' if args.ef else ''})"
                            if compressed
                            else "k_onebit (1-bit Adam, frozen variance)" if onebit
+                           else "staged trio, reduced gradient in gradient buffers 0 and 1"
+                           if staged_grads
                            else {0: "k_fused", 1: "staged trio", 2: "k_fused_tma"}[variant]),
                 "algorithmic_bytes_per_launch": alg_bytes, "bytes_per_param": bpp}
 
@@ -684,6 +695,13 @@ def run_table(args):
     sampler.start()
     sampler.mark_start()
 
+    def run_step(ds, t, variant):
+        if variant == "in_grads":                    # staged, reduced gradient in buffers 0 and 1
+            z.zero_step(ds.plan, ds.grads, ds.W, ds.m, ds.v, ds.params, ds.hp, t,
+                        variant=z.ZERO_VARIANT_STAGED, scratch=None)
+        else:
+            ds.step(t, variant=variant)
+
     def timed(ds, variant, reps, cold=True):
         ts = []
         t = ds.wl.step
@@ -692,7 +710,7 @@ def run_table(args):
                 flush.fill_(k & 0xFF)                  # evict L2 (256 MB > 129 MB)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-            ds.step(t, variant=variant)
+            run_step(ds, t, variant)
             e1.record()
             torch.cuda.synchronize()
             t += 1
@@ -700,28 +718,65 @@ def run_table(args):
                 ts.append(e0.elapsed_time(e1))
         return float(np.median(ts))
 
+    def timed_small(ds, variant, reps, cold):
+        """A step of microseconds: every launch is enqueued behind a sleep
+        kernel, so the events time the GPU, not the host's launch calls.
+        Warm: reps steps back to back between one event pair, the mean per
+        step.  Cold: a flush, then an event pair around one step, reps
+        times; the mean of the spans (the event timer ticks about every
+        2 us, so a median would only pick a tick)."""
+        t = ds.wl.step
+        for _ in range(3):
+            run_step(ds, t, variant)
+            t += 1
+        torch.cuda.synchronize()
+        torch.cuda._sleep(200_000_000)                 # ~0.1 s: the host enqueues meanwhile
+        if not cold:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for k in range(reps):
+                run_step(ds, t + k, variant)
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / reps
+        ev = []
+        for k in range(reps):
+            flush.fill_(k & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run_step(ds, t + k, variant)
+            e1.record()
+            ev.append((e0, e1))
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in ev]))
+
     def bpp(wl, variant):
         return wl.bytes_per_param() if variant == 0 else 2 * wl.R * wl.M + 36 + 2 * wl.R
 
-    def measure(wl, label, reps, variants=(0, 1)):
+    def measure(wl, label, reps, variants=(0, 1, "in_grads")):
         ds = H.DeviceState(wl, staged_scratch=True)
         ds.fill_state_device()
         ds.fill_grads_device(wl.step)
         torch.cuda.synchronize()
         resident = bpp(wl, 1) * wl.N < 129e6
         for variant in variants:
+            if variant == "in_grads" and not (wl.stage == 2 and wl.R * wl.M >= 2):
+                continue
             # a workload that fits in L2 is timed twice: after a flush (cold
             # L2, the flush's dirty lines written back during the launch) and
             # back to back with its inputs resident (warm L2)
             for cold in ((True, False) if resident else (True,)):
-                ms = timed(ds, variant, reps, cold)
+                ms = timed_small(ds, variant, 200, cold) if resident else timed(ds, variant, reps)
                 gbs = bpp(wl, variant) * wl.N / (ms / 1e3) / 1e9
                 row = {"workload": label, "R": wl.R, "M": wl.M, "N": wl.N,
-                       "variant": "fused" if variant == 0 else "staged", "ms": round(ms, 4),
+                       "variant": {0: "fused", 1: "staged"}.get(
+                           variant, "staged, reduced gradient in gradient buffers 0 and 1"),
+                       "ms": round(ms, 4),
                        "params_per_s": wl.N / (ms / 1e3), "bytes_per_param": bpp(wl, variant),
                        "GB_s": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
-                       "l2": ("cold (256 MB flush before each launch)" if cold
-                              else "warm (inputs resident, launches back to back)")
+                       "l2": ("cold: 256 MB flush before each launch; mean of 200 event "
+                              "spans around one launch (an empty pair spans ~2.1 us)" if cold
+                              else "warm: inputs resident, 200 launches back to back, mean")
                        if resident else "inputs far larger than L2; flushed before each launch"}
                 rows.append(row)
                 print(json.dumps(row), flush=True)
@@ -1204,8 +1259,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama-3.2-1b")
-    ap.add_argument("--variant", choices=["fused", "staged", "clipped", "tma", "zero3",
-                                          "compressed", "onebit"], default="fused")
+    ap.add_argument("--variant", choices=["fused", "staged", "staged_grads", "clipped", "tma",
+                                          "zero3", "compressed", "onebit"], default="fused",
+                    help="staged_grads: the staged step on a ZeRO-2 plan without scratch")
     ap.add_argument("--codec", choices=["fp16", "int8", "sign"], default="int8",
                     help="codec for --variant compressed")
     ap.add_argument("--ef", action="store_true", help="error feedback for --variant compressed")
