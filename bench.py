@@ -466,13 +466,24 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     ds = H.DeviceState(wl, str(dev), staged_scratch=(args.variant == "staged"))
+    restore = None
     if staged_grads:
-        # ZeRO-2 without scratch: the reduced gradient in gradient buffers 0 and 1
+        # ZeRO-2 without scratch: the reduced gradient in gradient buffers 0 and 1.
+        # The step leaves those two buffers unspecified; in training the next
+        # backward writes them again.  Here a copy of their inputs is put back
+        # before every step, outside the step's own event pair (the timed steps
+        # are then summed from those pairs): steps fed the previous step's
+        # leftovers would compute on arbitrary bits, NaN and Inf among them.
         if not (wl.stage == 2 and wl.R * wl.M >= 2):
             raise SystemExit("--variant staged_grads needs a ZeRO-2 workload with R*M >= 2")
         ds.step = lambda t, variant=0, flags=0: z.zero_step(
             ds.plan, ds.grads, ds.W, ds.m, ds.v, ds.params, ds.hp, t,
             variant=z.ZERO_VARIANT_STAGED, scratch=None, flags=flags, dev_status=ds.status)
+        kept = None
+
+        def restore():
+            for g, c in zip(ds.grads[:2], kept):
+                g.copy_(c)
     if clipped:
         ds.step = lambda t, variant=0, flags=0: ds.step_clipped(t, args.max_norm, flags=flags)
     elif zero3:
@@ -502,6 +513,8 @@ def run_ours(args, rank, world, local_rank):
         ds.step(t, variant=variant)
         t += 1
     ds.fill_grads_device(wl.step)
+    if restore is not None:
+        kept = [g.clone() for g in ds.grads[:2]]
     torch.cuda.synchronize()
 
     def barrier():
@@ -511,6 +524,8 @@ def run_ours(args, rank, world, local_rank):
 
     step_t = wl.step
     for _ in range(args.warmup):
+        if restore is not None:
+            restore()
         ds.step(step_t, variant=variant)
         step_t += 1
     torch.cuda.synchronize()
@@ -525,6 +540,8 @@ def run_ours(args, rank, world, local_rank):
     sampler.mark_start()
     e_all0.record(stream)
     for k in range(args.steps):
+        if restore is not None:
+            restore()
         ev[k][0].record(stream)
         ds.step(step_t, variant=variant)
         ev[k][1].record(stream)
@@ -536,6 +553,8 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop()
     total_ms = e_all0.elapsed_time(e_all1)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if restore is not None:
+        total_ms = float(sum(launch_ms))          # the steps alone, without the restores
 
     total_ms = max_over_ranks(total_ms, dev)
 
@@ -702,10 +721,18 @@ def run_table(args):
         else:
             ds.step(t, variant=variant)
 
+    def before_step(ds, variant):
+        # the in-buffer mode leaves gradient buffers 0 and 1 unspecified: put
+        # their inputs back before each step, outside its event pair
+        if variant == "in_grads":
+            for g, c in zip(ds.grads[:2], ds.kept_grads):
+                g.copy_(c)
+
     def timed(ds, variant, reps, cold=True):
         ts = []
         t = ds.wl.step
         for k in range(3 + reps):
+            before_step(ds, variant)
             if cold:
                 flush.fill_(k & 0xFF)                  # evict L2 (256 MB > 129 MB)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -757,6 +784,7 @@ def run_table(args):
         ds = H.DeviceState(wl, staged_scratch=True)
         ds.fill_state_device()
         ds.fill_grads_device(wl.step)
+        ds.kept_grads = [g.clone() for g in ds.grads[:2]] if "in_grads" in variants else []
         torch.cuda.synchronize()
         resident = bpp(wl, 1) * wl.N < 129e6
         for variant in variants:

@@ -195,8 +195,10 @@ int32_t zero_plan_owner(const zero_plan_t* plan, int64_t i);
  *               R*M >= 2 the staged variant accepts scratch = NULL and then
  *               keeps the reduced gradient in rank_grads[0] and
  *               rank_grads[1] (the low and high 16 bits of each element's
- *               fp32 value), whose contents are unspecified afterwards; those
- *               two buffers are then outputs and may alias no other buffer.
+ *               fp32 value), whose contents are unspecified afterwards (the
+ *               next backward must write them again: read as gradients they
+ *               are arbitrary bits); those two buffers are then outputs and
+ *               may alias no other buffer.
  *   flags       0, ZERO_FLAG_CHECK_FINITE, and for the TMA variant
  *               ZERO_FLAG_DEBUG_EXPIRE_WAITS (test only).
  *   dev_status  optional device int32 the kernels OR ZERO_DEV_* bits into.

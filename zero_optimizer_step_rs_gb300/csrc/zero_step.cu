@@ -556,6 +556,9 @@ __global__ void __launch_bounds__(kThreads) k_rs_avg(const __grid_constant__ Sta
     report_nonfinite<CHECK>(bad, a.status);
 }
 
+// SPLIT: the gradient comes as low and high halves from gradient buffers 0
+// and 1 (ZeRO-2 without scratch) instead of from the fp32 scratch
+template <bool SPLIT>
 __global__ void __launch_bounds__(kThreads) k_adamw(const __grid_constant__ StagedArgs a)
 {
     pdl_enter();
@@ -565,22 +568,17 @@ __global__ void __launch_bounds__(kThreads) k_adamw(const __grid_constant__ Stag
     for (int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x; q < nvec;
          q += (int64_t)gridDim.x * kThreads) {
         const int64_t e = lo + q * kVec;
-        // every load issued before the first use (the halves are combined
-        // only after the state loads are in flight)
-        uint2 l{}, h{};
-        float4 g{};
-        if (a.g_lo) {
-            l = ld_stream(a.g_lo + e);
-            h = ld_stream(a.g_hi + e);
-        } else {
-            g = ld_stream(a.gs + e);
-        }
-        float4 w = ld_stream(a.W + e), m = ld_stream(a.m + e), v = ld_stream(a.v + e);
-        if (a.g_lo)
+        float4 g;
+        if constexpr (SPLIT) {
+            const uint2 l = ld_stream(a.g_lo + e), h = ld_stream(a.g_hi + e);
             g = make_float4(__uint_as_float(__byte_perm(l.x, h.x, 0x5410)),
                             __uint_as_float(__byte_perm(l.x, h.x, 0x7632)),
                             __uint_as_float(__byte_perm(l.y, h.y, 0x5410)),
                             __uint_as_float(__byte_perm(l.y, h.y, 0x7632)));
+        } else {
+            g = ld_stream(a.gs + e);
+        }
+        float4 w = ld_stream(a.W + e), m = ld_stream(a.m + e), v = ld_stream(a.v + e);
         adamw(a.s, g.x, w.x, m.x, v.x);
         adamw(a.s, g.y, w.y, m.y, v.y);
         adamw(a.s, g.z, w.z, m.z, v.z);
@@ -592,9 +590,11 @@ __global__ void __launch_bounds__(kThreads) k_adamw(const __grid_constant__ Stag
     if (blockIdx.x == 0) {
         for (int64_t i = lo + nvec * kVec + threadIdx.x; i < lo + len; i += kThreads) {
             float w = a.W[i], m = a.m[i], v = a.v[i];
-            const float g = a.g_lo ? __uint_as_float((uint32_t)a.g_lo[i] |
-                                                     ((uint32_t)a.g_hi[i] << 16))
-                                   : a.gs[i];
+            float g;
+            if constexpr (SPLIT)
+                g = __uint_as_float((uint32_t)a.g_lo[i] | ((uint32_t)a.g_hi[i] << 16));
+            else
+                g = a.gs[i];
             adamw(a.s, g, w, m, v);
             a.W[i] = w;
             a.m[i] = m;
@@ -684,11 +684,14 @@ cudaError_t launch_rs(const StagedArgs& a, cudaStream_t st)
 
 cudaError_t launch_adamw(const StagedArgs& a, cudaStream_t st)
 {
-    const void* k = reinterpret_cast<const void*>(&k_adamw);
     const int64_t work = (a.S / kVec + kThreads - 1) / kThreads;
-    const int64_t per_rank = (int64_t)grid_for(k, work * a.R) / a.R;    // never past one wave
-    dim3 grid((unsigned)(per_rank < 1 ? 1 : per_rank), (unsigned)a.R);
-    return launch_pdl(k_adamw, grid, kThreads, st, a);
+    auto go = [&](auto kern) {
+        const void* k = reinterpret_cast<const void*>(kern);
+        const int64_t per_rank = (int64_t)grid_for(k, work * a.R) / a.R;    // never past one wave
+        dim3 grid((unsigned)(per_rank < 1 ? 1 : per_rank), (unsigned)a.R);
+        return launch_pdl(kern, grid, kThreads, st, a);
+    };
+    return a.g_lo ? go(k_adamw<true>) : go(k_adamw<false>);
 }
 
 constexpr int kAgVecs = 1;             // vectors of 8 elements per thread per iteration
