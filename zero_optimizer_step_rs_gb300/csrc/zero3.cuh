@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kThreads) k_gather_units(const __grid_constant
     for (int i = threadIdx.x; i <= a.n_units; i += kThreads) chunk0[i] = a.chunk0[i];
     __syncthreads();
     int u = 0;
-    for (uint32_t c = blockIdx.x; c < a.total_chunks; c += gridDim.x) {
+    for (int64_t c = blockIdx.x; c < (int64_t)a.total_chunks; c += gridDim.x) {
         if (c >= chunk0[u + 1]) {                   // past the unit: last unit whose first chunk <= c
             int ulo = u + 1, uhi = a.n_units - 1;
             while (ulo < uhi) {
