@@ -269,7 +269,10 @@ zero_status zero_ag_cast(const zero_plan_t* plan, const float* master,
  * replicas untouched) and ZERO_DEV_SKIPPED is set.
  *   max_norm   > 0 and finite.
  *   scratch    device, at least zero_clip_scratch_bytes(plan) bytes: the
- *              fp32 averaged gradients, the tree levels and a control record.
+ *              fp32 averaged gradients, the tree levels, a control record and
+ *              the tree's arrival counters (any contents on entry).
+ * Three launches: the reduce-scatter with the first tree level, the rest of
+ * the tree with the coefficient, the update with the all-gather.
  *   dev_sumsq  optional device double: receives the squared norm.
  * Traffic: 2RM + 4 bytes/param (reduce-scatter, gradient stash) plus
  * 4 + 24 + 2R (update and all-gather) plus 4/2048 for the tree.
