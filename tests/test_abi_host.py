@@ -569,3 +569,45 @@ def test_product_and_oracle_share_no_code():
             assert not re.search(r"^\s*(import|from)\s+zero_optimizer_step_rs_gb300\b",
                                  src, re.M), f
             assert "libzero_step" not in src, f
+
+
+def test_header_is_plain_c_and_a_c_program_links_the_library(tmp_path):
+    """include/zero_step.h compiles as strict C99, and a C program linked
+    against libzero_step.so calls its host-only entry points: a plan with the
+    pages' exercise-1 accounting, status strings, and the argument errors of
+    the device-status call (returned before any CUDA call)."""
+    import shutil
+    import subprocess
+    if not shutil.which("gcc"):
+        pytest.skip("gcc needed")
+    src = tmp_path / "abi.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "zero_step.h"
+int main(void)
+{
+    const int64_t n[1] = {7000000000LL};
+    zero_plan_t* p = NULL;
+    if (zero_plan_create(n, 1, 8, 1, 1, 0, &p) != ZERO_OK) return 1;
+    /* 7B parameters on 8 cards, ZeRO-1: 2+2 bytes replicated, 12 sharded */
+    if (p->bytes_per_rank_z1 != 4 * p->N + 12 * p->S) return 2;
+    zero_plan_destroy(p);
+    if (strcmp(zero_status_string(ZERO_ERR_DEVICE_TIMEOUT), "unknown status") == 0) return 3;
+    int32_t word = -1;
+    if (zero_get_device_status(NULL, NULL, &word) != ZERO_ERR_NULL) return 4;
+    if (zero_get_device_status((const int32_t*)(uintptr_t)0x1002, NULL, &word) != ZERO_ERR_ALIGN) return 5;
+    if (word != -1) return 6;
+    if (zero3_gather_units(NULL, NULL, NULL, 0, NULL) != ZERO_ERR_NULL) return 7;
+    printf("abi ok %d\n", zero_abi_version());
+    return 0;
+}
+''')
+    exe = tmp_path / "abi"
+    libdir = os.path.join(ROOT, "zero_optimizer_step_rs_gb300")
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                    "-L", libdir, "-lzero_step", f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, (out.returncode, out.stderr)
+    assert out.stdout.strip() == "abi ok 1"
