@@ -285,7 +285,7 @@ ORACLE_FN = {"fused": "oracle_dp_step_mt", "staged": "oracle_dp_step_mt",
              "staged_grads": "oracle_dp_step_mt",
              "tma": "oracle_dp_step_mt", "clipped": "oracle_dp_step_clipped",
              "compressed": "oracle_dp_step_compressed", "onebit": "oracle_onebit_step",
-             "zero3": "oracle_zero3_step"}
+             "zero3": "oracle_zero3_step", "zero3_gather_units": "oracle_zero3_gather"}
 
 
 def oracle_step_opts(args=None) -> dict:
@@ -311,6 +311,16 @@ def oracle_pass(wl, ctx, variant="fused", codec="int8", ef=False, max_norm=1.0):
     n, R, M, t = ctx["n"], wl.R, wl.M, wl.step
     hp = oracle.hparams(**wl.hparams())
     G, P = ctx["G"], ctx["P"]
+    if variant == "zero3_gather_units":
+        # every tensor of the sample (the workload's first n params) gathered
+        # from the padded shard buffer, one unit at a time
+        S = oracle.shard_len(n, R)
+        Ps = np.zeros(R * S, np.uint16)
+        cuts = [int(c) for c in wl.offsets if c < n] + [n]
+        t0 = time.perf_counter()
+        for lo, hi in zip(cuts[:-1], cuts[1:]):
+            oracle.zero3_gather(Ps, n, R, S, lo, hi, 0)
+        return time.perf_counter() - t0
     if variant == "zero3":
         S = oracle.shard_len(n, R)
         Wc, mc, vc = (np.zeros(R * S, np.float32) for _ in range(3))
@@ -453,11 +463,14 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     wl = W.by_name(args.workload)
+    if getattr(args, "scale", 0):
+        wl = wl.scaled(args.scale)
     variant = {"staged": z.ZERO_VARIANT_STAGED, "staged_grads": z.ZERO_VARIANT_STAGED,
                "tma": z.ZERO_VARIANT_FUSED_TMA}.get(args.variant, z.ZERO_VARIANT_FUSED)
     staged_grads = args.variant == "staged_grads"
     clipped = args.variant == "clipped"
     zero3 = args.variant == "zero3"
+    gather_units = args.variant == "zero3_gather_units"
     compressed = args.variant == "compressed"
     onebit = args.variant == "onebit"
     if onebit:                             # 1-bit Adam wants shards on the 128-element block grid
@@ -486,6 +499,17 @@ def run_ours(args, rank, world, local_rank):
                 g.copy_(c)
     if clipped:
         ds.step = lambda t, variant=0, flags=0: ds.step_clipped(t, args.max_norm, flags=flags)
+    elif gather_units:
+        # the whole parameter set gathered per tensor, one zero3_gather_units
+        # launch over the table of its units; the shards hold the result of a
+        # ZeRO-3 step taken before the timed region
+        shards = torch.empty(ds.padded, dtype=torch.bfloat16, device=dev)
+        offs = [int(x) for x in wl.offsets]
+        pairs = list(zip(offs[:-1], offs[1:]))
+        unit_outs = [torch.empty(hi - lo, dtype=torch.bfloat16, device=dev) for lo, hi in pairs]
+        table = z.gather_unit_table([(lo, hi, o) for (lo, hi), o in zip(pairs, unit_outs)])
+        ds.step = lambda t, variant=0, flags=0: z.zero3_gather_units(ds.plan, shards, table,
+                                                                     len(pairs))
     elif zero3:
         shards = torch.empty(ds.padded, dtype=torch.bfloat16, device=dev)
         ds.step = lambda t, variant=0, flags=0: z.zero3_step(
@@ -515,6 +539,8 @@ def run_ours(args, rank, world, local_rank):
     ds.fill_grads_device(wl.step)
     if restore is not None:
         kept = [g.clone() for g in ds.grads[:2]]
+    if gather_units:
+        z.zero3_step(ds.plan, ds.grads, ds.W, ds.m, ds.v, shards, ds.hp, wl.step)
     torch.cuda.synchronize()
 
     def barrier():
@@ -563,6 +589,8 @@ def run_ours(args, rank, world, local_rank):
     value = N * args.steps * world / (total_ms / 1e3)
     if clipped:
         bpp = 2 * wl.R * wl.M + 4 + 4 + 24 + 2 * wl.R      # stash written and read back
+    elif gather_units:
+        bpp = 4                                             # 2 read from the shards, 2 written
     elif zero3:
         bpp = 2 * wl.R * wl.M + 24 + 2
     elif compressed:
@@ -589,6 +617,8 @@ def run_ours(args, rank, world, local_rank):
                 "unit": "GB/s", "frac": round(achieved_gbs / peak, 4), "traffic": traffic,
                 "peak_source": peak_src,
                 "kernel": ("clipped step (k_rs_norm, k_norm_tree, k_adamw_ag)" if clipped
+                           else f"k_gather_units ({len(pairs)} per-tensor units, one launch)"
+                           if gather_units
                            else "k_fused (ZeRO-3 output)" if zero3
                            else f"k_comp ({args.codec}{', error feedback' if args.ef else ''})"
                            if compressed
@@ -669,6 +699,7 @@ def run_ours(args, rank, world, local_rank):
                    **({"max_norm": args.max_norm} if clipped else {}),
                    **({"codec": args.codec, "error_feedback": args.ef} if compressed else {}),
                    **({"freeze_step": max(1, wl.step - 1), "align": 128} if onebit else {}),
+                   **({"units": len(pairs)} if gather_units else {}),
                    "l2": "inputs (%.1f GB/step) far larger than the 129 MB L2; no flush"
                          % (alg_bytes / 1e9),
                    "parallelism": f"{world} independent replica(s) of an R={wl.R} "
@@ -680,7 +711,7 @@ def run_ours(args, rank, world, local_rank):
         # the emulated step does one reduce-scatter and one all-gather of
         # 2N-byte bf16 messages (micro-batches summed locally; ZeRO-3 has no
         # all-gather in the step), timed by the whole step
-        "emulated_busbw_gbs": round((1 if zero3 else 2) * 2 * N * (wl.R - 1) / wl.R
+        "emulated_busbw_gbs": round((1 if zero3 or gather_units else 2) * 2 * N * (wl.R - 1) / wl.R
                                     / (ms_per_step / 1e3) / 1e9, 1),
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -1248,6 +1279,8 @@ def run_reference(args):
     workload."""
     from zgen import workloads as W
     wl = W.by_name(args.workload)
+    if getattr(args, "scale", 0):
+        wl = wl.scaled(args.scale)
     t0 = time.time()
     sample = min(wl.N, 1 << 22)
     ctx = oracle_prepare(wl, sample)
@@ -1288,8 +1321,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama-3.2-1b")
     ap.add_argument("--variant", choices=["fused", "staged", "staged_grads", "clipped", "tma",
-                                          "zero3", "compressed", "onebit"], default="fused",
-                    help="staged_grads: the staged step on a ZeRO-2 plan without scratch")
+                                          "zero3", "zero3_gather_units", "compressed", "onebit"],
+                    default="fused",
+                    help="staged_grads: the staged step on a ZeRO-2 plan without scratch; "
+                         "zero3_gather_units: the ZeRO-3 all-gather of every tensor, one launch")
+    ap.add_argument("--scale", type=int, default=0,
+                    help="scale the workload's tensors down to about this many params")
     ap.add_argument("--codec", choices=["fp16", "int8", "sign"], default="int8",
                     help="codec for --variant compressed")
     ap.add_argument("--ef", action="store_true", help="error feedback for --variant compressed")

@@ -118,6 +118,7 @@ def test_sampler_polls_nvml_when_the_library_loads(tmp_path, monkeypatch):
 
 @pytest.mark.parametrize("variant,extra", [
     ("fused", {}), ("clipped", {"max_norm": 0.5}), ("zero3", {}), ("onebit", {}),
+    ("zero3_gather_units", {}), ("staged_grads", {}),
     ("compressed", {"codec": "sign", "ef": True}), ("compressed", {"codec": "int8"})])
 def test_reference_arm_times_the_oracle_of_the_measured_step(variant, extra):
     """bench.py --impl reference (and the cpu_baseline of a --variant line)
