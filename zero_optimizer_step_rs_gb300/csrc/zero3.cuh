@@ -11,6 +11,9 @@
 // (the ranks that need the unit), on demand before its use.
 //
 // k_gather copies 8 elements (16 bytes) per thread to every destination.
+// The ZeRO-3 kernels are launched with programmatic dependent launch, like
+// the step's: a schedule of many unit launches (gathers and reduce-scatters
+// in the backward's order) has its launch gaps hidden.
 // A unit can start at any element, so the source window of a destination
 // vector is shifted by SHIFT = lo mod 8 elements: the thread loads the two
 // aligned 16-byte source vectors that cover it and funnel-shifts them into
@@ -50,6 +53,7 @@ __device__ __forceinline__ uint4 realign8(uint4 A, uint4 B)
 template <int SHIFT>
 __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ GatherArgs a)
 {
+    pdl_enter();
     const int64_t base = a.lo - SHIFT;            // 8-element (16-byte) aligned
     const int64_t nvec = a.len / 8;
     constexpr int64_t window = SHIFT ? 16 : 8;
@@ -88,8 +92,7 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t st)
 {
     const int64_t work = (a.len / 8 + kThreads - 1) / kThreads;
     auto go = [&](const void* k, auto kern) {
-        kern<<<grid_for(k, work < 1 ? 1 : work), kThreads, 0, st>>>(a);
-        return cudaGetLastError();
+        return launch_pdl(kern, dim3(grid_for(k, work < 1 ? 1 : work)), kThreads, st, a);
     };
     switch ((int)(a.lo & 7)) {
     case 0: return go(reinterpret_cast<const void*>(&k_gather<0>), k_gather<0>);
@@ -145,6 +148,7 @@ __device__ __forceinline__ uint4 realign_rt(int s, uint4 A, uint4 B)
 __global__ void __launch_bounds__(kThreads) k_gather_units(const __grid_constant__ GatherUnitsArgs a)
 {
     __shared__ uint32_t chunk0[ZERO_MAX_GATHER_UNITS + 1];
+    pdl_enter();
     for (int i = threadIdx.x; i <= a.n_units; i += kThreads) chunk0[i] = a.chunk0[i];
     __syncthreads();
     int u = 0;
@@ -272,9 +276,8 @@ extern "C" zero_status zero3_gather_units(const zero_plan_t* plan, const uint16_
     a.n_units = n_units;
     a.total_chunks = (uint32_t)chunks;
     const void* k = reinterpret_cast<const void*>(&k_gather_units);
-    k_gather_units<<<grid_for(k, (int64_t)chunks), kThreads, 0,
-                     static_cast<cudaStream_t>(stream)>>>(a);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(launch_pdl(k_gather_units, dim3(grid_for(k, (int64_t)chunks)), kThreads,
+                                  static_cast<cudaStream_t>(stream), a));
 }
 
 // ============================================= ZeRO-3, unit by unit (FSDP) ==
@@ -312,6 +315,7 @@ StepScalars divisor_scalars(int R, int M)
 template <int RC, int MC, bool CHECK>
 __global__ void __launch_bounds__(kThreads) k_rs_unit(const __grid_constant__ UnitArgs a)
 {
+    pdl_enter();
     const int R = RC > 0 ? RC : a.R;
     const int M = MC > 0 ? MC : a.M;
     const int64_t nvec = a.len / kVec;
@@ -351,8 +355,7 @@ cudaError_t launch_rs_unit(const UnitArgs& a, cudaStream_t st)
 {
     const int64_t work = (a.len / kVec + kThreads - 1) / kThreads;
     auto go = [&](const void* k, auto kern) {
-        kern<<<grid_for(k, work < 1 ? 1 : work), kThreads, 0, st>>>(a);
-        return cudaGetLastError();
+        return launch_pdl(kern, dim3(grid_for(k, work < 1 ? 1 : work)), kThreads, st, a);
     };
 #define ZERO_CASE(r_, m_)                                                      \
     if (a.R == r_ && a.M == m_)                                                \
@@ -376,6 +379,7 @@ struct Z3UpdateArgs {
 
 __global__ void __launch_bounds__(kThreads) k_z3_update(const __grid_constant__ Z3UpdateArgs a)
 {
+    pdl_enter();
     const int64_t nvec = a.n / kVec;
     for (int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x; q < nvec;
          q += (int64_t)gridDim.x * kThreads) {
@@ -468,6 +472,6 @@ extern "C" zero_status zero3_update(const zero_plan_t* plan, const float* grad_s
     // 3 blocks per SM of the 5 that fit: 0.955 -> 0.98 of the copy peak on
     // the 1B-shaped workload (grid-size sweep)
     const unsigned grid = grid_for(k, work < 1 ? 1 : work, 12);
-    k_z3_update<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(launch_pdl(k_z3_update, dim3(grid), kThreads,
+                                  static_cast<cudaStream_t>(stream), a));
 }
