@@ -311,6 +311,7 @@ __device__ __forceinline__ void comp_ranks_generic(const CompArgs& a, int R, int
 template <int RC, int MC, int KIND, bool EF>
 __global__ void __launch_bounds__(kThreads) k_comp(const __grid_constant__ CompArgs a)
 {
+    pdl_enter();
     const int R = RC > 0 ? RC : a.R;
     const int M = MC > 0 ? MC : a.M;
     const int lane = threadIdx.x & 31;
@@ -435,8 +436,8 @@ cudaError_t launch_comp_t(const CompArgs& a, cudaStream_t st)
     // 0.98 -> 1.0 on the GPT-2-shaped one (grid-size sweep); every other
     // codec measured fastest with all resident blocks
     constexpr int quarters = (KIND == ZERO_COMP_SIGN && !EF) ? 14 : 0;
-    k_comp<RC, MC, KIND, EF><<<grid_for(k, work < 1 ? 1 : work, quarters), kThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_comp<RC, MC, KIND, EF>, dim3(grid_for(k, work < 1 ? 1 : work, quarters)),
+                      kThreads, st, a);
 }
 
 template <int KIND, bool EF>

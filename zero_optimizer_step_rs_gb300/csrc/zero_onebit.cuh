@@ -91,6 +91,7 @@ __device__ __forceinline__ float onebit_update(const OneBitScalars& s, float w, 
 template <int RC, int MC>
 __global__ void __launch_bounds__(kThreads) k_onebit(const __grid_constant__ OneBitArgs a)
 {
+    pdl_enter();
     const int R = RC > 0 ? RC : a.R;
     const int M = MC > 0 ? MC : a.M;
     const int lane = threadIdx.x & 31;
@@ -275,8 +276,7 @@ cudaError_t launch_onebit_t(const OneBitArgs& a, cudaStream_t st)
     const void* k = reinterpret_cast<const void*>(&k_onebit<RC, MC>);
     const int64_t blocks = (a.n + kCompBlock - 1) / kCompBlock;   // one warp each
     const int64_t work = (blocks + kThreads / 32 - 1) / (kThreads / 32);
-    k_onebit<RC, MC><<<grid_for(k, work < 1 ? 1 : work), kThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_onebit<RC, MC>, dim3(grid_for(k, work < 1 ? 1 : work)), kThreads, st, a);
 }
 
 cudaError_t launch_onebit(const OneBitArgs& a, cudaStream_t st)
