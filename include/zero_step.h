@@ -220,7 +220,8 @@ zero_status zero_step(const zero_plan_t* plan, const uint16_t* const* rank_grads
  *               aligned).  It is read, not cleared: zero it before the next
  *               steps that should report afresh.
  *   stream      the stream the steps ran on: the call enqueues the read of
- *               the word on it and waits for the stream to finish.
+ *               the word on it and waits for the stream to finish (so it is
+ *               a host-side call, not for a stream being captured).
  *   out         optional host int32: receives the word (ZERO_DEV_* bits).
  * Returns ZERO_ERR_DEVICE_TIMEOUT when ZERO_DEV_TIMEOUT is set (with or
  * without ZERO_DEV_DRAIN_FAILED), else ZERO_ERR_NONFINITE when
