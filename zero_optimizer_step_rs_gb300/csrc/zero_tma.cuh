@@ -87,6 +87,7 @@ TmaLayout tma_layout(int RM)
 __global__ void __launch_bounds__(kThreads) k_fused_tma(const __grid_constant__ FusedArgs a,
                                                         uint32_t wait_limit, int32_t check)
 {
+    pdl_enter();
     const int R = a.R, M = a.M, RM = R * M;
     constexpr uint32_t GB = kTmaTile * 2, SB = kTmaTile * 4;
     const uint32_t stage_bytes = (uint32_t)RM * GB + 3 * SB;
@@ -227,9 +228,19 @@ cudaError_t launch_fused_tma(const FusedArgs& a, bool expire_waits, bool check, 
     int64_t grid = (int64_t)device_sms(dev) * per_sm;
     if (grid > tiles) grid = tiles;
     if (grid < 1) grid = 1;
-    k_fused_tma<<<(unsigned)grid, kThreads, L.smem_bytes, st>>>(a, expire_waits ? 0u : kWaitLimit,
-                                                               check ? 1 : 0);
-    return cudaGetLastError();
+    // programmatic dependent launch, as the other step kernels (dynamic shared memory here)
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L.smem_bytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_fused_tma, a, expire_waits ? 0u : kWaitLimit,
+                              (int32_t)(check ? 1 : 0));
 }
 
 }  // namespace
