@@ -9,8 +9,9 @@ oracle runs the same steps on that chunk on all host cores (the step is
 elementwise, so a chunk's result is the whole run's at those indices), and
 the device's W, m, v and replica 0 over the same chunk must match bit for
 bit.  Every replica must equal replica 0 and the state pad must be
-untouched, checked on the device over the whole vector.  The flat sweep
-points keep a sampled comparison (random indices plus every shard and tensor
+untouched, checked on the device over the whole vector.  The TMA-staged
+variant is compared on every element of the GPT-2 and 1B workloads too.  The
+flat sweep points keep a sampled comparison (random indices plus every shard and tensor
 boundary and the last partial tile).
 """
 import os
@@ -164,11 +165,15 @@ def test_flat_sweep_points_sampled(R, S):
 
 
 @pytest.mark.parametrize("name", ["gpt2-small", "llama-3.2-1b"])
-def test_full_size_sampled_tma_variant(name):
-    """The TMA-bulk-staged variant (R*M <= 16) at full size, sampled against
-    the oracle like the sweep points."""
+def test_full_size_every_element_tma_variant(name):
+    """The TMA-bulk-staged variant (R*M <= 16) at full size, every element
+    against the oracle like the fused and staged steps."""
     wl = W.ALL[name]()
-    res, replicas_equal, pad_clean, status, k = _run_sampled(wl, z.ZERO_VARIANT_FUSED_TMA)
+    ds, steps = _device_run(wl, z.ZERO_VARIANT_FUSED_TMA)
+    replicas_equal, pad_clean, status = _everywhere(ds)
+    assert replicas_equal and pad_clean and status == 0, (replicas_equal, pad_clean, status)
+    res = _whole_vector_mismatches(wl, ds, steps)
+    del ds
+    torch.cuda.empty_cache()
     bad = {key: v for key, v in res.items() if v}
-    assert not bad, (name, bad, k)
-    assert replicas_equal and pad_clean and status == 0
+    assert not bad, (name, bad)
