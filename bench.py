@@ -616,7 +616,7 @@ def run_ours(args, rank, world, local_rank):
     roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved_gbs / peak, 4), "traffic": traffic,
                 "peak_source": peak_src,
-                "kernel": ("clipped step (k_rs_norm, k_norm_tree, k_adamw_ag)" if clipped
+                "kernel": ("clipped step (k_rs_norm, k_adamw_ag)" if clipped
                            else f"k_gather_units ({len(pairs)} per-tensor units, one launch)"
                            if gather_units
                            else "k_fused (ZeRO-3 output)" if zero3
@@ -677,7 +677,7 @@ def run_ours(args, rank, world, local_rank):
         del host_g, out
 
     if clipped:
-        launches_per_step = 3          # rs_norm, the rest of the norm tree + coefficient, update
+        launches_per_step = 2          # rs_norm with the tree up to the groups, update
     else:
         launches_per_step = 3 if variant == z.ZERO_VARIANT_STAGED else 1
     del ds

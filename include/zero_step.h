@@ -269,14 +269,17 @@ zero_status zero_ag_cast(const zero_plan_t* plan, const float* master,
  * dev_status; with ZERO_FLAG_SKIP_NONFINITE the update is skipped (state and
  * replicas untouched) and ZERO_DEV_SKIPPED is set.
  *   max_norm   > 0 and finite.
- *   scratch    device, at least zero_clip_scratch_bytes(plan) bytes: the
- *              fp32 averaged gradients, the tree levels, a control record and
- *              the tree's arrival counters (any contents on entry).
- * Three launches: the reduce-scatter with the first tree level, the rest of
- * the tree with the coefficient, the update with the all-gather.
+ *   scratch    device, 16-byte aligned, at least zero_clip_scratch_bytes(plan)
+ *              bytes: the fp32 averaged gradients and one tree partial per
+ *              group of tiles (any contents on entry; nothing persists
+ *              between calls).
+ * Two launches: the reduce-scatter with the tree up to one partial per group
+ * of tiles, then the update, whose blocks each finish the tree, derive the
+ * coefficient and run AdamW with the all-gather.
  *   dev_sumsq  optional device double: receives the squared norm.
  * Traffic: 2RM + 4 bytes/param (reduce-scatter, gradient stash) plus
- * 4 + 24 + 2R (update and all-gather) plus 4/2048 for the tree.
+ * 4 + 24 + 2R (update and all-gather); the tree's partials (at most 32 KB)
+ * are read from L2.
  */
 zero_status zero_step_clipped(const zero_plan_t* plan, const uint16_t* const* rank_grads,
                               float* master, float* m, float* v, uint16_t* const* rank_params,

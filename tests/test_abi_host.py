@@ -244,20 +244,22 @@ def test_binding_rejects_host_tensors_for_device_arguments():
 
 
 def test_clip_scratch_bytes_layout():
-    # fp32 gradient stash (4 * padded) + one 256-byte-rounded segment per tree
-    # level (ceil(N/256) warp partials, then ceil(./2048) ... down to 1) +
-    # control + one 4-byte arrival counter per group above the second level
+    # fp32 gradient stash (4 * padded, rounded to 256 bytes) + one fp32 partial
+    # per group of tiles (2048 elements a tile; a power-of-two number of tiles
+    # a group, the least that leaves at most 8192 groups), rounded to 256
+    # bytes; nothing else: no counters, no control record
     def r256(x):
         return -(-x // 256) * 256
-    p = z.Plan([65536], 4, 2, 1)                     # 256 -> 1 partials: no counters
-    assert z.zero_clip_scratch_bytes(p) == 4 * 65536 + 1024 + 256 + 256
-    p = z.Plan([1_235_814_400], 8, 1, 2)             # 4,827,400 -> 2,358 -> 2 -> 1 partials
-    levels = [4_827_400, 2_358, 2, 1]
-    want = (4 * p.padded + sum(r256(4 * n) for n in levels) + 256
-            + r256(4 * sum(levels[2:])))
-    assert z.zero_clip_scratch_bytes(p) == want
-    p = z.Plan([200], 2, 1, 2)                        # one partial: no counters
-    assert z.zero_clip_scratch_bytes(p) == 4 * p.padded + 256 + 256
+    p = z.Plan([65536], 4, 2, 1)                     # 32 tiles, a group each
+    assert z.zero_clip_scratch_bytes(p) == 4 * 65536 + 256
+    p = z.Plan([1_235_814_400], 8, 1, 2)             # 603,425 tiles: 128 a group
+    assert 1_235_814_400 == 603_425 * 2048
+    assert -(-603_425 // 64) > 8192 >= -(-603_425 // 128)
+    assert z.zero_clip_scratch_bytes(p) == 4 * p.padded + r256(4 * 4_715)
+    p = z.Plan([200], 2, 1, 2)                        # one tile
+    assert z.zero_clip_scratch_bytes(p) == 4 * p.padded + 256
+    p = z.Plan([8192 * 2048 + 1], 1, 1, 2)           # 8193 tiles: 2 a group
+    assert z.zero_clip_scratch_bytes(p) == 4 * p.padded + r256(4 * 4097)
 
 
 def test_clipped_step_argument_errors():

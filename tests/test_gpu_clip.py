@@ -3,8 +3,11 @@
 zero_step_clipped through the C ABI against oracle.dp_step_clipped on the same
 seeded inputs: the squared norm bit for bit, replicas bit for bit, the fp32
 state within 1e-6 (and bit for bit by design).  Sizes span one tile, ragged
-tails and three tree levels; full-size GPT-2 and uneven workloads are checked
-on sampled elements with the oracle run over the whole vector.
+tails, the largest count of one-tile groups (8192) and the first size with
+two-tile groups (its last group half empty); full-size GPT-2 and uneven
+workloads (8-tile groups) and the 1B workload (128-tile groups, reduced in 4
+rounds) are checked on sampled elements with the oracle run over the whole
+vector, the squared norm bit for bit.
 """
 import numpy as np
 import pytest
@@ -38,11 +41,12 @@ def _gpu_clipped(wl, G, W0, m0, v0, t, max_norm, flags=0):
     return ds, ds.result(), float(sumsq.item())
 
 
-@pytest.mark.parametrize("n", [1, 7, 2047, 2048, 2049, 100_003, 2048 * 2048 + 1])
+@pytest.mark.parametrize("n", [1, 7, 2047, 2048, 2049, 100_003, 2048 * 2048 + 1,
+                               2048 * 8192, 2048 * 8192 + 1])
 @pytest.mark.parametrize("R,M", [(8, 1), (4, 2), (7, 4), (3, 1)])
 def test_clipped_matches_oracle(n, R, M):
     if n > 1_000_000 and (R, M) != (8, 1):
-        pytest.skip("three tree levels are covered once")
+        pytest.skip("the large group counts are covered once")
     wl = W.flat(R, M, n, seed=n % 997 + R, step=3)
     G, W0, m0, v0 = H.host_inputs(wl, 3)
     for max_norm in (1e-4, 1e6):                    # clipping active / inactive

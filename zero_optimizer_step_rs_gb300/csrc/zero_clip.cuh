@@ -5,46 +5,43 @@
 // =========================================== step with global-norm clipping ==
 // zero_step_clipped: the averaged gradient of every element is stashed in
 // fp32 scratch while its square feeds a fixed pairwise tree (fp32, leaves
-// g*g, zero padding to a power of two); a small second kernel finishes the
-// tree and turns the squared norm into the clip coefficient (and the skip
-// decision for a non-finite norm), and a last pass applies it with the AdamW
-// update and the R-way bf16 all-gather: three launches.
+// g*g, zero padding to a power of two); the update pass finishes the tree,
+// turns the squared norm into the clip coefficient (and the skip decision for
+// a non-finite norm), and applies it with the AdamW update and the R-way bf16
+// all-gather: two launches.
 //
-// Tree decomposition: in the streaming pass each warp reduces 256
-// consecutive leaves (32 lanes x 8 leaves: a 3-level tree in registers, then
-// 5 levels of shuffles) - exactly an aligned subtree of the global tree - and
-// writes one partial, with no block-wide barrier; each further level is a
-// block reducing 2048 partials (8 per thread, the warp levels, then 3 levels
-// across the 8 warps), again an aligned subtree.  Adding a zero (padding)
-// changes no value, so the root equals the tree over the leaves padded to
-// the next power of two for any N and any grid.
-//
-// The levels above the first are finished in one launch with arrival
-// tickets, without any wait: the blocks reduce the groups of 2048 first-level
-// partials; a block that has written its group's sum makes it visible
-// (__threadfence) and takes a ticket on the counter of its group one level
-// up, and the block that draws that group's last ticket reduces it in turn;
-// the block that completes the root computes the coefficient.  No block ever
-// waits for another.  The counters are zeroed by the streaming pass, which
-// the tree launch follows in stream order.
+// Tree decomposition.  The norm pass works in tiles of 2048 elements (256
+// threads x 8) and takes them in groups of G consecutive tiles, G a power of
+// two chosen from N alone so that there are at most 8192 groups; one block
+// reduces a whole group (a block takes a run of consecutive groups), so every
+// group is an aligned subtree of the global tree.  Inside a group each warp reduces its 256 leaves of a tile (a 3-level
+// tree in registers, then 5 levels of shuffles) and leaves the partial in
+// shared memory; every 32 tiles (or at the group's end) the block reduces
+// those 256 partial slots, padded with zeros, and a group of more than 32
+// tiles combines its rounds pairwise.  The update pass reduces the group
+// partials, padded with zeros to 8192, again pairwise: each block redundantly,
+// from L2, before its first element.  A zero (padding) leaf or subtree changes
+// no value - the leaves are squares, so +0 or NaN, never -0 - and the root
+// therefore equals the tree over the leaves padded to the next power of two,
+// for any N and any grid.  No block ever waits for another, and the scratch
+// holds no counter: any contents on entry.
 namespace {
 
-constexpr int kTreeLeaves = 2048;                 // leaves per tree block (256 x 8)
-constexpr int kWarpLeaves = 256;                  // leaves per warp in the streaming pass
+constexpr int kTreeLeaves = 2048;                 // elements per norm-pass tile (256 x 8)
+constexpr int kWarpLeaves = 256;                  // leaves per warp and tile
+constexpr int kRoundTiles = 32;                   // tiles per shared-memory round (256 slots)
+constexpr int kMaxGroups = 8192;                  // group partials (256 threads x 32)
 
 struct ClipCtl {
     double sumsq;          // squared norm (the fp32 tree value, widened)
     float coef;            // multiplier when clip != 0
     int32_t clip;          // 1: multiply the averaged gradients by coef
     int32_t skip;          // 1: non-finite norm and skipping requested
-    int32_t pad[9];
 };
 
 struct ClipLayout {
-    int64_t g_off, ctl_off, cnt_off, cnt_bytes, total;
-    int levels;
-    int64_t lvl_off[8], lvl_len[8];
-    int64_t cnt_base[8];   // first counter of level k >= 2 (index into the counter array)
+    int64_t g_off, part_off, total;
+    int64_t tiles, group_tiles, groups;
 };
 
 int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
@@ -52,36 +49,26 @@ int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 ClipLayout clip_layout(const zero_plan_t* plan)
 {
     ClipLayout L{};
+    L.tiles = (plan->N + kTreeLeaves - 1) / kTreeLeaves;
+    if (L.tiles < 1) L.tiles = 1;
+    L.group_tiles = 1;
+    while ((L.tiles + L.group_tiles - 1) / L.group_tiles > kMaxGroups) L.group_tiles *= 2;
+    L.groups = (L.tiles + L.group_tiles - 1) / L.group_tiles;
     L.g_off = 0;
-    int64_t off = round256(4 * plan->padded);
-    int64_t len = (plan->N + kWarpLeaves - 1) / kWarpLeaves;
-    if (len < 1) len = 1;
-    L.levels = 0;
-    while (true) {
-        L.lvl_off[L.levels] = off;
-        L.lvl_len[L.levels] = len;
-        off += round256(4 * len);
-        ++L.levels;
-        if (len == 1 || L.levels == 8) break;
-        len = (len + kTreeLeaves - 1) / kTreeLeaves;
-    }
-    L.ctl_off = off;
-    L.cnt_off = off + round256((int64_t)sizeof(ClipCtl));
-    int64_t cnt = 0;                              // one counter per group above level 1
-    for (int k = 2; k < L.levels; ++k) {
-        L.cnt_base[k] = cnt;
-        cnt += L.lvl_len[k];
-    }
-    L.cnt_bytes = 4 * cnt;
-    L.total = L.cnt_off + round256(L.cnt_bytes);
+    L.part_off = round256(4 * plan->padded);
+    L.total = L.part_off + round256(4 * L.groups);
     return L;
 }
 
-// pairwise sum of 8 consecutive leaves (a perfect tree of 3 levels)
+// pairwise sum of 4 or 8 consecutive leaves (a perfect tree of 2 or 3 levels)
+__device__ __forceinline__ float tree4(float a, float b, float c, float d)
+{
+    return __fadd_rn(__fadd_rn(a, b), __fadd_rn(c, d));
+}
+
 __device__ __forceinline__ float tree8(const float (&x)[8])
 {
-    return __fadd_rn(__fadd_rn(__fadd_rn(x[0], x[1]), __fadd_rn(x[2], x[3])),
-                     __fadd_rn(__fadd_rn(x[4], x[5]), __fadd_rn(x[6], x[7])));
+    return __fadd_rn(tree4(x[0], x[1], x[2], x[3]), tree4(x[4], x[5], x[6], x[7]));
 }
 
 __device__ __forceinline__ float warp_tree(float v)
@@ -103,11 +90,12 @@ __device__ __forceinline__ float block_tree(float v)
     __syncthreads();
     float r = 0.0f;
     if (threadIdx.x == 0) {
-        const float* w = warp_sum;
-        r = __fadd_rn(__fadd_rn(__fadd_rn(w[0], w[1]), __fadd_rn(w[2], w[3])),
-                      __fadd_rn(__fadd_rn(w[4], w[5]), __fadd_rn(w[6], w[7])));
+        float w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = warp_sum[k];
+        r = tree8(w);
     }
-    __syncthreads();                   // warp_sum is reused by the next group
+    __syncthreads();                   // warp_sum is reused by the next call
     return r;                          // thread 0 holds the block's subtree
 }
 
@@ -115,16 +103,12 @@ struct ClipArgs {
     GradPtrs g;
     ReplicaPtrs P;
     float* gs;             // averaged gradients (padded floats; [0, N) used)
-    float* lvl[8];         // tree levels: level 0 has one partial per 256 elements (per warp)
-    int64_t lvl_len[8];
-    uint32_t* cnt[8];      // arrival counters of the groups of level k >= 2
-    uint32_t* cnt_all;     // all counters, zeroed by the streaming pass
-    int64_t n_cnt;
-    int32_t levels;
+    float* part;           // one partial per group of group_tiles tiles
+    int64_t tiles, group_tiles, groups;
+    int64_t groups_per_block;   // the norm pass's blocks take consecutive runs of groups
     float* W;
     float* m;
     float* v;
-    ClipCtl* ctl;
     int64_t n;
     int32_t R, M;
     StepScalars s;
@@ -135,8 +119,8 @@ struct ClipArgs {
 };
 
 // The squared norm into the clip coefficient (double, as clip_grad_norm_
-// computes it) and the skip decision, by the one thread that holds the root.
-__device__ void clip_finish(const ClipArgs& a, float ss)
+// computes it) and the skip decision.
+__device__ ClipCtl clip_control(const ClipArgs& a, float ss)
 {
     const double norm = sqrt((double)ss);
     const double coef = (double)a.max_norm / (norm + 1e-6);
@@ -144,125 +128,156 @@ __device__ void clip_finish(const ClipArgs& a, float ss)
     c.sumsq = (double)ss;
     c.clip = coef < 1.0 ? 1 : 0;
     c.coef = c.clip ? (float)coef : 1.0f;
-    const bool finite = isfinite(ss);
-    c.skip = (!finite && a.skip_nonfinite) ? 1 : 0;
-    *a.ctl = c;
-    if (a.status) {
-        if (!finite) atomicOr(a.status, ZERO_DEV_NONFINITE);
-        if (c.skip) atomicOr(a.status, ZERO_DEV_SKIPPED);
-    }
-    if (a.sumsq_out) *a.sumsq_out = c.sumsq;
-}
-
-// sum of group b of level k - 1 (at most 2048 partials, read from L2: other
-// blocks wrote them) into partial b of level k; the value in thread 0
-__device__ __forceinline__ float reduce_group(const ClipArgs& a, int k, int64_t b)
-{
-    const int64_t lo = b * kTreeLeaves;
-    const int64_t n_in = a.lvl_len[k - 1];
-    const float* in = a.lvl[k - 1];
-    const int64_t e = lo + (int64_t)threadIdx.x * 8;
-    float x[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) x[j] = e + j < n_in ? __ldcg(in + e + j) : 0.0f;
-    const float v = block_tree(tree8(x));
-    if (threadIdx.x == 0) a.lvl[k][b] = v;
-    return v;
-}
-
-// the levels above the first, then the coefficient: one launch
-__global__ void __launch_bounds__(kThreads) k_norm_tree(const __grid_constant__ ClipArgs a)
-{
-    __shared__ uint32_t last;
-    pdl_enter();
-    if (a.levels == 1) {                           // a single first-level partial is the root
-        if (blockIdx.x == 0 && threadIdx.x == 0) clip_finish(a, a.lvl[0][0]);
-        return;
-    }
-    for (int64_t g = blockIdx.x; g < a.lvl_len[1]; g += gridDim.x) {
-        float v = reduce_group(a, 1, g);
-        int64_t idx = g;
-        int k = 2;
-        for (; k < a.levels; ++k) {                // climb while this block is the last arrival
-            const int64_t b = idx / kTreeLeaves;
-            const int64_t n_in = a.lvl_len[k - 1] - b * kTreeLeaves;
-            const uint32_t expect = (uint32_t)(n_in < kTreeLeaves ? n_in : kTreeLeaves);
-            if (threadIdx.x == 0) {
-                __threadfence();                   // partial idx of level k - 1, before the ticket
-                last = atomicAdd(&a.cnt[k][b], 1u) == expect - 1;
-            }
-            __syncthreads();
-            const bool mine = last;
-            __syncthreads();                       // `last` is reused at the next level
-            if (!mine) break;
-            __threadfence();                       // the group's partials, after the tickets
-            v = reduce_group(a, k, b);
-            idx = b;
-        }
-        if (k == a.levels && threadIdx.x == 0) clip_finish(a, v);
-    }
+    c.skip = (!isfinite(ss) && a.skip_nonfinite) ? 1 : 0;
+    return c;
 }
 
 // pass 1: averaged gradient of 8 consecutive elements per thread, stashed,
-// and the tile's pairwise partial of their squares
+// and the group's pairwise partial of their squares.  Every block takes the
+// same number of consecutive groups (the last one fewer) and the grid is
+// sized to it: the pass streams at a rate set by its active blocks, and on
+// GB300 the 1B-shaped workload's 4,715 groups dealt round-robin to 760 blocks
+// (7 rounds where 6.2 would do) took 4.53 ms against 3.70 for the earlier
+// tile-by-tile pass; in runs of 6 groups over 786 blocks with 40 registers
+// (6 blocks per SM; 5 at the unbounded 48) it takes 3.62 ms.  The generic
+// (R, M) case runs 2 blocks per SM (128 registers, no spill); at 6 it
+// spilled 380 bytes.
 template <int RC, int MC>
-__global__ void __launch_bounds__(kThreads) k_rs_norm(const __grid_constant__ ClipArgs a)
+__global__ void __launch_bounds__(kThreads, RC > 0 ? 6 : 2)
+k_rs_norm(const __grid_constant__ ClipArgs a)
 {
+    __shared__ float slot[kRoundTiles * (kThreads / 32)];  // warp partials of one round
     pdl_enter();
     const int R = RC > 0 ? RC : a.R;
     const int M = MC > 0 ? MC : a.M;
     const int64_t n = a.n;
-    const int64_t tiles = (n + kTreeLeaves - 1) / kTreeLeaves;
-    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-        const int64_t e = tile * kTreeLeaves + (int64_t)threadIdx.x * 8;
-        float g[8];
-        if (e + 8 <= n) {
-            float lo[4], hi[4];
-            grad_sum4<RC, MC>(a.g, R, M, e, lo);
-            grad_sum4<RC, MC>(a.g, R, M, e + 4, hi);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t GT = a.group_tiles;
+    const int round_tiles = GT < kRoundTiles ? (int)GT : kRoundTiles;
+    const int64_t g0 = (int64_t)blockIdx.x * a.groups_per_block;
+    const int64_t g1 = g0 + a.groups_per_block < a.groups ? g0 + a.groups_per_block : a.groups;
+    for (int64_t grp = g0; grp < g1; ++grp) {
+        float stack[40];               // pairwise combination of the rounds (thread 0)
+        int64_t rounds = 0;
+        for (int64_t t0 = grp * GT; t0 < (grp + 1) * GT; t0 += round_tiles) {
+            for (int j = 0; j < round_tiles; ++j) {
+                const int64_t tile = t0 + j;
+                float part = 0.0f;
+                if (tile < a.tiles) {
+                    const int64_t e = tile * kTreeLeaves + (int64_t)threadIdx.x * 8;
+                    float g[8];
+                    if (e + 8 <= n) {
+                        float lo[4], hi[4];
+                        grad_sum4<RC, MC>(a.g, R, M, e, lo);
+                        grad_sum4<RC, MC>(a.g, R, M, e + 4, hi);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                g[k] = scale_grad(a.s, lo[k]);
-                g[4 + k] = scale_grad(a.s, hi[k]);
-            }
-            st_stream(a.gs + e, make_float4(g[0], g[1], g[2], g[3]));
-            st_stream(a.gs + e + 4, make_float4(g[4], g[5], g[6], g[7]));
-        } else {
+                        for (int k = 0; k < 4; ++k) {
+                            g[k] = scale_grad(a.s, lo[k]);
+                            g[4 + k] = scale_grad(a.s, hi[k]);
+                        }
+                        st_stream(a.gs + e, make_float4(g[0], g[1], g[2], g[3]));
+                        st_stream(a.gs + e + 4, make_float4(g[4], g[5], g[6], g[7]));
+                    } else {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                g[k] = 0.0f;
-                if (e + k < n) {
-                    g[k] = scale_grad(a.s, grad_sum1(a.g, R, M, e + k));
-                    a.gs[e + k] = g[k];
+                        for (int k = 0; k < 8; ++k) {
+                            g[k] = 0.0f;
+                            if (e + k < n) {
+                                g[k] = scale_grad(a.s, grad_sum1(a.g, R, M, e + k));
+                                a.gs[e + k] = g[k];
+                            }
+                        }
+                    }
+                    float sq[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) sq[k] = __fmul_rn(g[k], g[k]);  // padding: +0
+                    part = warp_tree(tree8(sq));
                 }
+                if (lane == 0) slot[j * (kThreads / 32) + warp] = part;
+            }
+            __syncthreads();
+            // the round's 256 slots, zero past round_tiles * 8: one per thread
+            const int used = round_tiles * (kThreads / 32);
+            const float v = block_tree((int)threadIdx.x < used ? slot[threadIdx.x] : 0.0f);
+            if (threadIdx.x == 0) {    // push the round; merge equal-sized subtrees
+                float x = v;
+                int64_t c = rounds++;
+                int top = __popcll(c);
+                while (c & 1) {
+                    x = __fadd_rn(stack[--top], x);
+                    c >>= 1;
+                }
+                stack[top] = x;
             }
         }
-        float sq[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) sq[k] = __fmul_rn(g[k], g[k]);   // padding leaves are +0
-        const float part = warp_tree(tree8(sq));
-        const int64_t wpart = tile * (kTreeLeaves / kWarpLeaves) + (threadIdx.x >> 5);
-        if ((threadIdx.x & 31) == 0 && wpart * kWarpLeaves < n) a.lvl[0][wpart] = part;
+        // rounds per group is 1 or a power of two: the stack holds one value
+        if (threadIdx.x == 0) a.part[grp] = stack[0];
     }
-    // the tree launch that follows takes tickets on these counters
-    if (blockIdx.x == 0)
-        for (int64_t i = threadIdx.x; i < a.n_cnt; i += kThreads) a.cnt_all[i] = 0u;
 }
 
-// pass 2: g' = g * coef (when clipping), AdamW, bf16 all-gather; tiles of
-// 256 threads x 4 elements x kAgUnits units with every load of a tile issued
-// first, as in k_fused.  This pass writes 28 of its 44 bytes per parameter,
-// and write-heavy streams ran faster with more warps per SM: one unit at 8
+// pass 2: the root of the tree over the group partials and the clip
+// coefficient (every block, redundantly: 32 KB from L2 at most), then
+// g' = g * coef (when clipping), AdamW, bf16 all-gather; tiles of 256 threads
+// x 4 elements x kAgUnits units with every load of a tile issued first, as in
+// k_fused.  This pass writes 28 of its 44 bytes per parameter, and
+// write-heavy streams ran faster with more warps per SM: one unit at 8
 // blocks per SM (32 registers, 56 bytes spilled to L1) measured 0.951 of the
 // copy peak for the whole step against 0.947 for 4 units at 2 blocks per SM
 // (114 registers); 1 unit at 4 or 6, 2 units at 4 and 4 units at 3 blocks
 // per SM measured 0.942-0.948.
 constexpr int kAgUnits = 1;
+
+// Warp w reduces slots [1024 w, 1024 (w + 1)) of the 8192: lane l holds
+// slots 128 q + 4 l .. + 3 of chunk q, so the lanes' shuffle tree spans the
+// chunk's 128 consecutive slots, and the 8 chunks and then the 8 warps close
+// the tree.  Slots past the last group are zero.
+__device__ __forceinline__ float groups_root(const ClipArgs& a)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float c[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int64_t s = (int64_t)warp * 1024 + q * 128 + lane * 4;
+        float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (s + 4 <= a.groups) {
+            x = __ldcg(reinterpret_cast<const float4*>(a.part + s));
+        } else if (s < a.groups) {
+            x.x = __ldcg(a.part + s);
+            if (s + 1 < a.groups) x.y = __ldcg(a.part + s + 1);
+            if (s + 2 < a.groups) x.z = __ldcg(a.part + s + 2);
+        }
+        c[q] = warp_tree(tree4(x.x, x.y, x.z, x.w));
+    }
+    __shared__ float warp_sum[kThreads / 32];
+    if (lane == 0) warp_sum[warp] = tree8(c);
+    __syncthreads();
+    float r = 0.0f;
+    if (threadIdx.x == 0) {
+        float w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = warp_sum[k];
+        r = tree8(w);
+    }
+    return r;                          // thread 0 holds the root
+}
+
 template <int RC>
 __global__ void __launch_bounds__(kThreads, 8) k_adamw_ag(const __grid_constant__ ClipArgs a)
 {
+    __shared__ ClipCtl ctl;
     pdl_enter();
-    const ClipCtl c = *a.ctl;
+    const float ss = groups_root(a);
+    if (threadIdx.x == 0) {
+        ctl = clip_control(a, ss);
+        if (blockIdx.x == 0) {
+            if (a.status) {
+                if (!isfinite(ss)) atomicOr(a.status, ZERO_DEV_NONFINITE);
+                if (ctl.skip) atomicOr(a.status, ZERO_DEV_SKIPPED);
+            }
+            if (a.sumsq_out) *a.sumsq_out = ctl.sumsq;
+        }
+    }
+    __syncthreads();
+    const ClipCtl c = ctl;
     if (c.skip) return;
     const int R = RC > 0 ? RC : a.R;
     constexpr int U = kAgUnits;
@@ -324,8 +339,11 @@ template <int RC, int MC>
 cudaError_t launch_rs_norm_t(const ClipArgs& a, cudaStream_t st)
 {
     const void* k = reinterpret_cast<const void*>(&k_rs_norm<RC, MC>);
-    const int64_t tiles = (a.n + kTreeLeaves - 1) / kTreeLeaves;
-    return launch_pdl(k_rs_norm<RC, MC>, dim3(grid_for(k, tiles)), kThreads, st, a);
+    const int64_t cap = grid_for(k, a.groups);
+    ClipArgs b = a;
+    b.groups_per_block = (a.groups + cap - 1) / cap;
+    const int64_t grid = (a.groups + b.groups_per_block - 1) / b.groups_per_block;
+    return launch_pdl(k_rs_norm<RC, MC>, dim3((unsigned)grid), kThreads, st, b);
 }
 
 cudaError_t launch_rs_norm(const ClipArgs& a, cudaStream_t st)
@@ -395,15 +413,10 @@ extern "C" zero_status zero_step_clipped(const zero_plan_t* plan,
     fill_grad_ptrs(a.g, plan, rank_grads);
     fill_replica_ptrs(a.P, plan, rank_params);
     a.gs = reinterpret_cast<float*>(base + L.g_off);
-    uint32_t* counters = reinterpret_cast<uint32_t*>(base + L.cnt_off);
-    a.levels = L.levels;
-    for (int k = 0; k < L.levels; ++k) {
-        a.lvl[k] = reinterpret_cast<float*>(base + L.lvl_off[k]);
-        a.lvl_len[k] = L.lvl_len[k];
-        a.cnt[k] = k >= 2 ? counters + L.cnt_base[k] : nullptr;
-    }
-    a.cnt_all = counters;
-    a.n_cnt = L.cnt_bytes / 4;
+    a.part = reinterpret_cast<float*>(base + L.part_off);
+    a.tiles = L.tiles;
+    a.group_tiles = L.group_tiles;
+    a.groups = L.groups;
     a.max_norm = max_norm;
     a.skip_nonfinite = (flags & ZERO_FLAG_SKIP_NONFINITE) ? 1 : 0;
     a.status = dev_status;
@@ -411,7 +424,6 @@ extern "C" zero_status zero_step_clipped(const zero_plan_t* plan,
     a.W = master;
     a.m = m;
     a.v = v;
-    a.ctl = reinterpret_cast<ClipCtl*>(base + L.ctl_off);
     a.n = plan->N;
     a.R = plan->R;
     a.M = plan->M;
@@ -419,11 +431,6 @@ extern "C" zero_status zero_step_clipped(const zero_plan_t* plan,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     cudaError_t err = launch_rs_norm(a, st);
-    if (err == cudaSuccess) {
-        const void* k = reinterpret_cast<const void*>(&k_norm_tree);
-        err = launch_pdl(k_norm_tree, dim3(L.levels > 1 ? grid_for(k, L.lvl_len[1]) : 1),
-                         kThreads, st, a);
-    }
     if (err == cudaSuccess) err = launch_adamw_ag(a, st);
     return cuda_status(err);
 }
