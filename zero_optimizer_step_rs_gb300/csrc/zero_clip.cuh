@@ -223,7 +223,9 @@ k_rs_norm(const __grid_constant__ ClipArgs a)
 // blocks per SM (32 registers, 56 bytes spilled to L1) measured 0.951 of the
 // copy peak for the whole step against 0.947 for 4 units at 2 blocks per SM
 // (114 registers); 1 unit at 4 or 6, 2 units at 4 and 4 units at 3 blocks
-// per SM measured 0.942-0.948.
+// per SM measured 0.942-0.948.  The replica tile staged in shared memory
+// and written by R bulk copies (cp.async.bulk, one thread, double-buffered)
+// measured 0.944 against 0.957 for the register stores.
 constexpr int kAgUnits = 1;
 
 // Warp w reduces slots [1024 w, 1024 (w + 1)) of the 8192: lane l holds
