@@ -312,8 +312,13 @@ StepScalars divisor_scalars(int R, int M)
     return s;
 }
 
+// R=8, M=1 runs 6 blocks per SM (40 registers, 8 bytes spilled; 5 at the
+// unbounded 47): the 1B-shaped workload's 18 per-layer reduce-scatters went
+// from 0.953 to 0.958 of the copy peak on GB300 (8 blocks, 32 registers:
+// 0.915).
 template <int RC, int MC, bool CHECK>
-__global__ void __launch_bounds__(kThreads) k_rs_unit(const __grid_constant__ UnitArgs a)
+__global__ void __launch_bounds__(kThreads, (RC == 8 && MC == 1) ? 6 : 1)
+k_rs_unit(const __grid_constant__ UnitArgs a)
 {
     pdl_enter();
     const int R = RC > 0 ? RC : a.R;
