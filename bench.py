@@ -740,6 +740,10 @@ def run_table(args):
     peaks = measured_peaks() or {}
     peak = float(peaks.get("hbm_gbs", 6800.0))
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    # read after the write flush, it leaves L2 holding clean lines of an
+    # unrelated buffer: the timed launch then writes back none of the
+    # flush's dirty lines (up to the 129 MB of L2 at 6.7 TB/s: ~19 us)
+    clean_src = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
     rows = []
     sampler = ClockSampler(gpu_uuid(0))          # SM clocks over the GPU part
     sampler.start()
@@ -759,13 +763,15 @@ def run_table(args):
             for g, c in zip(ds.grads[:2], ds.kept_grads):
                 g.copy_(c)
 
-    def timed(ds, variant, reps, cold=True):
+    def timed(ds, variant, reps, cold=True, clean=False):
         ts = []
         t = ds.wl.step
         for k in range(3 + reps):
             before_step(ds, variant)
             if cold:
                 flush.fill_(k & 0xFF)                  # evict L2 (256 MB > 129 MB)
+                if clean:
+                    clean_src.sum()                    # dirty lines written back here
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             run_step(ds, t, variant)
@@ -776,7 +782,7 @@ def run_table(args):
                 ts.append(e0.elapsed_time(e1))
         return float(np.median(ts))
 
-    def timed_small(ds, variant, reps, cold):
+    def timed_small(ds, variant, reps, cold, clean=False):
         """A step of microseconds: every launch is enqueued behind a sleep
         kernel, so the events time the GPU, not the host's launch calls.
         Warm: reps steps back to back between one event pair, the mean per
@@ -800,6 +806,8 @@ def run_table(args):
         ev = []
         for k in range(reps):
             flush.fill_(k & 0xFF)
+            if clean:
+                clean_src.sum()                        # dirty lines written back here
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             run_step(ds, t + k, variant)
@@ -837,6 +845,12 @@ def run_table(args):
                               "spans around one launch (an empty pair spans ~2.1 us)" if cold
                               else "warm: inputs resident, 200 launches back to back, mean")
                        if resident else "inputs far larger than L2; flushed before each launch"}
+                if cold:
+                    ms_c = (timed(ds, variant, reps, clean=True) if not resident
+                            else timed_small(ds, variant, 200, True, clean=True))
+                    row["ms_clean_l2"] = round(ms_c, 4)
+                    row["frac_clean_l2"] = round(
+                        bpp(wl, variant) * wl.N / (ms_c / 1e3) / 1e9 / peak, 4)
                 rows.append(row)
                 print(json.dumps(row), flush=True)
         del ds
