@@ -29,11 +29,13 @@ def _oracle_clipped(wl, G, W0, m0, v0, t, max_norm, skip=False):
     return (Wc, mc, vc, P), ss, sk
 
 
-def _gpu_clipped(wl, G, W0, m0, v0, t, max_norm, flags=0):
+def _gpu_clipped(wl, G, W0, m0, v0, t, max_norm, flags=0, scratch_fill=None):
     ds = H.DeviceState(wl, staged_scratch=False)
     ds.upload_state(W0, m0, v0)
     ds.upload_grads(G)
     scratch = torch.empty(z.zero_clip_scratch_bytes(ds.plan), dtype=torch.uint8, device="cuda")
+    if scratch_fill is not None:
+        scratch.fill_(scratch_fill)
     sumsq = torch.zeros(1, dtype=torch.float64, device="cuda")
     z.zero_step_clipped(ds.plan, ds.grads, ds.W, ds.m, ds.v, ds.params, ds.hp, t, max_norm,
                         scratch, flags=flags, dev_status=ds.status, dev_sumsq=sumsq)
@@ -68,6 +70,46 @@ def test_clipped_largest_rank_and_microbatch_counts(n, R, M):
     ds, got, gss = _gpu_clipped(wl, G, W0, m0, v0, 3, 1e-4)
     assert gss == ss, (gss, ss)
     res = H.compare(got, want)
+    assert not {k: v for k, v in res.items() if v}, res
+
+
+@pytest.mark.parametrize("n", [2049, 2048 * 8192 + 1])
+def test_clipped_scratch_contents_on_entry_do_not_matter(n):
+    """The scratch holds no counter or state across calls: filled with 0xFF
+    bytes (NaN in every fp32 slot) it gives the same bits."""
+    wl = W.flat(8, 1, n, seed=21, step=3)
+    G, W0, m0, v0 = H.host_inputs(wl, 3)
+    want, ss, _ = _oracle_clipped(wl, G, W0, m0, v0, 3, 1e-4)
+    ds, got, gss = _gpu_clipped(wl, G, W0, m0, v0, 3, 1e-4, scratch_fill=0xFF)
+    assert gss == ss, (gss, ss)
+    res = H.compare(got, want)
+    assert not {k: v for k, v in res.items() if v}, res
+    assert int(ds.status.item()) == 0
+
+
+def test_clipped_consecutive_steps_share_scratch():
+    """Two steps through one scratch buffer, the second with fresh gradients
+    and clipping inactive, each against the oracle."""
+    wl = W.flat(7, 4, 2 * 2048 * 8192 + 77, seed=22, step=3)    # groups of 4 tiles
+    G3, W0, m0, v0 = H.host_inputs(wl, 3)
+    G4, _, _, _ = H.host_inputs(wl, 4)
+    hp = oracle.hparams(**wl.hparams())
+    Wc, mc, vc = W0.copy(), m0.copy(), v0.copy()
+    P = [np.zeros(wl.N, np.uint16) for _ in range(wl.R)]
+    ss3, _ = oracle.dp_step_clipped(G3, Wc, mc, vc, P, hp, 3, wl.R, wl.M, max_norm=1e-4)
+    ss4, _ = oracle.dp_step_clipped(G4, Wc, mc, vc, P, hp, 4, wl.R, wl.M, max_norm=1e6)
+    ds = H.DeviceState(wl, staged_scratch=False)
+    ds.upload_state(W0, m0, v0)
+    sq = torch.zeros(1, dtype=torch.float64, device="cuda")
+    ds.upload_grads(G3)
+    ds.step_clipped(3, 1e-4, sumsq=sq)
+    torch.cuda.synchronize()
+    assert float(sq.item()) == ss3
+    ds.upload_grads(G4)
+    ds.step_clipped(4, 1e6, sumsq=sq)
+    torch.cuda.synchronize()
+    assert float(sq.item()) == ss4
+    res = H.compare(ds.result(), (Wc, mc, vc, P))
     assert not {k: v for k, v in res.items() if v}, res
 
 

@@ -226,6 +226,27 @@ def test_staged_zero2_without_scratch_matches_oracle(name, target):
     assert int(ds.status.item()) == 0
 
 
+def test_staged_scratch_contents_on_entry_do_not_matter():
+    """The staged step's caller scratch carries nothing between calls: filled
+    with 0xFF bytes (NaN in every fp32 slot) before each step, two steps with
+    fresh gradients still give the oracle's bits."""
+    wl = W.uneven().scaled(250_003)
+    steps = [wl.first_step(), wl.first_step() + 1]
+    _, W0, m0, v0 = H.host_inputs(wl, steps[0])
+    idx = np.arange(wl.N, dtype=np.int64)
+    Gs = {t: W.host_grads_at(wl, t, idx) for t in steps}
+    want = H.oracle_run(wl, Gs, W0, m0, v0, steps)
+    ds = H.DeviceState(wl)
+    ds.upload_state(W0, m0, v0)
+    for t in steps:
+        ds.upload_grads(Gs[t])
+        ds.scratch.view(torch.uint8).fill_(0xFF)
+        ds.step(t, variant=z.ZERO_VARIANT_STAGED, flags=z.ZERO_FLAG_CHECK_FINITE)
+    torch.cuda.synchronize()
+    _assert_parity(H.compare(ds.result(), want))
+    assert int(ds.status.item()) == 0
+
+
 def test_staged_zero2_without_scratch_touches_only_two_gradient_buffers():
     """Guard bands around every buffer: the mode writes gradient buffers 0
     and 1 and nothing else beside the state and the replicas; the other
