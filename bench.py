@@ -1327,6 +1327,208 @@ def run_reference(args):
     }
 
 
+def render_table(rows, peak_gbs):
+    """The rows of `bench.py --table` (parsed JSON lines) as the markdown
+    tables of the all-workload profile; the commentary under them is
+    written by hand."""
+    out = []
+    P = out.append
+
+    def gp(x):                                    # params/s as G params/s
+        return f"{x / 1e9:.2f}"
+
+    def t_str(ms):
+        return f"{ms * 1e3:.2f} µs" if ms < 0.1 else f"{ms:.4f} ms"
+
+    def clean(r):                                 # the clean-L2 columns
+        if "ms_clean_l2" not in r:
+            return "– | –"
+        return f"{t_str(r['ms_clean_l2'])} | {r['frac_clean_l2']:.3f}"
+
+    def l2_label(r, resident="warm"):
+        l2 = r.get("l2", "")
+        return "cold" if l2.startswith("cold") else resident if l2.startswith("warm") else "> L2"
+
+    P("# All workloads; the clipped, compressed, 1-bit Adam and ZeRO-3 steps; the flat sweep; "
+      "the oracle on 1 and 16 host cores")
+    P("")
+    P("Commands (one GB300, one call; the tables are rendered from the JSON lines, the reading at "
+      "the end is written by hand):")
+    P("")
+    P("    python bench.py --table > table.jsonl")
+    P("    python bench.py --render-table table.jsonl")
+    P("")
+    P("Timing:")
+    P("")
+    P("- Workloads larger than L2: a 256 MB write evicts L2 before every timed launch; median of 20 "
+      "reps (10 for")
+    P("  the ~4B workload, ZeRO-3, the compressed codecs, 1-bit Adam and the clipped step). That "
+      "write leaves L2")
+    P("  full of dirty lines, and the timed launch writes them back as its own data evicts them: up "
+      "to ~19 us at")
+    P("  the copy peak, noise at the 1B size but most of the gap at a few million params. The "
+      "**clean L2**")
+    P("  columns time the same launches after the write and then a 256 MB read of another buffer, "
+      "which leaves")
+    P("  L2 holding clean, unrelated lines: the kernel's own cost from a cold cache.")
+    P("- Workloads that fit in L2 (tiny, small sweep points), every launch enqueued behind a sleep "
+      "kernel so the")
+    P("  events time the GPU, not the host's launch calls: **cold** = a flush, then an event pair "
+      "around one")
+    P("  launch, mean of 200 (the event timer ticks about every 2 µs and an empty pair spans "
+      "~2.1 µs);")
+    P("  **warm** = 200 launches back to back between one event pair, mean per launch.")
+    P("")
+    P(f"Peak: {peak_gbs:,.1f} GB/s, the pool's measured copy bandwidth (`MEASURED_PEAKS.json`). "
+      "Bytes per parameter are algorithmic:")
+    P("")
+    for line in ("- fused: 2RM + 24 + 2R;",
+                 "- staged (scratch, or the reduced gradient in gradient buffers 0 and 1): "
+                 "2RM + 36 + 2R;",
+                 "- ZeRO-3 step: 2RM + 26;",
+                 "- ZeRO-3 gather: 4 per element (2 read, 2 written);",
+                 "- ZeRO-3 unit reduce-scatter: 2RM + 4; shard update: 30;",
+                 "- compressed: 2RM + 24 + 2R, plus 8R with error feedback;",
+                 "- clipped: 2RM + 32 + 2R;",
+                 "- 1-bit Adam: 2RM + 10R + 28."):
+        P(line)
+    P("")
+    clk = next((r["clocks"] for r in rows if "clocks" in r), None)
+    if clk:
+        P(f"SM clock over the GPU rows (NVML every 5 ms): median {clk['sm_mhz']:.0f} MHz of "
+          f"{clk['sm_max_mhz']:.0f}, throttle reasons: {', '.join(clk['reasons']) or 'none'} "
+          f"({clk['samples']} samples).")
+        P("")
+    P("## ZeRO-1/2 step, every workload")
+    P("")
+    P("| workload | R | M | N | variant | L2 | B/param | µs or ms | G params/s | GB/s | "
+      "of measured peak | clean L2: µs or ms | of peak |")
+    P("|---|---:|---:|---:|---|---|---:|---:|---:|---:|---:|---:|---:|")
+    for r in rows:
+        v = str(r.get("variant", ""))
+        if v not in ("fused", "staged") and not v.startswith("staged, reduced"):
+            continue
+        if str(r["workload"]).startswith("sweep"):
+            continue
+        vs = "staged, gradient in buffers 0/1" if v.startswith("staged, reduced") else v
+        P(f"| {r['workload']} | {r['R']} | {r['M']} | {r['N']:,} | {vs} | {l2_label(r)} | "
+          f"{r['bytes_per_param']} | {t_str(r['ms'])} | {gp(r['params_per_s'])} | {r['GB_s']} | "
+          f"{r['frac_of_measured_peak']:.3f} | {clean(r)} |")
+    P("")
+    P("## ZeRO-3: step (cast into each rank's own shard, no all-gather)")
+    P("")
+    P("| workload | R | M | N | B/param | ms | G params/s | GB/s | of measured peak |")
+    P("|---|---:|---:|---:|---:|---:|---:|---:|---:|")
+    for r in rows:
+        if r.get("variant") == "zero3_step":
+            P(f"| {r['workload']} | {r['R']} | {r['M']} | {r['N']:,} | {r['bytes_per_param']} | "
+              f"{r['ms']:.4f} | {gp(r['params_per_s'])} | {r['GB_s']} | "
+              f"{r['frac_of_measured_peak']:.3f} |")
+    P("")
+    P("## ZeRO-3: all-gather of the whole Llama-3.2-1B-shaped model, by unit size "
+      "(one destination)")
+    P("")
+    P("| unit | launches | ms for the whole model | GB/s | of measured peak |")
+    P("|---|---:|---:|---:|---:|")
+    for r in rows:
+        if r.get("variant") == "zero3_gather":
+            P(f"| {r['unit']} | {r['launches']} | {r['ms']:.4f} | {r['GB_s']} | "
+              f"{r['frac_of_measured_peak']:.3f} |")
+    P("")
+    P("## ZeRO-3 backward unit by unit (FSDP) on the Llama-3.2-1B-shaped workload: one "
+      "reduce-scatter per layer, last layer first, then the shard update")
+    P("")
+    P("The fp32 gradient shard is written by the reduce-scatters and read by the update: "
+      "8 B/param more than the whole-step kernel.")
+    P("")
+    part_hdr = ("| {} | launches | B/param | ms | G params/s | GB/s | of measured peak |",
+                "|---|---:|---:|---:|---:|---:|---:|")
+    P(part_hdr[0].format("part"))
+    P(part_hdr[1])
+    for r in rows:
+        if r.get("variant") == "zero3_units":
+            P(f"| {r['part']} | {r['launches']} | {r['bytes_per_param']} | {r['ms']:.4f} | "
+              f"{gp(r['params_per_s'])} | {r['GB_s']} | {r['frac_of_measured_peak']:.3f} |")
+    P("")
+    P("With each layer's parameters all-gathered again before its reduce-scatter (FSDP "
+      "materialises a unit for its backward) into one of two transient buffers: "
+      "4 + 2RM + 4 B/param.")
+    P("")
+    P(part_hdr[0].format("schedule"))
+    P(part_hdr[1])
+    for r in rows:
+        if r.get("variant") == "zero3_backward":
+            P(f"| {r['part']} | {r['launches']} | {r['bytes_per_param']} | {r['ms']:.4f} | "
+              f"{gp(r['params_per_s'])} | {r['GB_s']} | {r['frac_of_measured_peak']:.3f} |")
+    P("")
+    P("## Compressed reduce-scatter on the Llama-3.2-1B-shaped workload (R=8, M=1)")
+    P("")
+    P("Error feedback reads and writes one fp32 residual per rank: +8R B/param. The compressed "
+      "message stays in registers; wire bytes are what a rank would send.")
+    P("")
+    P("| codec | error feedback | wire B/param per rank | B/param (HBM) | ms | G params/s | GB/s | "
+      "of measured peak |")
+    P("|---|---|---:|---:|---:|---:|---:|---:|")
+    for r in rows:
+        if r.get("variant") == "compressed" and "ms" in r:
+            P(f"| {r['codec']} | {'yes' if r['error_feedback'] else 'no'} | "
+              f"{r['wire_bytes_per_param_per_rank']} | {r['bytes_per_param']} | {r['ms']:.4f} | "
+              f"{gp(r['params_per_s'])} | {r['GB_s']} | {r['frac_of_measured_peak']:.3f} |")
+    P("")
+    P("## Clipped and 1-bit Adam steps on the Llama-3.2-1B-shaped workload (R=8, M=1)")
+    P("")
+    P("Clipped: 2RM + 8 + 24 + 2R B/param (the fp32 gradient stash written and read back), "
+      "clipping active, two launches (the norm pass with the tree up to one partial per group "
+      "of tiles; the update, every block finishing the tree first). 1-bit Adam after its "
+      "warm-up: 2RM + 10R + 28 B/param, shards on the 128-element grid.")
+    P("")
+    P("| step | launches | B/param | ms | G params/s | GB/s | of measured peak |")
+    P("|---|---:|---:|---:|---:|---:|---:|")
+    for r in rows:
+        if r.get("variant") in ("onebit", "clipped") and "ms" in r:
+            P(f"| {r['variant']} | {r.get('launches', 1)} | {r['bytes_per_param']} | "
+              f"{r['ms']:.4f} | {gp(r['params_per_s'])} | {r['GB_s']} | "
+              f"{r['frac_of_measured_peak']:.3f} |")
+    P("")
+    P("## Flat sweep (fused): fp32 master shard of 4 KB ... 1 GB (S = 1 Ki ... 256 Mi elements), "
+      "N = R*S")
+    P("")
+    P("| R | S | N | L2 | µs or ms | G params/s | GB/s | of measured peak | clean L2: µs or ms | "
+      "of peak |")
+    P("|---:|---:|---:|---|---:|---:|---:|---:|---:|---:|")
+    for r in rows:
+        if str(r.get("workload", "")).startswith("sweep"):
+            S = int(r["workload"].split("S=")[1])
+            P(f"| {r['R']} | {S:,} | {r['N']:,} | {l2_label(r, 'warm (L2-resident)')} | "
+              f"{t_str(r['ms'])} | {gp(r['params_per_s'])} | {r['GB_s']} | "
+              f"{r['frac_of_measured_peak']:.3f} | {clean(r)} |")
+    P("")
+    P("## Oracle (unchanged) on the box's host cores, first 2^22 params of each workload, "
+      "best of 3")
+    P("")
+    P("`oracle_dp_step_mt` for the plain step, on 1 and 16 threads:")
+    P("")
+    P("| workload | threads | M params/s | GB/s (same byte model) |")
+    P("|---|---:|---:|---:|")
+    for r in rows:
+        if "oracle_threads" in r and "oracle" not in r:
+            P(f"| {r['workload']} | {r['oracle_threads']} | {r['params_per_s'] / 1e6:.1f} | "
+              f"{r['GB_s']} |")
+    P("")
+    P("The oracle of each step variant on the Llama-3.2-1B-shaped workload (one core: these "
+      "functions are single-threaded), beside the GPU rows above:")
+    P("")
+    P("| oracle | variant | M params/s |")
+    P("|---|---|---:|")
+    for r in rows:
+        if "oracle" in r and "oracle_threads" in r:
+            v = r["variant"]
+            if v == "compressed":
+                v = f"compressed {r['codec']}{' + error feedback' if r['ef'] else ''}"
+            P(f"| `{r['oracle']}` | {v} | {r['params_per_s'] / 1e6:.1f} |")
+    return "\n".join(out) + "\n"
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1352,7 +1554,15 @@ def main():
                     help="every workload and the flat sweep, one JSON line each")
     ap.add_argument("--ckpt", action="store_true",
                     help="checkpoint save / load / reshard timings of two workloads")
+    ap.add_argument("--render-table", metavar="JSONL",
+                    help="print the JSON lines of a --table run as markdown tables")
     args = ap.parse_args()
+    if args.render_table:
+        with open(args.render_table) as f:
+            rows = [json.loads(line) for line in f if line.startswith("{")]
+        peak = float((measured_peaks() or {}).get("hbm_gbs", 6800.0))
+        sys.stdout.write(render_table(rows, peak))
+        return 0
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 

@@ -1,13 +1,20 @@
 """Host logic of bench.py that needs no GPU: the summary of the nvidia-smi
 clock samples that goes into the bench line (median SM clock, maximum SM
-clock, throttle reasons seen inside the timed region), and the oracle leg
-(cpu_baseline and the reference arm) timing the oracle of the measured step."""
+clock, throttle reasons seen inside the timed region), the oracle leg
+(cpu_baseline and the reference arm) timing the oracle of the measured step,
+and the markdown rendering of a --table run."""
 import datetime
+import json
 import os
+import pathlib
+import subprocess
+import sys
 
 import pytest
 
 import bench
+
+REPO = pathlib.Path(__file__).resolve().parent.parent
 
 
 def _line(t, sm, mx=2070, reasons=("Not Active",) * 4):
@@ -169,3 +176,38 @@ def test_cpu_baseline_carries_the_all_core_and_one_core_oracle_rates():
     one = bench.oracle_baseline(wl, {"variant": "clipped", "max_norm": 1.0}, target_s=0.05,
                                 sample_elems=1 << 14)
     assert one["cores"] == 1 and one["value_1core"] == one["value"]
+
+
+def test_render_table_writes_every_section_from_the_json_lines(tmp_path):
+    """`bench.py --render-table` turns the JSON lines of a --table run into
+    the markdown tables of the all-workload profile."""
+    rows = [
+        {"workload": "llama-3.2-1b", "R": 8, "M": 1, "N": 1235814400, "variant": "fused",
+         "ms": 10.5574, "params_per_s": 1.1706e11, "bytes_per_param": 56, "GB_s": 6555.2,
+         "frac_of_measured_peak": 0.9772, "l2": "inputs far larger than L2; flushed",
+         "ms_clean_l2": 10.555, "frac_clean_l2": 0.9775},
+        {"workload": "tiny", "R": 4, "M": 2, "N": 65536, "variant": "fused", "ms": 0.0027,
+         "params_per_s": 2.4e10, "bytes_per_param": 48, "GB_s": 1168.9,
+         "frac_of_measured_peak": 0.1743, "l2": "warm: inputs resident"},
+        {"workload": "sweep R=4 S=1048576", "R": 4, "M": 1, "N": 4194304, "variant": "fused",
+         "ms": 0.0355, "params_per_s": 1.18e11, "bytes_per_param": 40, "GB_s": 4731.8,
+         "frac_of_measured_peak": 0.7054, "l2": "inputs far larger than L2; flushed",
+         "ms_clean_l2": 0.0268, "frac_clean_l2": 0.935},
+        {"workload": "llama-3.2-1b", "R": 8, "M": 1, "N": 1235814400, "variant": "clipped",
+         "launches": 2, "ms": 12.3822, "params_per_s": 9.98e10, "bytes_per_param": 64,
+         "GB_s": 6387.6, "frac_of_measured_peak": 0.9523},
+        {"clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 9}},
+        {"workload": "tiny", "oracle_threads": 1, "sample_params": 65536,
+         "params_per_s": 3.6e7, "GB_s": 1.7},
+    ]
+    path = tmp_path / "table.jsonl"
+    path.write_text("".join(json.dumps(r) + "\n" for r in rows) + "not json\n")
+    out = subprocess.run([sys.executable, str(REPO / "bench.py"), "--render-table", str(path)],
+                         capture_output=True, text=True, check=True, cwd=REPO).stdout
+    assert ("| llama-3.2-1b | 8 | 1 | 1,235,814,400 | fused | > L2 | 56 | 10.5574 ms | 117.06 | "
+            "6555.2 | 0.977 | 10.5550 ms | 0.978 |") in out
+    assert "| tiny | 4 | 2 | 65,536 | fused | warm | 48 | 2.70 µs |" in out
+    assert "| 4 | 1,048,576 | 4,194,304 | > L2 | 35.50 µs |" in out and "26.80 µs | 0.935 |" in out
+    assert "| clipped | 2 | 64 | 12.3822 |" in out
+    assert "median 2070 MHz of 2070, throttle reasons: none (9 samples)" in out
+    assert "| tiny | 1 | 36.0 | 1.7 |" in out
