@@ -225,7 +225,10 @@ k_rs_norm(const __grid_constant__ ClipArgs a)
 // (114 registers); 1 unit at 4 or 6, 2 units at 4 and 4 units at 3 blocks
 // per SM measured 0.942-0.948.  The replica tile staged in shared memory
 // and written by R bulk copies (cp.async.bulk, one thread, double-buffered)
-// measured 0.944 against 0.957 for the register stores.
+// measured 0.944 against 0.957 for the register stores.  The streaming cache
+// hints stay: write-back stores for the replicas or for every store cost
+// 0.3-3 %, and L2-only loads (ld.global.cg) 1-1.6 % on the uneven and
+// 4B-shaped workloads.
 constexpr int kAgUnits = 1;
 
 // Warp w reduces slots [1024 w, 1024 (w + 1)) of the 8192: lane l holds
