@@ -265,7 +265,9 @@ def zero_bytes(N: float, P: int, bp: float, bg: float, bo: float):
 
 
 def grad_sumsq(g: np.ndarray) -> float:
-    """Pairwise fp64 sum of squares of a float32 vector (reading R10)."""
+    """Pairwise sum of squares of a float32 vector: fp32 leaves g*g and fp32
+    nodes over the leaves padded with zeros to a power of two, returned
+    widened to double (reading R10)."""
     _check(g, np.float32, None, "g")
     return float(lib().oracle_grad_sumsq(_ptr(g), g.size))
 
