@@ -209,6 +209,15 @@ def test_compressed_step_at_a_persistent_grid_size(kind, ef):
     _run(W.flat(8, 1, 4_000_037, seed=41, step=1, state="synthetic"), kind, ef, [1, 2])
 
 
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("ef", [False, True])
+def test_generic_rank_count_at_a_persistent_grid_size(kind, ef):
+    """(R, M) = (3, 2) has no compile-time case: the run-time path, over
+    enough blocks that every warp of the persistent grid loops, whole vector
+    against the oracle."""
+    _run(W.flat(3, 2, 2_000_003, seed=43, step=1, state="synthetic"), kind, ef, [1, 2])
+
+
 # ------------------------------------------------------------- full size --
 
 def _sample_blocks(wl, plan, seed=777, n_random=160):

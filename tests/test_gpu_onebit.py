@@ -79,6 +79,14 @@ def test_onebit_rank_microbatch_pairs(R, M):
     _run(wl, [1, 2, 3, 4], freeze=1)
 
 
+def test_onebit_generic_rank_count_at_a_persistent_grid_size():
+    """(R, M) = (3, 2), the run-time path, over enough 128-element blocks
+    that every warp of the persistent grid loops; warm-up, then the frozen
+    phase."""
+    _run(_with_align(W.flat(3, 2, 2_000_003, seed=44, step=1, state="synthetic")), [1, 2, 3],
+         freeze=1)
+
+
 def test_onebit_uneven_workload_scaled():
     _run(_with_align(W.uneven().scaled(200_000)), [1, 2, 3], freeze=1)
 

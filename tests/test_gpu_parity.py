@@ -84,6 +84,17 @@ def test_rank_microbatch_pairs(R, M):
         _assert_parity(H.compare(got, want))
 
 
+@pytest.mark.parametrize("R,M", [(3, 1), (5, 3), (6, 1)])
+def test_generic_rank_counts_at_full_size_tiling(R, M):
+    """(R, M) pairs without a compile-time case, at a size where the fused
+    kernel takes its full-size tiling (2-unit tiles, several per persistent
+    block) and every staged grid row loops over many tiles."""
+    wl = W.flat(R, M, 3_000_017, seed=R * 100 + M, step=3)
+    for variant in VARIANTS:
+        _, got, want = _run_both(wl, variant)
+        _assert_parity(H.compare(got, want))
+
+
 @pytest.mark.parametrize("align", [4, 8, 64, 128, 4096])
 def test_shard_alignment_and_empty_shards(align):
     for n, R in ((5, 4), (130, 7), (10_000, 8), (4096 * 3 + 1, 4)):

@@ -61,7 +61,8 @@ def test_zero3_step_matches_oracle(name, target):
 
 
 @pytest.mark.parametrize("n,R,M", [(1, 2, 1), (7, 4, 1), (2049, 3, 1), (4096 * 8, 8, 1),
-                                   (100_003, 7, 1), (100_003, 64, 4), (2049, 1, 256)])
+                                   (100_003, 7, 1), (100_003, 64, 4), (2049, 1, 256),
+                                   (3_000_017, 3, 2)])   # run-time path, full-size tiling
 def test_zero3_step_ragged(n, R, M):
     wl = W.flat(R, M, n, seed=n, step=2)
     plan, ds, shards, (Wz, mz, vz, Ps) = _zero3_run(wl, [2])
