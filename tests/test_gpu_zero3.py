@@ -175,7 +175,8 @@ def _random_units(n, rng, pieces):
 
 @pytest.mark.parametrize("n,R,M,pieces", [(1, 2, 1, 1), (1000, 4, 2, 7), (4099, 7, 4, 30),
                                           (8192, 8, 1, 3), (20_011, 3, 2, 64), (100_003, 8, 1, 9),
-                                          (5003, 64, 4, 5), (2049, 1, 256, 4)])
+                                          (5003, 64, 4, 5), (2049, 1, 256, 4),
+                                          (3_000_017, 3, 2, 5)])   # run-time path, many waves
 def test_unit_reduce_scatter_then_update_matches_oracle(n, R, M, pieces):
     """Random units (any start, so the fp32 shard stores take both the
     vector and the scalar path) in shuffled order, each unit's gradient in
