@@ -354,8 +354,9 @@ def test_zero_emulation_oracle_agrees_with_gpu():
 
 
 @pytest.mark.parametrize("mode", ["zero_copy", "copy_engine"])
-def test_step_from_host_buffers(mode):
-    wl = W.llama32_1b().scaled(100_000)
+@pytest.mark.parametrize("target", [100_000, 3_000_000])   # small-vector path, full-size tiling
+def test_step_from_host_buffers(mode, target):
+    wl = W.llama32_1b().scaled(target)
     G, W0, m0, v0 = H.host_inputs(wl, wl.step)
     want = H.oracle_run(wl, {wl.step: G}, W0, m0, v0, [wl.step])
     ds = H.DeviceState(wl)
