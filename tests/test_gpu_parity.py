@@ -214,7 +214,9 @@ def test_guard_bands_and_padding_untouched():
 
 
 @pytest.mark.parametrize("name,target", [("uneven", 250_003), ("llama-3.2-1b", 400_000),
-                                         ("tiny", 65_536)])
+                                         ("tiny", 65_536),
+                                         # many tiles per block in every staged grid row
+                                         ("uneven", 3_000_017), ("llama-3.2-1b", 6_000_000)])
 def test_staged_zero2_without_scratch_matches_oracle(name, target):
     """ZeRO-2 gives up the gradients once reduced: the staged step without
     scratch keeps the fp32 reduced gradient in gradient buffers 0 and 1 and
