@@ -231,7 +231,11 @@ k_rs_norm(const __grid_constant__ ClipArgs a)
 // 4B-shaped workloads.  8 consecutive elements a thread, taken as two
 // 4-element halves to keep the registers of this loop, with one 16-byte
 // store per replica (a third fewer store instructions) measured 0.74-0.78:
-// each half's loads use every other 16 bytes of the lines they touch.
+// each half's loads use every other 16 bytes of the lines they touch.  Lanes
+// 2i and 2i+1 swapping their packed values by a shuffle, each then storing 8
+// elements to half of the replicas (half the replica store instructions, the
+// loads unchanged), measured the same as this within 0.2 %: the pass is bound
+// by the DRAM's handling of its write-heavy mix, not by its store issue.
 constexpr int kAgUnits = 1;
 
 // Warp w reduces slots [1024 w, 1024 (w + 1)) of the 8192: lane l holds
